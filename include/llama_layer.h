@@ -1,0 +1,184 @@
+/*
+ * llama_layer.h -- C ABI of the GB300 (sm_103a) forward pass of one
+ * Llama-style decoder layer.
+ *
+ * The operator chain follows the page "Which ops-transformer operators one
+ * Llama2-7B layer calls" (seekfood.cn/news/1207529), section "single-layer
+ * operator call chain": x -> RMSNorm -> merged Q/K/V Linear -> RotaryEmbedding
+ * -> Self-Attention (GQA) -> Attention Output Linear -> residual -> RMSNorm ->
+ * merged Gate/Up Linear -> SiLU * up -> Down Linear -> residual.  Prefill and
+ * decode take different attention kernels (same page, section "KV Cache and
+ * the operators").  The KV cache is paged as on the page "ATB KV-cache paging,
+ * quantisation, speculative decoding and communication overlap"
+ * (hwcomputing.csdn.net), section "KV Cache memory wall": fixed-size blocks,
+ * a block_table from logical to physical blocks, contextLens per request, and
+ * ReshapeAndCache writing each step's K/V into its slot.
+ *
+ * Conventions shared by every call
+ *  - All tensor pointers are DEVICE pointers, caller-owned, row-major, and
+ *    16-byte aligned.  BF16 is IEEE bfloat16 (2 bytes); gains are float32.
+ *  - Every call is asynchronous on `stream` (a cudaStream_t, NULL = legacy
+ *    default stream).  No call allocates device memory, synchronises, or
+ *    keeps a pointer after it returns, except ll_pack_weights (see there).
+ *  - The return value reports what the host can check before launching
+ *    (LL_OK or an LL_ERR_* code; nothing is launched on error).  Problems
+ *    only the device can see (a block_table entry or slot out of range, a
+ *    position beyond the RoPE table) are OR-ed as LL_DEV_* bits into
+ *    `*status`, a caller-owned device int32 that the caller zeroes and reads
+ *    after synchronising.  The offending row is skipped; kernels never trap.
+ *  - Every bounded wait inside a kernel gives up after about two seconds,
+ *    sets LL_DEV_TIMEOUT and lets the kernel finish.
+ *  - The KV pool is two tensors, K and V, each BF16
+ *    [num_blocks, n_kv_heads, block_size, head_dim] ("BNSD" inside a block, as
+ *    the 910B layout on the paging page).  Slot s = block * block_size + offset.
+ *  - block_table is int32 [batch, max_blocks]; entry j is the physical block
+ *    holding positions j*block_size .. (j+1)*block_size-1 of that sequence.
+ */
+#ifndef LLAMA_LAYER_H
+#define LLAMA_LAYER_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* host-detectable errors (return values) */
+#define LL_OK 0
+#define LL_ERR_INVALID_ARG 1   /* null pointer, non-positive or inconsistent size */
+#define LL_ERR_UNSUPPORTED 2   /* shape outside what the kernels implement */
+#define LL_ERR_WORKSPACE 3     /* workspace missing or smaller than required */
+#define LL_ERR_CUDA 4          /* a CUDA runtime/driver call failed */
+
+/* device-detected problems (bits OR-ed into *status) */
+#define LL_DEV_BAD_BLOCK 1     /* block_table entry < 0 or >= num_blocks where a block was needed */
+#define LL_DEV_BAD_SLOT 2      /* slot_mapping entry >= num_blocks * block_size */
+#define LL_DEV_BAD_POSITION 4  /* position < 0 or >= max_position, or context_len out of range */
+#define LL_DEV_TIMEOUT 8       /* a bounded in-kernel wait gave up */
+
+/* Layer shape.  head_dim must be 64 or 128; n_heads % n_kv_heads == 0;
+ * hidden and intermediate multiples of 16 (>= 64); block_size a power of two
+ * in [16, 256]; max_position = rows of the RoPE table (largest position + 1).
+ * RoPE uses half-split pairs and angle pos * rope_theta^(-2i/head_dim). */
+typedef struct {
+    int32_t hidden;
+    int32_t n_heads;
+    int32_t n_kv_heads;
+    int32_t head_dim;
+    int32_t intermediate;
+    int32_t block_size;
+    int32_t max_position;
+    float rms_eps;
+    float rope_theta;
+} ll_config;
+
+/* Canonical weights as a model stores them, all BF16 [out, in] row-major:
+ * w_qkv [(n_heads + 2 n_kv_heads) head_dim, hidden], rows = Q heads, then K
+ * heads, then V heads (the merged QKV MatMul of the chain page);
+ * w_o [hidden, n_heads head_dim]; w_gate and w_up [intermediate, hidden];
+ * w_down [hidden, intermediate]; g_attn and g_ffn float32 [hidden]. */
+typedef struct {
+    const void* w_qkv;
+    const void* w_o;
+    const void* w_gate;
+    const void* w_up;
+    const void* w_down;
+    const float* g_attn;
+    const float* g_ffn;
+} ll_weights;
+
+typedef struct {
+    void* k;              /* BF16 [num_blocks, n_kv_heads, block_size, head_dim] */
+    void* v;              /* same shape */
+    int32_t num_blocks;
+} ll_kv_pool;
+
+/* Human-readable name of an LL_ERR_* code (static string). */
+const char* ll_strerror(int code);
+
+/* Bytes of the packed-weight buffer for `cfg` (0 if cfg is invalid). */
+size_t ll_packed_weights_size(const ll_config* cfg);
+
+/* Lays out the weights the way the kernels read them, into the caller-owned
+ * device buffer `packed` (ll_packed_weights_size bytes): Q/K head rows
+ * reordered so that each RoPE pair is adjacent, gate and up rows interleaved
+ * (the MergedMatMul(GateUp) of the chain page), the other weights copied, and
+ * a float32 cos/sin table for max_position positions computed in float64.
+ * The canonical weights may be freed once the stream has passed this call.
+ * Setup-time call: it synchronises `stream` before returning. */
+int ll_pack_weights(const ll_config* cfg, const ll_weights* w, void* packed, size_t packed_bytes,
+                    void* stream);
+
+/* Workspace bytes for layer calls of up to max_tokens tokens (prefill: batch *
+ * seq_len; decode: batch) and block tables up to max_blocks wide. */
+size_t ll_workspace_size(const ll_config* cfg, int32_t max_tokens, int32_t max_blocks);
+
+/* Prefill: x BF16 [batch*seq_len, hidden], token-major; token t belongs to
+ * sequence t / seq_len and sits at positions[t] (int32 [batch*seq_len]).
+ * Writes every token's K and V (after RoPE on K) into the pool at
+ * block_table[seq][pos / block_size], offset pos % block_size; then every
+ * query at position p attends (causally, GQA) over cache positions 0..p of
+ * its sequence, which therefore must already be cached below this call's
+ * first position (chunked prefill).  Writes y BF16 [batch*seq_len, hidden];
+ * y must not alias x.  The chain page's prefill path. */
+int ll_layer_prefill(const ll_config* cfg, const void* packed, const void* x,
+                     const int32_t* positions, int32_t batch, int32_t seq_len,
+                     const ll_kv_pool* pool, const int32_t* block_table, int32_t max_blocks,
+                     void* y, void* workspace, size_t workspace_bytes, int32_t* status,
+                     void* stream);
+
+/* Decode step: x BF16 [batch, hidden], one new token per sequence.
+ * context_lens (int32 [batch]) counts each sequence's cache INCLUDING the new
+ * token, which is written at position context_lens[b] - 1; its query attends
+ * over positions 0..context_lens[b]-1.  y BF16 [batch, hidden].  The chain
+ * page's decode path (one-row query against the cached K/V); batch <= 256. */
+int ll_layer_decode_step(const ll_config* cfg, const void* packed, const void* x,
+                         const ll_kv_pool* pool, const int32_t* block_table, int32_t max_blocks,
+                         const int32_t* context_lens, int32_t batch, void* y, void* workspace,
+                         size_t workspace_bytes, int32_t* status, void* stream);
+
+/* ReshapeAndCache (paging page, section "KV Cache memory wall",
+ * ReshapeAndCacheOperation): k, v BF16 [tokens, n_kv_heads, head_dim];
+ * slot_mapping int32 [tokens]; token t's rows go to
+ * pool[slot / block_size, :, slot % block_size, :].  slot -1 skips the token;
+ * slot >= num_blocks*block_size sets LL_DEV_BAD_SLOT and skips it.  Bit-exact
+ * copy.  head_dim a multiple of 8. */
+int ll_reshape_and_cache(const void* k, const void* v, const int32_t* slot_mapping, int32_t tokens,
+                         int32_t n_kv_heads, int32_t head_dim, int32_t block_size,
+                         const ll_kv_pool* pool, int32_t* status, void* stream);
+
+/* Workspace bytes for ll_paged_attention_decode. */
+size_t ll_attention_workspace_size(int32_t batch, int32_t n_heads, int32_t head_dim,
+                                   int32_t max_blocks, int32_t block_size);
+
+/* Decode attention over the paged cache (chain page, section "KV Cache and
+ * the operators", flash_attention_decode; paging page PagedAttentionOperation):
+ * q BF16 [batch, n_heads, head_dim]; sequence b's query head h attends over
+ * positions 0..context_lens[b]-1 of KV head h / (n_heads / n_kv_heads) with
+ * softmax(q k^T * scale).  out BF16 [batch, n_heads, head_dim]. */
+int ll_paged_attention_decode(const void* q, const ll_kv_pool* pool, const int32_t* block_table,
+                              int32_t max_blocks, const int32_t* context_lens, int32_t batch,
+                              int32_t n_heads, int32_t n_kv_heads, int32_t head_dim,
+                              int32_t block_size, float scale, void* out, void* workspace,
+                              size_t workspace_bytes, int32_t* status, void* stream);
+
+/* Workspace bytes for ll_linear. */
+size_t ll_linear_workspace_size(int32_t m, int32_t n, int32_t k);
+
+/* Plain Linear y = x w^T (the chain page's Q/K/V, Output, Gate/Up and Down
+ * Linear without their fused epilogues): x BF16 [m, k], w BF16 [n, k],
+ * y BF16 [m, n], float32 accumulation.  n and k multiples of 16.  Runs the
+ * same tensor-core GEMM the layer uses (m <= 256 takes the decode form). */
+int ll_linear(const void* x, const void* w, void* y, int32_t m, int32_t n, int32_t k,
+              void* workspace, size_t workspace_bytes, int32_t* status, void* stream);
+
+/* Number of streaming multiprocessors the library sizes its grids for
+ * (queried once per device), or -1 without a device. */
+int ll_device_sm_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LLAMA_LAYER_H */

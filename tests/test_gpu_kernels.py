@@ -1,0 +1,185 @@
+"""GPU parity of each C-ABI entry point against the CPU oracle, on small and
+ragged shapes that still span several tiles."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import llama_layer as O
+from tests.helpers import assert_close, bits, f64
+from transformer_decoder_layer_llama_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+if torch.cuda.is_available():
+    from transformer_decoder_layer_llama_gb300 import api
+DEV = "cuda"
+
+
+# ---------------------------------------------------------------- Linear (the tensor-core GEMM)
+
+@pytest.mark.parametrize("m,n,k", [
+    (1, 128, 64), (2, 512, 256), (16, 1376, 688), (64, 4096, 4096), (33, 11008, 4096),
+    (64, 4096, 11008),                                   # weight form, split K
+    (65, 256, 128), (128, 512, 256), (300, 1376, 688), (2048, 4096, 4096), (257, 12288, 4096),
+])
+def test_linear_matches_float64_matmul(m, n, k):
+    x = synth.normal_bf16((m, k), 1.0, seed=m * 7 + 1)
+    w = synth.normal_bf16((n, k), 0.02, seed=n * 3 + k)
+    y = api.linear(x.to(DEV), w.to(DEV))
+    torch.cuda.synchronize()
+    ref = f64(x) @ f64(w).T
+    # BF16 output rounding (2^-9 relative) plus float32 accumulation order
+    assert_close(f64(y), ref, f"linear {m}x{n}x{k}", atol=2e-3, rtol=8e-3)
+
+
+def test_linear_twice_same_buffers_is_repeatable():
+    x = synth.normal_bf16((64, 4096), 1.0, seed=1).to(DEV)
+    w = synth.normal_bf16((4096, 4096), 0.02, seed=2).to(DEV)
+    ws = torch.empty(api.lib.ll_linear_workspace_size(64, 4096, 4096), dtype=torch.uint8, device=DEV)
+    y1 = api.linear(x, w, workspace=ws)
+    y2 = api.linear(x, w, workspace=ws)
+    torch.cuda.synchronize()
+    assert torch.equal(y1, y2)
+
+
+# ---------------------------------------------------------------- ReshapeAndCache
+
+@pytest.mark.parametrize("T,Hkv,d,bs,nb", [(37, 2, 64, 16, 8), (300, 8, 128, 128, 5), (1, 32, 128, 128, 2)])
+def test_reshape_and_cache_bit_exact(T, Hkv, d, bs, nb):
+    dims = synth.LayerDims(Hkv * d, Hkv, Hkv, d, 64, bs)
+    k = synth.normal_bf16((T, Hkv, d), 1.0, seed=T + 1)
+    v = synth.normal_bf16((T, Hkv, d), 1.0, seed=T + 2)
+    slots = synth.make_slot_mapping(T, nb * bs, seed=T + 3, n_skip=min(3, T - 1))
+    kp, vp = synth.make_pool(nb, dims, 0, fill="sentinel")
+    kpd, vpd = kp.to(DEV), vp.to(DEV)
+    st = api.reshape_and_cache(k.to(DEV), v.to(DEV), slots.to(DEV), kpd, vpd)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    ko, vo = bits(kp), bits(vp)
+    O.reshape_and_cache(f64(k), f64(v), slots.numpy(), ko, vo)
+    np.testing.assert_array_equal(bits(kpd), ko)
+    np.testing.assert_array_equal(bits(vpd), vo)
+
+
+def test_reshape_and_cache_flags_out_of_range_slot():
+    dims = synth.LayerDims(128, 2, 2, 64, 64, 16)
+    k = synth.normal_bf16((4, 2, 64), 1.0, seed=1)
+    slots = torch.tensor([0, 5, 10_000, -1], dtype=torch.int32)
+    kp, vp = synth.make_pool(4, dims, 0, fill="sentinel")
+    kpd, vpd = kp.to(DEV), vp.to(DEV)
+    st = api.reshape_and_cache(k.to(DEV), k.to(DEV), slots.to(DEV), kpd, vpd)
+    torch.cuda.synchronize()
+    assert int(st.item()) == api.LL_DEV_BAD_SLOT
+    ko, vo = bits(kp), bits(vp)
+    O.reshape_and_cache(f64(k), f64(k), [0, 5, -1, -1], ko, vo)   # the bad one is skipped
+    np.testing.assert_array_equal(bits(kpd), ko)
+
+
+# ---------------------------------------------------------------- paged decode attention
+
+@pytest.mark.parametrize("B,Hq,Hkv,d,bs,ctx_lo,ctx_hi", [
+    (2, 4, 2, 64, 16, 1, 80),           # tiny GQA layer shape
+    (5, 8, 8, 128, 128, 1, 300),        # MHA, ragged
+    (3, 16, 2, 128, 128, 900, 3100),    # GQA 8, several 1024-key splits
+    (4, 4, 4, 64, 32, 1023, 1026),      # split boundaries
+])
+def test_paged_attention_decode(B, Hq, Hkv, d, bs, ctx_lo, ctx_hi):
+    dims = synth.LayerDims(Hq * d, Hq, Hkv, d, 64, bs)
+    ctx = synth.make_context_lens(B, ctx_lo, ctx_hi, seed=B * 11)
+    ctx[0] = ctx_lo
+    table, nb = synth.make_block_table(ctx.tolist(), bs, seed=B * 13, extra_blocks=3)
+    kp, vp = synth.make_pool(nb, dims, seed=B * 17)
+    q = synth.normal_bf16((B, Hq, d), 1.0, seed=B * 19)
+    scale = 1 / math.sqrt(d)
+    out = api.paged_attention_decode(q.to(DEV), kp.to(DEV), vp.to(DEV), table.to(DEV), ctx.to(DEV), scale)
+    torch.cuda.synchronize()
+    ref = O.paged_attention_decode(f64(q), bits(kp), bits(vp), table.numpy(), ctx.numpy(), scale)
+    assert_close(f64(out), ref, "paged_attention_decode")
+
+
+# ---------------------------------------------------------------- whole layer, tiny GQA workload
+
+def _tiny_setup(seed=1, S=None, B=None, steps=8):
+    wl = synth.WORKLOADS["tiny_gqa"]
+    d = wl.dims
+    B = B or wl.batch
+    S = S or wl.prefill_len
+    W = synth.make_weights(d, wl.w_std, seed=seed)
+    table, nb = synth.make_block_table([S + steps] * B, d.block_size, seed=seed + 3, extra_blocks=3)
+    kp, vp = synth.make_pool(nb, d, seed=seed + 4, fill="sentinel")
+    cfg = api.make_config(d, max_position=S + steps + 1)
+    packed = api.pack_weights(cfg, {k: v.to(DEV) for k, v in W.items()})
+    Wn = {k: f64(v) for k, v in W.items()}
+    return wl, d, B, S, W, Wn, table, kp, vp, cfg, packed
+
+
+def test_tiny_layer_prefill_then_decode_steps():
+    wl, d, B, S, W, Wn, table, kp, vp, cfg, packed = _tiny_setup()
+    x = synth.make_x(B * S, d.hidden, seed=21)
+    pos = synth.prefill_positions(B, S)
+    kpd, vpd, td = kp.to(DEV), vp.to(DEV), table.to(DEV)
+    status = api.new_status()
+    y = api.layer_prefill(cfg, packed, x.to(DEV), pos.to(DEV), B, S, kpd, vpd, td, status=status)
+    torch.cuda.synchronize()
+    ko, vo = bits(kp), bits(vp)
+    want = {}
+    y_ref = O.layer_prefill(d, Wn, f64(x), pos.numpy(), B, S, ko, vo, table.numpy(), want=want)
+    assert int(status.item()) == 0
+    assert_close(f64(y), y_ref, "prefill y")
+    # the same slots were written (others keep the sentinel), values within BF16 tolerance
+    kg, vg = bits(kpd), bits(vpd)
+    sentinel = 0xC480
+    np.testing.assert_array_equal(kg == sentinel, ko == sentinel)
+    assert_close(O.bf16_value(kg), O.bf16_value(ko), "K cache")
+    assert_close(O.bf16_value(vg), O.bf16_value(vo), "V cache")
+    for step in range(wl.decode_steps):
+        xd = synth.make_x(B, d.hidden, seed=100 + step)
+        ctx = torch.full((B,), S + step + 1, dtype=torch.int32)
+        yd = api.layer_decode_step(cfg, packed, xd.to(DEV), kpd, vpd, td, ctx.to(DEV), status=status)
+        torch.cuda.synchronize()
+        yd_ref = O.layer_decode_step(d, Wn, f64(xd), ko, vo, table.numpy(), ctx.numpy())
+        assert int(status.item()) == 0
+        assert_close(f64(yd), yd_ref, f"decode step {step}")
+
+
+@pytest.mark.parametrize("B,S", [(3, 17), (1, 130), (2, 1), (1, 200)])
+def test_tiny_layer_ragged_prefill(B, S):
+    wl, d, B, S, W, Wn, table, kp, vp, cfg, packed = _tiny_setup(seed=5, S=S, B=B, steps=0)
+    x = synth.make_x(B * S, d.hidden, seed=31)
+    pos = synth.prefill_positions(B, S)
+    kpd, vpd = kp.to(DEV), vp.to(DEV)
+    y = api.layer_prefill(cfg, packed, x.to(DEV), pos.to(DEV), B, S, kpd, vpd, table.to(DEV))
+    torch.cuda.synchronize()
+    ko, vo = bits(kp), bits(vp)
+    y_ref = O.layer_prefill(d, Wn, f64(x), pos.numpy(), B, S, ko, vo, table.numpy())
+    assert_close(f64(y), y_ref, f"prefill B{B} S{S}")
+
+
+def test_chunked_prefill_attends_to_cached_prefix():
+    wl, d, B, S, W, Wn, table, kp, vp, cfg, packed = _tiny_setup(seed=7, S=64, B=2, steps=40)
+    kpd, vpd, td = kp.to(DEV), vp.to(DEV), table.to(DEV)
+    ko, vo = bits(kp), bits(vp)
+    for start, n in ((0, 64), (64, 40)):
+        x = synth.make_x(B * n, d.hidden, seed=41 + start)
+        pos = synth.prefill_positions(B, n, start=start)
+        y = api.layer_prefill(cfg, packed, x.to(DEV), pos.to(DEV), B, n, kpd, vpd, td)
+        torch.cuda.synchronize()
+        y_ref = O.layer_prefill(d, Wn, f64(x), pos.numpy(), B, n, ko, vo, table.numpy())
+        assert_close(f64(y), y_ref, f"chunk at {start}")
+
+
+def test_bad_block_table_sets_status_without_fault():
+    wl, d, B, S, W, Wn, table, kp, vp, cfg, packed = _tiny_setup(seed=9, S=32, B=2, steps=1)
+    bad = table.clone()
+    bad[1, 0] = 10_000        # beyond the pool
+    bad[0, 1] = -1            # a hole inside the context
+    x = synth.make_x(B * 32, d.hidden, seed=51)
+    pos = synth.prefill_positions(B, 32)
+    status = api.new_status()
+    y = api.layer_prefill(cfg, packed, x.to(DEV), pos.to(DEV), B, 32, kp.to(DEV), vp.to(DEV),
+                          bad.to(DEV), status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) & api.LL_DEV_BAD_BLOCK
+    assert torch.isfinite(y.float()).all()

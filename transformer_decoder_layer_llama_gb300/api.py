@@ -1,0 +1,281 @@
+"""ctypes binding of libllamalayer.so (include/llama_layer.h), names as in the C ABI.
+
+Argument marshalling only: tensors are checked for device, dtype, shape and
+contiguity, then their device pointers go to the library; every step of the
+layer runs in the library's CUDA kernels.  Importing this module loads the
+library and fails loudly if it has not been built (there is no fallback).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from .build import LIB_PATH
+
+LL_OK = 0
+LL_ERR_INVALID_ARG = 1
+LL_ERR_UNSUPPORTED = 2
+LL_ERR_WORKSPACE = 3
+LL_ERR_CUDA = 4
+
+LL_DEV_BAD_BLOCK = 1
+LL_DEV_BAD_SLOT = 2
+LL_DEV_BAD_POSITION = 4
+LL_DEV_TIMEOUT = 8
+
+EXPORTED = [
+    "ll_strerror", "ll_packed_weights_size", "ll_pack_weights", "ll_workspace_size",
+    "ll_layer_prefill", "ll_layer_decode_step", "ll_reshape_and_cache",
+    "ll_attention_workspace_size", "ll_paged_attention_decode", "ll_linear_workspace_size",
+    "ll_linear", "ll_device_sm_count",
+]
+
+
+class ll_config(ctypes.Structure):
+    _fields_ = [("hidden", ctypes.c_int32), ("n_heads", ctypes.c_int32),
+                ("n_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
+                ("intermediate", ctypes.c_int32), ("block_size", ctypes.c_int32),
+                ("max_position", ctypes.c_int32), ("rms_eps", ctypes.c_float),
+                ("rope_theta", ctypes.c_float)]
+
+
+class ll_weights(ctypes.Structure):
+    _fields_ = [("w_qkv", ctypes.c_void_p), ("w_o", ctypes.c_void_p), ("w_gate", ctypes.c_void_p),
+                ("w_up", ctypes.c_void_p), ("w_down", ctypes.c_void_p),
+                ("g_attn", ctypes.c_void_p), ("g_ffn", ctypes.c_void_p)]
+
+
+class ll_kv_pool(ctypes.Structure):
+    _fields_ = [("k", ctypes.c_void_p), ("v", ctypes.c_void_p), ("num_blocks", ctypes.c_int32)]
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"{LIB_PATH} is missing: build it first "
+                          "(python -c 'import __graft_entry__ as g; g.build()')")
+    lib = ctypes.CDLL(LIB_PATH)
+    P, S, I32 = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int32
+    cfgp = ctypes.POINTER(ll_config)
+    poolp = ctypes.POINTER(ll_kv_pool)
+    sig = {
+        "ll_strerror": (ctypes.c_char_p, [ctypes.c_int]),
+        "ll_packed_weights_size": (S, [cfgp]),
+        "ll_pack_weights": (ctypes.c_int, [cfgp, ctypes.POINTER(ll_weights), P, S, P]),
+        "ll_workspace_size": (S, [cfgp, I32, I32]),
+        "ll_layer_prefill": (ctypes.c_int, [cfgp, P, P, P, I32, I32, poolp, P, I32, P, P, S, P, P]),
+        "ll_layer_decode_step": (ctypes.c_int, [cfgp, P, P, poolp, P, I32, P, I32, P, P, S, P, P]),
+        "ll_reshape_and_cache": (ctypes.c_int, [P, P, P, I32, I32, I32, I32, poolp, P, P]),
+        "ll_attention_workspace_size": (S, [I32, I32, I32, I32, I32]),
+        "ll_paged_attention_decode": (ctypes.c_int, [P, poolp, P, I32, P, I32, I32, I32, I32, I32,
+                                                     ctypes.c_float, P, P, S, P, P]),
+        "ll_linear_workspace_size": (S, [I32, I32, I32]),
+        "ll_linear": (ctypes.c_int, [P, P, P, I32, I32, I32, P, S, P, P]),
+        "ll_device_sm_count": (ctypes.c_int, []),
+    }
+    for name, (res, args) in sig.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    return lib
+
+
+lib = _load()
+
+
+class LayerError(RuntimeError):
+    def __init__(self, name, code):
+        super().__init__(f"{name}: {lib.ll_strerror(code).decode()} (code {code})")
+        self.code = code
+
+
+def _check(name, rc):
+    if rc != LL_OK:
+        raise LayerError(name, rc)
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(0)
+
+
+def _stream(stream):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _need(t, name, dtype, device=True, shape=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if device and not t.is_cuda:
+        raise ValueError(f"{name} must live on the GPU")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+
+
+def make_config(dims, max_position: int) -> ll_config:
+    """ll_config from any object with the layer's dimension attributes."""
+    return ll_config(dims.hidden, dims.n_heads, dims.n_kv_heads, dims.head_dim, dims.intermediate,
+                     dims.block_size, int(max_position), float(dims.rms_eps), float(dims.rope_theta))
+
+
+def new_status(device=None):
+    return torch.zeros(1, dtype=torch.int32, device=device or "cuda")
+
+
+def packed_weights_size(cfg: ll_config) -> int:
+    return lib.ll_packed_weights_size(ctypes.byref(cfg))
+
+
+def pack_weights(cfg: ll_config, W: dict, stream=None) -> torch.Tensor:
+    """Packs canonical weights (dict of CUDA tensors, see include/llama_layer.h) into a new
+    uint8 CUDA buffer and returns it."""
+    H, I, d = cfg.hidden, cfg.intermediate, cfg.head_dim
+    _need(W["w_qkv"], "w_qkv", torch.bfloat16, shape=((cfg.n_heads + 2 * cfg.n_kv_heads) * d, H))
+    _need(W["w_o"], "w_o", torch.bfloat16, shape=(H, cfg.n_heads * d))
+    _need(W["w_gate"], "w_gate", torch.bfloat16, shape=(I, H))
+    _need(W["w_up"], "w_up", torch.bfloat16, shape=(I, H))
+    _need(W["w_down"], "w_down", torch.bfloat16, shape=(H, I))
+    _need(W["g_attn"], "g_attn", torch.float32, shape=(H,))
+    _need(W["g_ffn"], "g_ffn", torch.float32, shape=(H,))
+    n = packed_weights_size(cfg)
+    if n == 0:
+        raise LayerError("ll_packed_weights_size", LL_ERR_UNSUPPORTED)
+    packed = torch.empty(n, dtype=torch.uint8, device=W["w_qkv"].device)
+    w = ll_weights(W["w_qkv"].data_ptr(), W["w_o"].data_ptr(), W["w_gate"].data_ptr(),
+                   W["w_up"].data_ptr(), W["w_down"].data_ptr(), W["g_attn"].data_ptr(),
+                   W["g_ffn"].data_ptr())
+    _check("ll_pack_weights", lib.ll_pack_weights(ctypes.byref(cfg), ctypes.byref(w), _ptr(packed),
+                                                  n, _stream(stream)))
+    return packed
+
+
+def workspace_size(cfg: ll_config, max_tokens: int, max_blocks: int) -> int:
+    return lib.ll_workspace_size(ctypes.byref(cfg), int(max_tokens), int(max_blocks))
+
+
+def new_workspace(cfg, max_tokens, max_blocks, device=None):
+    n = workspace_size(cfg, max_tokens, max_blocks)
+    if n == 0:
+        raise LayerError("ll_workspace_size", LL_ERR_INVALID_ARG)
+    return torch.empty(n, dtype=torch.uint8, device=device or "cuda")
+
+
+def _pool(k_pool, v_pool):
+    _need(k_pool, "k_pool", torch.bfloat16)
+    _need(v_pool, "v_pool", torch.bfloat16)
+    if k_pool.shape != v_pool.shape or k_pool.dim() != 4:
+        raise ValueError("k_pool and v_pool must both be [num_blocks, n_kv_heads, block_size, head_dim]")
+    return ll_kv_pool(k_pool.data_ptr(), v_pool.data_ptr(), k_pool.shape[0])
+
+
+def layer_prefill(cfg, packed, x, positions, batch, seq_len, k_pool, v_pool, block_table,
+                  y=None, workspace=None, status=None, stream=None):
+    """ll_layer_prefill.  Returns y (BF16 [batch*seq_len, hidden])."""
+    T = int(batch) * int(seq_len)
+    _need(x, "x", torch.bfloat16, shape=(T, cfg.hidden))
+    _need(positions, "positions", torch.int32, shape=(T,))
+    _need(block_table, "block_table", torch.int32)
+    if block_table.dim() != 2 or block_table.shape[0] < batch:
+        raise ValueError("block_table must be [batch, max_blocks]")
+    pool = _pool(k_pool, v_pool)
+    if y is None:
+        y = torch.empty_like(x)
+    if workspace is None:
+        workspace = new_workspace(cfg, T, block_table.shape[1], x.device)
+    if status is None:
+        status = new_status(x.device)
+    _check("ll_layer_prefill", lib.ll_layer_prefill(
+        ctypes.byref(cfg), _ptr(packed), _ptr(x), _ptr(positions), int(batch), int(seq_len),
+        ctypes.byref(pool), _ptr(block_table), block_table.shape[1], _ptr(y), _ptr(workspace),
+        workspace.numel(), _ptr(status), _stream(stream)))
+    return y
+
+
+def layer_decode_step(cfg, packed, x, k_pool, v_pool, block_table, context_lens, y=None,
+                      workspace=None, status=None, stream=None):
+    """ll_layer_decode_step.  Returns y (BF16 [batch, hidden])."""
+    B = x.shape[0]
+    _need(x, "x", torch.bfloat16, shape=(B, cfg.hidden))
+    _need(context_lens, "context_lens", torch.int32, shape=(B,))
+    _need(block_table, "block_table", torch.int32)
+    if block_table.dim() != 2 or block_table.shape[0] < B:
+        raise ValueError("block_table must be [batch, max_blocks]")
+    pool = _pool(k_pool, v_pool)
+    if y is None:
+        y = torch.empty_like(x)
+    if workspace is None:
+        workspace = new_workspace(cfg, B, block_table.shape[1], x.device)
+    if status is None:
+        status = new_status(x.device)
+    _check("ll_layer_decode_step", lib.ll_layer_decode_step(
+        ctypes.byref(cfg), _ptr(packed), _ptr(x), ctypes.byref(pool), _ptr(block_table),
+        block_table.shape[1], _ptr(context_lens), B, _ptr(y), _ptr(workspace), workspace.numel(),
+        _ptr(status), _stream(stream)))
+    return y
+
+
+def reshape_and_cache(k, v, slot_mapping, k_pool, v_pool, status=None, stream=None):
+    """ll_reshape_and_cache: k, v BF16 [tokens, n_kv_heads, head_dim]."""
+    _need(k, "k", torch.bfloat16)
+    _need(v, "v", torch.bfloat16, shape=tuple(k.shape))
+    T, Hkv, d = k.shape
+    _need(slot_mapping, "slot_mapping", torch.int32, shape=(T,))
+    pool = _pool(k_pool, v_pool)
+    if status is None:
+        status = new_status(k.device)
+    _check("ll_reshape_and_cache", lib.ll_reshape_and_cache(
+        _ptr(k), _ptr(v), _ptr(slot_mapping), T, Hkv, d, k_pool.shape[2], ctypes.byref(pool),
+        _ptr(status), _stream(stream)))
+    return status
+
+
+def attention_workspace_size(batch, n_heads, head_dim, max_blocks, block_size):
+    return lib.ll_attention_workspace_size(batch, n_heads, head_dim, max_blocks, block_size)
+
+
+def paged_attention_decode(q, k_pool, v_pool, block_table, context_lens, scale, out=None,
+                           workspace=None, status=None, stream=None):
+    """ll_paged_attention_decode: q BF16 [batch, n_heads, head_dim]."""
+    _need(q, "q", torch.bfloat16)
+    B, Hq, d = q.shape
+    _need(block_table, "block_table", torch.int32)
+    _need(context_lens, "context_lens", torch.int32, shape=(B,))
+    pool = _pool(k_pool, v_pool)
+    bs = k_pool.shape[2]
+    if out is None:
+        out = torch.empty_like(q)
+    if workspace is None:
+        n = attention_workspace_size(B, Hq, d, block_table.shape[1], bs)
+        workspace = torch.empty(max(n, 1), dtype=torch.uint8, device=q.device)
+    if status is None:
+        status = new_status(q.device)
+    _check("ll_paged_attention_decode", lib.ll_paged_attention_decode(
+        _ptr(q), ctypes.byref(pool), _ptr(block_table), block_table.shape[1], _ptr(context_lens), B,
+        Hq, k_pool.shape[1], d, bs, float(scale), _ptr(out), _ptr(workspace), workspace.numel(),
+        _ptr(status), _stream(stream)))
+    return out
+
+
+def linear(x, w, y=None, workspace=None, status=None, stream=None):
+    """ll_linear: y = x w^T, x BF16 [m, k], w BF16 [n, k]."""
+    _need(x, "x", torch.bfloat16)
+    _need(w, "w", torch.bfloat16)
+    m, k = x.shape
+    n = w.shape[0]
+    if w.shape[1] != k:
+        raise ValueError("w must be [n, k]")
+    if y is None:
+        y = torch.empty(m, n, dtype=torch.bfloat16, device=x.device)
+    if workspace is None:
+        workspace = torch.empty(lib.ll_linear_workspace_size(m, n, k), dtype=torch.uint8,
+                                device=x.device)
+    if status is None:
+        status = new_status(x.device)
+    _check("ll_linear", lib.ll_linear(_ptr(x), _ptr(w), _ptr(y), m, n, k, _ptr(workspace),
+                                      workspace.numel(), _ptr(status), _stream(stream)))
+    return y

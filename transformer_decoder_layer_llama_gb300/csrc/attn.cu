@@ -1,0 +1,570 @@
+// Attention over the paged KV cache: the prefill (FlashAttention) and the
+// decode (flash_attention_decode) variants of the Llama2-7B operator chain
+// (page "Which ops-transformer operators one Llama2-7B layer calls", sections
+// "single-layer operator call chain" and "KV Cache and the operators").
+//
+// Both read K/V through block_table from the pool [num_blocks, n_kv_heads,
+// block_size, head_dim] (paging page, section "KV Cache memory wall"), never
+// materialise the score matrix, and keep a running max / denominator per
+// query row (online softmax, exp2 with the scale folded into log2 e).
+// Query head h reads KV head h / (n_heads / n_kv_heads).
+//
+// Prefill: one CTA = 128 queries of one sequence and one head, 8 warps of 16
+// rows; 64-key tiles double-buffered in shared memory with cp.async (16-byte
+// vectors, XOR-swizzled rows so ldmatrix is conflict-free); QK^T and PV on
+// the tensor cores with mma.sync m16n8k16 (BF16 in, float32 accumulate).
+//
+// Decode: the context of each (sequence, KV head) is cut into 1024-key
+// splits, one CTA each; the CTA's 4 warps share the G = n_heads / n_kv_heads
+// query rows of the group (padded to 16 MMA rows) and each takes 16 keys of
+// every 64-key tile from a 3-stage cp.async pipeline.  Warps merge in shared
+// memory, splits merge in a second kernel through their log-sum-exp.
+#include <algorithm>
+#include <cfloat>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace ll {
+
+namespace {
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr int kDecodeChunk = 1024;
+
+// byte offset of 16-byte chunk c of row r in a [rows][D] BF16 tile whose
+// chunks are XOR-swizzled by (r & 7)
+template <int D>
+LL_DEVINL uint32_t swz(int r, int c) {
+    return (uint32_t)(r * (D * 2) + ((c ^ (r & 7)) << 4));
+}
+
+// Loads rows [0, nrows) of a KV tile covering cache positions p0..p0+63 of one
+// sequence/head.  Thread i handles row i / TPR and chunks (i % TPR) * CPT ..
+template <int D, int NTHREADS>
+LL_DEVINL void load_kv_tile(uint8_t* sk, uint8_t* sv, const __nv_bfloat16* __restrict__ kp,
+                            const __nv_bfloat16* __restrict__ vp, const int32_t* __restrict__ table_row,
+                            int p0, int p_end, int hk, int n_kv_heads, int block_size, int num_blocks,
+                            int32_t* status) {
+    constexpr int CPR = D / 8;                  // 16-byte chunks per row
+    constexpr int TPR = NTHREADS / 64;          // threads per row
+    constexpr int CPT = CPR / TPR;              // chunks per thread
+    const int row = threadIdx.x / TPR;
+    const int c0 = (threadIdx.x % TPR) * CPT;
+    const int p = p0 + row;
+    bool valid = p < p_end;
+    size_t off = 0;
+    if (valid) {
+        const int blk = table_row[p / block_size];
+        if (blk < 0 || blk >= num_blocks) {
+            valid = false;
+            flag_status(status, LL_DEV_BAD_BLOCK);
+        } else {
+            off = (((size_t)blk * n_kv_heads + hk) * block_size + (p % block_size)) * D;
+        }
+    }
+#pragma unroll
+    for (int j = 0; j < CPT; ++j) {
+        const int c = c0 + j;
+        cp_async16(sk + swz<D>(row, c), kp + off + c * 8, valid);
+        cp_async16(sv + swz<D>(row, c), vp + off + c * 8, valid);
+    }
+}
+
+// ---------------------------------------------------------------- prefill
+
+template <int D>
+__global__ void __launch_bounds__(256, 1)
+    attn_prefill_kernel(const AttnPrefillArgs a) {
+    constexpr int BMQ = 128, BN = 64, NT = 256;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* sq = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
+    uint8_t* sk = sq + BMQ * D * 2;                  // [2][BN][D]
+    uint8_t* sv = sk + 2 * BN * D * 2;               // [2][BN][D]
+    __shared__ int max_pos_s;
+    __shared__ int warp_max_pos[8];
+
+    const int b = blockIdx.z;
+    const int h = blockIdx.y;
+    // heavy (late) query tiles first
+    const int mt = gridDim.x - 1 - blockIdx.x;
+    const int G = a.n_heads / a.n_kv_heads;
+    const int hk = h / G;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int row0 = mt * BMQ;
+    const size_t tok0 = (size_t)b * a.seq_len;
+    const int32_t* table_row = a.block_table + (size_t)b * a.max_blocks;
+
+    if (threadIdx.x == 0) max_pos_s = -1;
+    __syncthreads();
+    // positions of this tile's rows
+    int my_pos = -1;
+    if (threadIdx.x < BMQ && row0 + (int)threadIdx.x < a.seq_len)
+        my_pos = a.positions[tok0 + row0 + threadIdx.x];
+    if (my_pos >= a.max_blocks * a.block_size) {
+        flag_status(a.status, LL_DEV_BAD_POSITION);
+        my_pos = -1;
+    }
+    if (threadIdx.x < BMQ) atomicMax(&max_pos_s, my_pos);
+    {
+        // rows 32p .. 32p+15 (lanes 0-15 of warp p) belong to MMA warp 2p, the next 16 to 2p+1
+        int v = my_pos;
+#pragma unroll
+        for (int o = 8; o > 0; o >>= 1) v = max(v, __shfl_xor_sync(0xffffffffu, v, o));
+        if (threadIdx.x < BMQ && (lane & 15) == 0) warp_max_pos[threadIdx.x >> 4] = v;
+    }
+
+    // Q tile: 128 rows x D
+
+    {
+        constexpr int CPR = D / 8;
+        for (int i = threadIdx.x; i < BMQ * CPR; i += NT) {
+            const int r = i / CPR, c = i % CPR;
+            const bool ok = row0 + r < a.seq_len;
+            const __nv_bfloat16* src =
+                a.q + ((tok0 + row0 + (ok ? r : 0)) * a.n_heads + h) * D + c * 8;
+            cp_async16(sq + swz<D>(r, c), src, ok);
+        }
+        cp_async_commit();
+    }
+    __syncthreads();
+    const int max_pos = max_pos_s;
+    const int n_kt = (max_pos + BN) / BN;   // key tiles covering positions 0..max_pos
+    const int wmax = warp_max_pos[warp];
+
+    if (n_kt > 0)
+        load_kv_tile<D, NT>(sk, sv, a.k_pool, a.v_pool, table_row, 0, max_pos + 1, hk, a.n_kv_heads,
+                            a.block_size, a.num_blocks, a.status);
+    cp_async_commit();
+
+    const float sl2 = a.scale * kLog2e;
+    const int g = lane >> 2, cq = lane & 3;
+    const int qr0 = warp * 16 + g, qr1 = qr0 + 8;
+    const int pos_cap = a.max_blocks * a.block_size;
+    int qpos0 = -1, qpos1 = -1;
+    if (row0 + qr0 < a.seq_len) qpos0 = a.positions[tok0 + row0 + qr0];
+    if (row0 + qr1 < a.seq_len) qpos1 = a.positions[tok0 + row0 + qr1];
+    if (qpos0 >= pos_cap) qpos0 = -1;
+    if (qpos1 >= pos_cap) qpos1 = -1;
+
+    float acc[D / 8][4];
+#pragma unroll
+    for (int i = 0; i < D / 8; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+    uint32_t qf[D / 16][4];
+
+    cp_async_wait<1>();   // Q landed
+    __syncthreads();
+    {
+        const uint32_t qb = smem_u32(sq);
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+            const int r = warp * 16 + (lane & 15);
+            const int c = ks * 2 + (lane >> 4);
+            ldmatrix_x4(qf[ks], qb + swz<D>(r, c));
+        }
+    }
+
+    for (int kt = 0; kt < n_kt; ++kt) {
+        const int buf = kt & 1;
+        if (kt + 1 < n_kt)
+            load_kv_tile<D, NT>(sk + (buf ^ 1) * BN * D * 2, sv + (buf ^ 1) * BN * D * 2, a.k_pool,
+                                a.v_pool, table_row, (kt + 1) * BN, max_pos + 1, hk, a.n_kv_heads,
+                                a.block_size, a.num_blocks, a.status);
+        cp_async_commit();
+        cp_async_wait<1>();
+        __syncthreads();
+        if (kt * BN <= wmax) {
+            const uint32_t kb = smem_u32(sk + buf * BN * D * 2);
+            const uint32_t vb = smem_u32(sv + buf * BN * D * 2);
+            float s[BN / 8][4];
+#pragma unroll
+            for (int i = 0; i < BN / 8; ++i) s[i][0] = s[i][1] = s[i][2] = s[i][3] = 0.f;
+#pragma unroll
+            for (int ks = 0; ks < D / 16; ++ks) {
+#pragma unroll
+                for (int np = 0; np < BN / 16; ++np) {
+                    uint32_t bfr[4];
+                    const int r = np * 16 + (lane & 7) + ((lane >> 4) << 3);
+                    const int c = ks * 2 + ((lane >> 3) & 1);
+                    ldmatrix_x4(bfr, kb + swz<D>(r, c));
+                    mma_bf16_16816(s[2 * np], qf[ks], bfr[0], bfr[1]);
+                    mma_bf16_16816(s[2 * np + 1], qf[ks], bfr[2], bfr[3]);
+                }
+            }
+            // scale, causal mask, online softmax (rows qr0 -> s[.][0..1], qr1 -> s[.][2..3])
+            float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+            for (int nt = 0; nt < BN / 8; ++nt) {
+                const int kp = kt * BN + nt * 8 + 2 * cq;
+                s[nt][0] = (kp <= qpos0) ? s[nt][0] * sl2 : -INFINITY;
+                s[nt][1] = (kp + 1 <= qpos0) ? s[nt][1] * sl2 : -INFINITY;
+                s[nt][2] = (kp <= qpos1) ? s[nt][2] * sl2 : -INFINITY;
+                s[nt][3] = (kp + 1 <= qpos1) ? s[nt][3] * sl2 : -INFINITY;
+                mx0 = fmaxf(mx0, fmaxf(s[nt][0], s[nt][1]));
+                mx1 = fmaxf(mx1, fmaxf(s[nt][2], s[nt][3]));
+            }
+#pragma unroll
+            for (int o = 1; o <= 2; o <<= 1) {
+                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
+                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
+            }
+            const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+            const float base0 = (mn0 == -INFINITY) ? 0.f : mn0;
+            const float base1 = (mn1 == -INFINITY) ? 0.f : mn1;
+            const float al0 = exp2f(m0 - base0), al1 = exp2f(m1 - base1);
+            m0 = mn0;
+            m1 = mn1;
+            float rs0 = 0.f, rs1 = 0.f;
+            uint32_t pf[BN / 16][4];
+#pragma unroll
+            for (int nt = 0; nt < BN / 8; ++nt) {
+                const float p0 = exp2f(s[nt][0] - base0), p1 = exp2f(s[nt][1] - base0);
+                const float p2 = exp2f(s[nt][2] - base1), p3 = exp2f(s[nt][3] - base1);
+                rs0 += p0 + p1;
+                rs1 += p2 + p3;
+                const int kk = nt >> 1;
+                if ((nt & 1) == 0) {
+                    pf[kk][0] = pack_bf16x2(p0, p1);
+                    pf[kk][1] = pack_bf16x2(p2, p3);
+                } else {
+                    pf[kk][2] = pack_bf16x2(p0, p1);
+                    pf[kk][3] = pack_bf16x2(p2, p3);
+                }
+            }
+            l0 = l0 * al0 + rs0;
+            l1 = l1 * al1 + rs1;
+#pragma unroll
+            for (int i = 0; i < D / 8; ++i) {
+                acc[i][0] *= al0;
+                acc[i][1] *= al0;
+                acc[i][2] *= al1;
+                acc[i][3] *= al1;
+            }
+#pragma unroll
+            for (int kk = 0; kk < BN / 16; ++kk) {
+#pragma unroll
+                for (int dp = 0; dp < D / 16; ++dp) {
+                    uint32_t bfr[4];
+                    const int r = kk * 16 + (lane & 7) + (((lane >> 3) & 1) << 3);
+                    const int c = dp * 2 + (lane >> 4);
+                    ldmatrix_x4_trans(bfr, vb + swz<D>(r, c));
+                    mma_bf16_16816(acc[2 * dp], pf[kk], bfr[0], bfr[1]);
+                    mma_bf16_16816(acc[2 * dp + 1], pf[kk], bfr[2], bfr[3]);
+                }
+            }
+        }
+        __syncthreads();
+    }
+    cp_async_wait<0>();
+
+    // row sums across the quad
+#pragma unroll
+    for (int o = 1; o <= 2; o <<= 1) {
+        l0 += __shfl_xor_sync(0xffffffffu, l0, o);
+        l1 += __shfl_xor_sync(0xffffffffu, l1, o);
+    }
+    const float inv0 = l0 > 0.f ? 1.f / l0 : 0.f;
+    const float inv1 = l1 > 0.f ? 1.f / l1 : 0.f;
+    if (row0 + qr0 < a.seq_len) {
+        __nv_bfloat16* o = a.out + ((tok0 + row0 + qr0) * a.n_heads + h) * D;
+#pragma unroll
+        for (int i = 0; i < D / 8; ++i)
+            *reinterpret_cast<uint32_t*>(o + i * 8 + 2 * cq) = pack_bf16x2(acc[i][0] * inv0, acc[i][1] * inv0);
+    }
+    if (row0 + qr1 < a.seq_len) {
+        __nv_bfloat16* o = a.out + ((tok0 + row0 + qr1) * a.n_heads + h) * D;
+#pragma unroll
+        for (int i = 0; i < D / 8; ++i)
+            *reinterpret_cast<uint32_t*>(o + i * 8 + 2 * cq) = pack_bf16x2(acc[i][2] * inv1, acc[i][3] * inv1);
+    }
+}
+
+// ---------------------------------------------------------------- decode
+
+template <int D>
+__global__ void __launch_bounds__(128)
+    attn_decode_split_kernel(const AttnDecodeArgs a, int max_splits) {
+    constexpr int BN = 64, NT = 128, STAGES = 3;
+    constexpr int TILE = BN * D * 2;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* sbase = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
+    uint8_t* sq = sbase;                       // [16][D]
+    uint8_t* sk = sq + 16 * D * 2;             // [STAGES][BN][D]
+    uint8_t* sv = sk + STAGES * TILE;          // [STAGES][BN][D]
+
+    const int split = blockIdx.x, hk = blockIdx.y, b = blockIdx.z;
+    const int G = a.n_heads / a.n_kv_heads;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    int ctx = a.context_lens[b];
+    if (ctx > a.max_blocks * a.block_size || ctx < 0) {
+        if (threadIdx.x == 0 && split == 0 && hk == 0) flag_status(a.status, LL_DEV_BAD_POSITION);
+        ctx = min(max(ctx, 0), a.max_blocks * a.block_size);
+    }
+    const int k_begin = split * kDecodeChunk;
+    const int k_end = min(ctx, k_begin + kDecodeChunk);
+    const size_t part_row = ((size_t)b * a.n_heads + (size_t)hk * G) * max_splits + split;
+    if (k_begin >= k_end) {
+        // nothing to do: an empty split (ignored by the combine, which sees m = -inf)
+        if (threadIdx.x < G) {
+            float* ml = a.part_ml + 2 * (part_row + (size_t)threadIdx.x * max_splits);
+            ml[0] = -INFINITY;
+            ml[1] = 0.f;
+        }
+        return;
+    }
+    const int32_t* table_row = a.block_table + (size_t)b * a.max_blocks;
+    const int n_kt = (k_end - k_begin + BN - 1) / BN;
+
+    // query rows of the group, padded to 16 with zeros
+    {
+        constexpr int CPR = D / 8;
+        for (int i = threadIdx.x; i < 16 * CPR; i += NT) {
+            const int r = i / CPR, c = i % CPR;
+            const bool ok = r < G;
+            const __nv_bfloat16* src = a.q + ((size_t)b * a.n_heads + hk * G + (ok ? r : 0)) * D + c * 8;
+            cp_async16(sq + swz<D>(r, c), src, ok);
+        }
+    }
+#pragma unroll
+    for (int s = 0; s < STAGES - 1; ++s) {
+        if (s < n_kt)
+            load_kv_tile<D, NT>(sk + s * TILE, sv + s * TILE, a.k_pool, a.v_pool, table_row,
+                                k_begin + s * BN, k_end, hk, a.n_kv_heads, a.block_size,
+                                a.num_blocks, a.status);
+        cp_async_commit();
+    }
+
+    const float sl2 = a.scale * kLog2e;
+    const int g = lane >> 2, cq = lane & 3;
+    float acc[D / 8][4];
+#pragma unroll
+    for (int i = 0; i < D / 8; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+    uint32_t qf[D / 16][4];
+    bool q_loaded = false;
+
+    for (int kt = 0; kt < n_kt; ++kt) {
+        const int st = kt % STAGES;
+        {
+            const int nk = kt + STAGES - 1;
+            if (nk < n_kt)
+                load_kv_tile<D, NT>(sk + (nk % STAGES) * TILE, sv + (nk % STAGES) * TILE, a.k_pool,
+                                    a.v_pool, table_row, k_begin + nk * BN, k_end, hk, a.n_kv_heads,
+                                    a.block_size, a.num_blocks, a.status);
+            cp_async_commit();
+        }
+        cp_async_wait<STAGES - 1>();
+        __syncthreads();
+        if (!q_loaded) {
+            const uint32_t qb = smem_u32(sq);
+#pragma unroll
+            for (int ks = 0; ks < D / 16; ++ks)
+                ldmatrix_x4(qf[ks], qb + swz<D>(lane & 15, ks * 2 + (lane >> 4)));
+            q_loaded = true;
+        }
+        const uint32_t kb = smem_u32(sk + st * TILE);
+        const uint32_t vb = smem_u32(sv + st * TILE);
+        // this warp's 16 keys: tile rows 16*warp .. +15
+        float s[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+            uint32_t bfr[4];
+            const int r = warp * 16 + (lane & 7) + ((lane >> 4) << 3);
+            const int c = ks * 2 + ((lane >> 3) & 1);
+            ldmatrix_x4(bfr, kb + swz<D>(r, c));
+            mma_bf16_16816(s[0], qf[ks], bfr[0], bfr[1]);
+            mma_bf16_16816(s[1], qf[ks], bfr[2], bfr[3]);
+        }
+        float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+            const int kp = k_begin + kt * BN + warp * 16 + nt * 8 + 2 * cq;
+            s[nt][0] = (kp < k_end) ? s[nt][0] * sl2 : -INFINITY;
+            s[nt][1] = (kp + 1 < k_end) ? s[nt][1] * sl2 : -INFINITY;
+            s[nt][2] = (kp < k_end) ? s[nt][2] * sl2 : -INFINITY;
+            s[nt][3] = (kp + 1 < k_end) ? s[nt][3] * sl2 : -INFINITY;
+            mx0 = fmaxf(mx0, fmaxf(s[nt][0], s[nt][1]));
+            mx1 = fmaxf(mx1, fmaxf(s[nt][2], s[nt][3]));
+        }
+#pragma unroll
+        for (int o = 1; o <= 2; o <<= 1) {
+            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
+            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
+        }
+        const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+        const float base0 = (mn0 == -INFINITY) ? 0.f : mn0;
+        const float base1 = (mn1 == -INFINITY) ? 0.f : mn1;
+        const float al0 = exp2f(m0 - base0), al1 = exp2f(m1 - base1);
+        m0 = mn0;
+        m1 = mn1;
+        uint32_t pf[4];
+        float rs0 = 0.f, rs1 = 0.f;
+        {
+            float p[2][4];
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt) {
+                p[nt][0] = exp2f(s[nt][0] - base0);
+                p[nt][1] = exp2f(s[nt][1] - base0);
+                p[nt][2] = exp2f(s[nt][2] - base1);
+                p[nt][3] = exp2f(s[nt][3] - base1);
+                rs0 += p[nt][0] + p[nt][1];
+                rs1 += p[nt][2] + p[nt][3];
+            }
+            pf[0] = pack_bf16x2(p[0][0], p[0][1]);
+            pf[1] = pack_bf16x2(p[0][2], p[0][3]);
+            pf[2] = pack_bf16x2(p[1][0], p[1][1]);
+            pf[3] = pack_bf16x2(p[1][2], p[1][3]);
+        }
+        l0 = l0 * al0 + rs0;
+        l1 = l1 * al1 + rs1;
+#pragma unroll
+        for (int i = 0; i < D / 8; ++i) {
+            acc[i][0] *= al0;
+            acc[i][1] *= al0;
+            acc[i][2] *= al1;
+            acc[i][3] *= al1;
+        }
+#pragma unroll
+        for (int dp = 0; dp < D / 16; ++dp) {
+            uint32_t bfr[4];
+            const int r = warp * 16 + (lane & 7) + (((lane >> 3) & 1) << 3);
+            const int c = dp * 2 + (lane >> 4);
+            ldmatrix_x4_trans(bfr, vb + swz<D>(r, c));
+            mma_bf16_16816(acc[2 * dp], pf, bfr[0], bfr[1]);
+            mma_bf16_16816(acc[2 * dp + 1], pf, bfr[2], bfr[3]);
+        }
+        __syncthreads();
+    }
+    cp_async_wait<0>();
+#pragma unroll
+    for (int o = 1; o <= 2; o <<= 1) {
+        l0 += __shfl_xor_sync(0xffffffffu, l0, o);
+        l1 += __shfl_xor_sync(0xffffffffu, l1, o);
+    }
+
+    // merge the 4 warps: smem [4][16] (m, l) and [4][16][D] acc, reusing the K/V stages
+    __syncthreads();
+    float* s_ml = reinterpret_cast<float*>(sk);            // [4][16][2]
+    float* s_acc = s_ml + 4 * 16 * 2;                      // [4][16][D]
+    if (cq == 0) {
+        s_ml[(warp * 16 + g) * 2 + 0] = m0;
+        s_ml[(warp * 16 + g) * 2 + 1] = l0;
+        s_ml[(warp * 16 + g + 8) * 2 + 0] = m1;
+        s_ml[(warp * 16 + g + 8) * 2 + 1] = l1;
+    }
+#pragma unroll
+    for (int i = 0; i < D / 8; ++i) {
+        const int col = i * 8 + 2 * cq;
+        s_acc[(warp * 16 + g) * D + col] = acc[i][0];
+        s_acc[(warp * 16 + g) * D + col + 1] = acc[i][1];
+        s_acc[(warp * 16 + g + 8) * D + col] = acc[i][2];
+        s_acc[(warp * 16 + g + 8) * D + col + 1] = acc[i][3];
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < G * D; i += NT) {
+        const int r = i / D, col = i % D;
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < 4; ++w) M = fmaxf(M, s_ml[(w * 16 + r) * 2]);
+        const float base = (M == -INFINITY) ? 0.f : M;
+        float num = 0.f, den = 0.f;
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+            const float e = exp2f(s_ml[(w * 16 + r) * 2] - base);
+            num += e * s_acc[(w * 16 + r) * D + col];
+            den += e * s_ml[(w * 16 + r) * 2 + 1];
+        }
+        const size_t pr = part_row + (size_t)r * max_splits;
+        a.part_o[pr * D + col] = den > 0.f ? num / den : 0.f;
+        if (col == 0) {
+            a.part_ml[2 * pr] = M;
+            a.part_ml[2 * pr + 1] = den;
+        }
+    }
+}
+
+// out[b][h] = sum_s 2^(m_s - M) l_s o_s / sum_s 2^(m_s - M) l_s over the splits of (b, h)
+__global__ void attn_decode_combine_kernel(const AttnDecodeArgs a, int max_splits) {
+    const int h = blockIdx.x, b = blockIdx.y;
+    const int D = a.head_dim;
+    int ctx = min(max(a.context_lens[b], 0), a.max_blocks * a.block_size);
+    const int ns = min(max_splits, (ctx + kDecodeChunk - 1) / kDecodeChunk);
+    const size_t base_row = ((size_t)b * a.n_heads + h) * max_splits;
+    float M = -INFINITY;
+    for (int s = 0; s < ns; ++s) M = fmaxf(M, a.part_ml[2 * (base_row + s)]);
+    const float mb = (M == -INFINITY) ? 0.f : M;
+    for (int col = threadIdx.x; col < D; col += blockDim.x) {
+        float num = 0.f, den = 0.f;
+        for (int s = 0; s < ns; ++s) {
+            const float ms = a.part_ml[2 * (base_row + s)];
+            const float w = exp2f(ms - mb) * a.part_ml[2 * (base_row + s) + 1];
+            num += w * a.part_o[(base_row + s) * D + col];
+            den += w;
+        }
+        a.out[((size_t)b * a.n_heads + h) * D + col] = __float2bfloat16_rn(den > 0.f ? num / den : 0.f);
+    }
+}
+
+template <int D>
+cudaError_t prefill_for(const AttnPrefillArgs& a, cudaStream_t stream) {
+    const size_t smem = (size_t)(128 * D * 2) + 4 * (64 * D * 2) + 128;
+    static bool configured = false;
+    if (!configured) {
+        cudaError_t e = cudaFuncSetAttribute(attn_prefill_kernel<D>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        configured = true;
+    }
+    dim3 grid((a.seq_len + 127) / 128, a.n_heads, a.batch);
+    attn_prefill_kernel<D><<<grid, 256, smem, stream>>>(a);
+    return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t decode_for(const AttnDecodeArgs& a, cudaStream_t stream) {
+    const int max_splits = attn_decode_max_splits(a.max_blocks, a.block_size);
+    const size_t smem = (size_t)(16 * D * 2) + 2 * 3 * (64 * D * 2) + 128;
+    static bool configured = false;
+    if (!configured) {
+        cudaError_t e = cudaFuncSetAttribute(attn_decode_split_kernel<D>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        configured = true;
+    }
+    dim3 grid(max_splits, a.n_kv_heads, a.batch);
+    attn_decode_split_kernel<D><<<grid, 128, smem, stream>>>(a, max_splits);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    attn_decode_combine_kernel<<<dim3(a.n_heads, a.batch), D, 0, stream>>>(a, max_splits);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+int attn_decode_max_splits(int max_blocks, int block_size) {
+    const long long max_ctx = (long long)max_blocks * block_size;
+    return (int)std::max<long long>(1, (max_ctx + kDecodeChunk - 1) / kDecodeChunk);
+}
+
+size_t attn_decode_scratch_bytes(int batch, int n_heads, int head_dim, int max_blocks,
+                                 int block_size) {
+    const size_t rows = (size_t)batch * n_heads * attn_decode_max_splits(max_blocks, block_size);
+    return rows * head_dim * sizeof(float) + rows * 2 * sizeof(float);
+}
+
+cudaError_t launch_attn_prefill(const AttnPrefillArgs& a, cudaStream_t stream) {
+    if (a.batch <= 0 || a.seq_len <= 0) return cudaSuccess;
+    if (a.head_dim == 128) return prefill_for<128>(a, stream);
+    if (a.head_dim == 64) return prefill_for<64>(a, stream);
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_attn_decode(const AttnDecodeArgs& a, cudaStream_t stream) {
+    if (a.batch <= 0) return cudaSuccess;
+    if (a.head_dim == 128) return decode_for<128>(a, stream);
+    if (a.head_dim == 64) return decode_for<64>(a, stream);
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace ll

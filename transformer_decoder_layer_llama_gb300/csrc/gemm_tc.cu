@@ -1,0 +1,640 @@
+// Tensor-core GEMM of the decoder layer on sm_103a: D = A * B^T with BF16
+// operands staged by TMA (128-byte swizzle) and float32 accumulators in
+// TMEM, issued as tcgen05.mma kind::f16 by one thread.  Its epilogues fuse
+// the element-wise steps that follow each Linear of the Llama2-7B operator
+// chain (page "Which ops-transformer operators one Llama2-7B layer calls",
+// section "single-layer operator call chain"): RoPE on the merged QKV output
+// plus the ReshapeAndCache write of K/V into the paged pool, the residual add
+// after the output and down projections, and SiLU(gate) * up after the merged
+// gate/up projection.
+//
+// Two forms share the kernel:
+//  * token form (many tokens, prefill): A = activations [tokens, K] in
+//    128-row blocks, B = weights [N, K] in 256-row blocks; persistent CTAs walk
+//    the output tiles token-block-fastest so that CTAs running together share
+//    the weight tile in L2.
+//  * weight form (<= 64 tokens, decode): A = weights in 128-row blocks, B = the
+//    few token rows (MMA N = tokens rounded up to 16).  The K range is split
+//    across CTAs so that enough of them stream weights; float32 partial tiles
+//    go to a scratch buffer and the last CTA to finish a tile (an atomic
+//    ticket, no spinning) adds them up and runs the epilogue.
+//
+// Warp roles (192 threads): warp 0 issues TMA loads, warp 1 allocates TMEM
+// and issues the MMAs, warps 2-5 drain TMEM (warp w reads TMEM lanes
+// 32*(w%4) .. +31) and run the epilogue.  Two TMEM accumulators let the
+// epilogue of one tile overlap the main loop of the next.
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <mutex>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace ll {
+
+namespace {
+
+constexpr int BM = 128;          // rows of the A block = MMA M
+constexpr int BK = 64;           // K per pipeline stage: one 128-byte swizzle row of BF16
+constexpr int UK = 16;           // K of one tcgen05.mma kind::f16
+constexpr int MAX_STAGES = 8;
+constexpr int kThreads = 192;
+constexpr int kTokenFormBN = 256;
+constexpr int kSwapMaxTokens = 64;
+
+struct GemmArgs {
+    EpiParams ep;
+    int swap;
+    int tokens, n, k;
+    int bn;                  // MMA N
+    int tiles_m;             // number of A blocks
+    int tiles_n;             // number of B blocks
+    int splits;
+    int num_kb;
+    int units;
+    int stages;
+    uint32_t stage_bytes;
+    uint32_t a_bytes;
+    uint32_t tmem_cols;
+    float* partials;
+    int32_t* counters;
+};
+
+LL_DEVINL void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+LL_DEVINL float silu_f(float z) { return z / (1.0f + expf(-z)); }
+
+struct TokenSlot {
+    int pos;         // -1 if invalid
+    long long kv_row;  // row index (blk * Hkv) * bs + off of head 0, or -1
+};
+
+LL_DEVINL TokenSlot token_slot(const EpiParams& ep, int t) {
+    TokenSlot s{-1, -1};
+    int pos = ep.positions ? ep.positions[t] : ep.context_lens[t] - 1;
+    if (pos < 0 || pos >= ep.max_position) {
+        flag_status(ep.status, LL_DEV_BAD_POSITION);
+        return s;
+    }
+    s.pos = pos;
+    int seq = t / ep.seq_len;
+    int lb = pos / ep.block_size;
+    if (lb >= ep.max_blocks) {
+        flag_status(ep.status, LL_DEV_BAD_BLOCK);
+        return s;
+    }
+    int blk = ep.block_table[(size_t)seq * ep.max_blocks + lb];
+    if (blk < 0 || blk >= ep.num_blocks) {
+        flag_status(ep.status, LL_DEV_BAD_BLOCK);
+        return s;
+    }
+    s.kv_row = ((long long)blk * ep.n_kv_heads) * ep.block_size + (pos % ep.block_size);
+    return s;
+}
+
+// ---------------------------------------------------------------- token-form epilogue
+// One thread owns one token row t and 16 consecutive output features n0..n0+15.
+LL_DEVINL void epi_token_chunk(const EpiParams& ep, int t, bool row_ok, int n0, int N,
+                               const TokenSlot& ts, const float (&v)[16]) {
+    if (!row_ok) return;
+    switch (ep.kind) {
+        case EPI_STORE: {
+            uint4 o0, o1;
+            o0.x = pack_bf16x2(v[0], v[1]);   o0.y = pack_bf16x2(v[2], v[3]);
+            o0.z = pack_bf16x2(v[4], v[5]);   o0.w = pack_bf16x2(v[6], v[7]);
+            o1.x = pack_bf16x2(v[8], v[9]);   o1.y = pack_bf16x2(v[10], v[11]);
+            o1.z = pack_bf16x2(v[12], v[13]); o1.w = pack_bf16x2(v[14], v[15]);
+            uint4* dst = reinterpret_cast<uint4*>(ep.out + (size_t)t * ep.ld_out + n0);
+            dst[0] = o0;
+            dst[1] = o1;
+            break;
+        }
+        case EPI_RESID: {
+            const uint4* rp = reinterpret_cast<const uint4*>(ep.resid + (size_t)t * N + n0);
+            uint4 r0 = rp[0], r1 = rp[1];
+            uint32_t rr[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
+            uint32_t oo[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                oo[j] = pack_bf16x2(bf16_lo(rr[j]) + v[2 * j], bf16_hi(rr[j]) + v[2 * j + 1]);
+            uint4* dst = reinterpret_cast<uint4*>(ep.out + (size_t)t * ep.ld_out + n0);
+            dst[0] = make_uint4(oo[0], oo[1], oo[2], oo[3]);
+            dst[1] = make_uint4(oo[4], oo[5], oo[6], oo[7]);
+            break;
+        }
+        case EPI_SWIGLU: {
+            float a[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) a[j] = silu_f(v[2 * j]) * v[2 * j + 1];
+            uint4 o;
+            o.x = pack_bf16x2(a[0], a[1]); o.y = pack_bf16x2(a[2], a[3]);
+            o.z = pack_bf16x2(a[4], a[5]); o.w = pack_bf16x2(a[6], a[7]);
+            *reinterpret_cast<uint4*>(ep.out + (size_t)t * ep.ld_out + (n0 >> 1)) = o;
+            break;
+        }
+        case EPI_QKV: {
+            const int d = ep.head_dim;
+            const int nq = ep.n_heads * d;
+            const int nk = ep.n_kv_heads * d;
+            if (ts.pos < 0) return;
+            int sec, head, e0;
+            if (n0 < nq) { sec = 0; head = n0 / d; e0 = n0 - head * d; }
+            else if (n0 < nq + nk) { sec = 1; head = (n0 - nq) / d; e0 = n0 - nq - head * d; }
+            else { sec = 2; head = (n0 - nq - nk) / d; e0 = n0 - nq - nk - head * d; }
+            __nv_bfloat16* base;
+            if (sec == 0) {
+                base = ep.q_out + (size_t)t * nq + (size_t)head * d;
+            } else {
+                if (ts.kv_row < 0) return;
+                size_t row = (size_t)ts.kv_row + (size_t)head * ep.block_size;
+                base = (sec == 1 ? ep.k_pool : ep.v_pool) + row * d;
+            }
+            if (sec == 2) {
+                uint4 o0, o1;
+                o0.x = pack_bf16x2(v[0], v[1]);   o0.y = pack_bf16x2(v[2], v[3]);
+                o0.z = pack_bf16x2(v[4], v[5]);   o0.w = pack_bf16x2(v[6], v[7]);
+                o1.x = pack_bf16x2(v[8], v[9]);   o1.y = pack_bf16x2(v[10], v[11]);
+                o1.z = pack_bf16x2(v[12], v[13]); o1.w = pack_bf16x2(v[14], v[15]);
+                reinterpret_cast<uint4*>(base + e0)[0] = o0;
+                reinterpret_cast<uint4*>(base + e0)[1] = o1;
+            } else {
+                // packed feature e0 + 2j holds element i = e0/2 + j, e0 + 2j + 1 holds i + d/2
+                const int i0 = e0 >> 1;
+                const float4* cs4 = reinterpret_cast<const float4*>(
+                    ep.rope_cs + (size_t)ts.pos * (d >> 1) + i0);
+                float lo[8], hi[8];
+#pragma unroll
+                for (int jj = 0; jj < 4; ++jj) {
+                    float4 c = cs4[jj];   // (cos, sin) of pairs i0+2jj and i0+2jj+1
+                    int j = 2 * jj;
+                    lo[j] = v[2 * j] * c.x - v[2 * j + 1] * c.y;
+                    hi[j] = v[2 * j + 1] * c.x + v[2 * j] * c.y;
+                    lo[j + 1] = v[2 * j + 2] * c.z - v[2 * j + 3] * c.w;
+                    hi[j + 1] = v[2 * j + 3] * c.z + v[2 * j + 2] * c.w;
+                }
+                uint4 a, b;
+                a.x = pack_bf16x2(lo[0], lo[1]); a.y = pack_bf16x2(lo[2], lo[3]);
+                a.z = pack_bf16x2(lo[4], lo[5]); a.w = pack_bf16x2(lo[6], lo[7]);
+                b.x = pack_bf16x2(hi[0], hi[1]); b.y = pack_bf16x2(hi[2], hi[3]);
+                b.z = pack_bf16x2(hi[4], hi[5]); b.w = pack_bf16x2(hi[6], hi[7]);
+                *reinterpret_cast<uint4*>(base + i0) = a;
+                *reinterpret_cast<uint4*>(base + (d >> 1) + i0) = b;
+            }
+            break;
+        }
+    }
+}
+
+// ---------------------------------------------------------------- weight-form epilogue
+// One thread owns one output feature n (its TMEM lane) and 16 consecutive
+// tokens t0..t0+15.  All 32 lanes of the warp call this together (shuffles).
+LL_DEVINL void epi_weight_chunk(const EpiParams& ep, int n, int N, int t0, int T,
+                                const float (&v)[16]) {
+    const bool n_ok = n < N;
+    switch (ep.kind) {
+        case EPI_STORE:
+            if (n_ok)
+#pragma unroll
+                for (int j = 0; j < 16; ++j)
+                    if (t0 + j < T) ep.out[(size_t)(t0 + j) * ep.ld_out + n] = __float2bfloat16_rn(v[j]);
+            break;
+        case EPI_RESID:
+            if (n_ok)
+#pragma unroll
+                for (int j = 0; j < 16; ++j)
+                    if (t0 + j < T) {
+                        float r = __bfloat162float(ep.resid[(size_t)(t0 + j) * N + n]);
+                        ep.out[(size_t)(t0 + j) * ep.ld_out + n] = __float2bfloat16_rn(r + v[j]);
+                    }
+            break;
+        case EPI_SWIGLU:
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                float other = __shfl_xor_sync(0xffffffffu, v[j], 1);
+                if (n_ok && (n & 1) == 0 && t0 + j < T)
+                    ep.out[(size_t)(t0 + j) * ep.ld_out + (n >> 1)] =
+                        __float2bfloat16_rn(silu_f(v[j]) * other);
+            }
+            break;
+        case EPI_QKV: {
+            const int d = ep.head_dim;
+            const int nq = ep.n_heads * d;
+            const int nk = ep.n_kv_heads * d;
+            int sec, head, e;
+            if (n < nq) { sec = 0; head = n / d; e = n - head * d; }
+            else if (n < nq + nk) { sec = 1; head = (n - nq) / d; e = n - nq - head * d; }
+            else { sec = 2; head = (n - nq - nk) / d; e = n - nq - nk - head * d; }
+            const int pair = e >> 1;
+            const int orig = (sec == 2) ? e : ((e & 1) ? pair + (d >> 1) : pair);
+#pragma unroll 4
+            for (int j = 0; j < 16; ++j) {
+                float other = __shfl_xor_sync(0xffffffffu, v[j], 1);
+                int t = t0 + j;
+                if (!n_ok || t >= T) continue;
+                TokenSlot ts = token_slot(ep, t);
+                if (ts.pos < 0) continue;
+                float val = v[j];
+                if (sec != 2) {
+                    float2 c = ep.rope_cs[(size_t)ts.pos * (d >> 1) + pair];
+                    val = (e & 1) ? (v[j] * c.x + other * c.y) : (v[j] * c.x - other * c.y);
+                }
+                __nv_bfloat16 bv = __float2bfloat16_rn(val);
+                if (sec == 0) {
+                    ep.q_out[(size_t)t * nq + (size_t)head * d + orig] = bv;
+                } else if (ts.kv_row >= 0) {
+                    size_t row = (size_t)ts.kv_row + (size_t)head * ep.block_size;
+                    (sec == 1 ? ep.k_pool : ep.v_pool)[row * d + orig] = bv;
+                }
+            }
+            break;
+        }
+    }
+}
+
+LL_DEVINL void unit_coords(const GemmArgs& a, int u, int& a_blk, int& b_blk, int& split, int& kb0,
+                           int& kb1) {
+    split = u % a.splits;
+    int tile = u / a.splits;
+    a_blk = tile % a.tiles_m;
+    b_blk = tile / a.tiles_m;
+    kb0 = (int)((long long)split * a.num_kb / a.splits);
+    kb1 = (int)((long long)(split + 1) * a.num_kb / a.splits);
+}
+
+__global__ void __launch_bounds__(kThreads, 2)
+    gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const GemmArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                               ~uintptr_t(1023));
+    __shared__ uint64_t full_bar[MAX_STAGES], empty_bar[MAX_STAGES];
+    __shared__ uint64_t tfull_bar[2], tempty_bar[2], drain_bar;
+    __shared__ uint32_t tmem_base_s;
+    __shared__ int abort_s;
+    __shared__ int last_s;
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    int32_t* status = a.ep.status;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < a.stages; ++s) {
+            mbar_init(&full_bar[s], 1);
+            mbar_init(&empty_bar[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&tfull_bar[b], 1);
+            mbar_init(&tempty_bar[b], 128);
+        }
+        mbar_init(&drain_bar, 1);
+        abort_s = 0;
+        last_s = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tmA);
+        tma_prefetch_desc(&tmB);
+    }
+    if (warp == 1) {
+        tmem_alloc(&tmem_base_s, a.tmem_cols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_base_s;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ------------------------------------------------ TMA producer
+            int stage = 0;
+            uint32_t phase = 0;
+            uint32_t issued[MAX_STAGES];
+            for (int s = 0; s < MAX_STAGES; ++s) issued[s] = 0;
+            const uint64_t pol_w = l2_policy_evict_first();
+            bool ok = true;
+            for (int u = blockIdx.x; u < a.units && ok; u += gridDim.x) {
+                int a_blk, b_blk, split, kb0, kb1;
+                unit_coords(a, u, a_blk, b_blk, split, kb0, kb1);
+                for (int kb = kb0; kb < kb1; ++kb) {
+                    if (!mbar_wait_bounded(&empty_bar[stage], phase ^ 1, &abort_s, status)) {
+                        ok = false;
+                        break;
+                    }
+                    uint8_t* sa = smem + (size_t)stage * a.stage_bytes;
+                    uint8_t* sb = sa + a.a_bytes;
+                    mbar_arrive_expect_tx(&full_bar[stage], a.stage_bytes);
+                    if (a.swap) {
+                        // weights stream once: keep them from pushing the activations out of L2
+                        tma_load_2d_hint(sa, &tmA, kb * BK, a_blk * BM, &full_bar[stage], pol_w);
+                        tma_load_2d(sb, &tmB, kb * BK, b_blk * a.bn, &full_bar[stage]);
+                    } else {
+                        tma_load_2d(sa, &tmA, kb * BK, a_blk * BM, &full_bar[stage]);
+                        tma_load_2d(sb, &tmB, kb * BK, b_blk * a.bn, &full_bar[stage]);
+                    }
+                    for (int s = 0; s < MAX_STAGES; ++s) issued[s] += (s == stage);
+                    if (++stage == a.stages) {
+                        stage = 0;
+                        phase ^= 1;
+                    }
+                }
+            }
+            if (abort_s) {
+                // let loads already in flight land before the CTA's shared memory goes away
+                volatile int never = 0;
+                for (int s = 0; s < a.stages; ++s)
+                    if (issued[s]) mbar_wait_bounded(&full_bar[s], (issued[s] - 1) & 1, &never, nullptr);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        if (lane == 0) {
+            // ------------------------------------------------ MMA issuer
+            const uint32_t idesc = umma_idesc_bf16(BM, a.bn);
+            int stage = 0;
+            uint32_t phase = 0;
+            int local = 0;
+            bool ok = true;
+            for (int u = blockIdx.x; u < a.units && ok; u += gridDim.x, ++local) {
+                int a_blk, b_blk, split, kb0, kb1;
+                unit_coords(a, u, a_blk, b_blk, split, kb0, kb1);
+                const int buf = local & 1;
+                const uint32_t accp = (local >> 1) & 1;
+                if (!mbar_wait_bounded(&tempty_bar[buf], accp ^ 1, &abort_s, status)) break;
+                tc_fence_after();
+                const uint32_t d_tmem = tmem + (uint32_t)(buf * a.bn);
+                for (int kb = kb0; kb < kb1; ++kb) {
+                    if (!mbar_wait_bounded(&full_bar[stage], phase, &abort_s, status)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t sa = smem_u32(smem + (size_t)stage * a.stage_bytes);
+                    const uint32_t sb = sa + a.a_bytes;
+                    const uint64_t da = umma_desc_sw128(sa);
+                    const uint64_t db = umma_desc_sw128(sb);
+#pragma unroll
+                    for (int kk = 0; kk < BK / UK; ++kk) {
+                        // advance the start address by kk * 32 bytes inside the swizzled row
+                        tc_mma_bf16(d_tmem, da + (uint64_t)(kk * 2), db + (uint64_t)(kk * 2), idesc,
+                                    (kb > kb0 || kk > 0) ? 1u : 0u);
+                    }
+                    tc_commit(&empty_bar[stage]);
+                    if (++stage == a.stages) {
+                        stage = 0;
+                        phase ^= 1;
+                    }
+                }
+                if (ok) tc_commit(&tfull_bar[buf]);
+            }
+            // all MMAs issued by this thread must be complete before TMEM is freed
+            tc_commit(&drain_bar);
+            volatile int never = 0;
+            mbar_wait_bounded(&drain_bar, 0, &never, status);
+        }
+        __syncwarp();
+    } else {
+        // ---------------------------------------------------- epilogue warps
+        const int q = warp & 3;
+        const int r = q * 32 + lane;             // TMEM lane = row of the A block
+        const uint32_t lane_base = (uint32_t)(q * 32) << 16;
+        int local = 0;
+        for (int u = blockIdx.x; u < a.units; u += gridDim.x, ++local) {
+            int a_blk, b_blk, split, kb0, kb1;
+            unit_coords(a, u, a_blk, b_blk, split, kb0, kb1);
+            const int buf = local & 1;
+            const uint32_t accp = (local >> 1) & 1;
+            const bool got = mbar_wait_bounded(&tfull_bar[buf], accp, &abort_s, status);
+            if (a.swap && a.splits > 1) {
+                // this path meets again at named barriers: leave together or not at all
+                epi_bar();
+                if (abort_s) break;
+            } else if (!got) {
+                break;
+            }
+            tc_fence_after();
+            const uint32_t taddr = tmem + lane_base + (uint32_t)(buf * a.bn);
+            if (!a.swap) {
+                const int t = a_blk * BM + r;
+                const bool row_ok = t < a.tokens;
+                TokenSlot ts{-1, -1};
+                if (a.ep.kind == EPI_QKV && row_ok) ts = token_slot(a.ep, t);
+                for (int c = 0; c < a.bn; c += 16) {
+                    const int n0 = b_blk * a.bn + c;
+                    if (n0 >= a.n) break;
+                    float v[16];
+                    tmem_ld16(taddr + (uint32_t)c, v);
+                    epi_token_chunk(a.ep, t, row_ok, n0, a.n, ts, v);
+                }
+                tc_fence_before();
+                mbar_arrive(&tempty_bar[buf]);
+            } else {
+                const int n = a_blk * BM + r;
+                const int T = a.tokens;
+                if (a.splits == 1) {
+                    for (int c = 0; c < a.bn; c += 16) {
+                        float v[16];
+                        tmem_ld16(taddr + (uint32_t)c, v);
+                        epi_weight_chunk(a.ep, n, a.n, c, T, v);
+                    }
+                    tc_fence_before();
+                    mbar_arrive(&tempty_bar[buf]);
+                } else {
+                    const int tile = a_blk;
+                    float* part = a.partials + (size_t)(tile * a.splits + split) * (size_t)(BM * a.bn);
+                    for (int c = 0; c < a.bn; c += 16) {
+                        float v[16];
+                        tmem_ld16(taddr + (uint32_t)c, v);
+#pragma unroll
+                        for (int j = 0; j < 16; ++j)
+                            if (c + j < T) __stcg(part + (size_t)(c + j) * BM + r, v[j]);
+                    }
+                    tc_fence_before();
+                    mbar_arrive(&tempty_bar[buf]);
+                    __threadfence();
+                    epi_bar();
+                    if (threadIdx.x == 64) {
+                        int old = atomicAdd(&a.counters[tile], 1);
+                        int last = (old == a.splits - 1);
+                        if (last) atomicExch(&a.counters[tile], 0);
+                        last_s = last;
+                    }
+                    epi_bar();
+                    if (last_s) {
+                        __threadfence();
+                        const float* p0 = a.partials + (size_t)(tile * a.splits) * (size_t)(BM * a.bn);
+                        for (int c = 0; c < a.bn; c += 16) {
+                            float v[16];
+#pragma unroll
+                            for (int j = 0; j < 16; ++j) {
+                                float s = 0.f;
+                                if (c + j < T)
+                                    for (int sp = 0; sp < a.splits; ++sp)
+                                        s += __ldcg(p0 + (size_t)sp * (BM * a.bn) + (size_t)(c + j) * BM + r);
+                                v[j] = s;
+                            }
+                            epi_weight_chunk(a.ep, n, a.n, c, T, v);
+                        }
+                    }
+                }
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem, a.tmem_cols);
+}
+
+// ---------------------------------------------------------------- host side
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// 2-D BF16 tensor [rows, inner] row-major, box [box_rows, 64] with the 128-byte swizzle.
+bool make_tmap(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t rows, uint32_t box_rows) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {inner, rows};
+    cuuint64_t strides[1] = {inner * 2};
+    cuuint32_t box[2] = {(cuuint32_t)BK, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides,
+                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+int ceil_div(int a, int b) { return (a + b - 1) / b; }
+
+uint32_t pow2_at_least(uint32_t x) {
+    uint32_t p = 32;
+    while (p < x) p <<= 1;
+    return p;
+}
+
+struct Plan {
+    bool swap;
+    int bn, tiles_m, tiles_n, splits, num_kb, units, stages, ctas_per_sm;
+    uint32_t stage_bytes, a_bytes, tmem_cols;
+    size_t smem_bytes;
+};
+
+Plan make_plan(int tokens, int n, int k, int sms) {
+    Plan p{};
+    p.swap = tokens <= kSwapMaxTokens;
+    p.num_kb = ceil_div(k, BK);
+    p.a_bytes = BM * BK * 2;
+    if (!p.swap) {
+        p.bn = kTokenFormBN;
+        p.tiles_m = ceil_div(tokens, BM);
+        p.tiles_n = ceil_div(n, p.bn);
+        p.splits = 1;
+        p.stage_bytes = p.a_bytes + p.bn * BK * 2;
+        p.stages = 4;
+        p.ctas_per_sm = 1;
+    } else {
+        p.bn = std::max(16, ceil_div(tokens, 16) * 16);
+        p.tiles_m = ceil_div(n, BM);
+        p.tiles_n = 1;
+        p.stage_bytes = p.a_bytes + p.bn * BK * 2;
+        p.ctas_per_sm = 2;
+        int budget = (227 * 1024) / p.ctas_per_sm - 1024 - 1024;
+        p.stages = std::min(MAX_STAGES, budget / (int)p.stage_bytes);
+        int target = sms * p.ctas_per_sm;
+        int splits = std::max(1, (target + p.tiles_m / 2) / p.tiles_m);
+        splits = std::min(splits, std::max(1, p.num_kb / 4));
+        splits = std::min(splits, 16);
+        p.splits = splits;
+    }
+    p.units = p.tiles_m * p.tiles_n * p.splits;
+    p.tmem_cols = pow2_at_least(2u * (uint32_t)p.bn);
+    p.smem_bytes = (size_t)p.stages * p.stage_bytes + 1024;
+    return p;
+}
+
+}  // namespace
+
+int device_sm_count() {
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return -1;
+    return sms;
+}
+
+void gemm_scratch_need(int tokens, int n, int k, size_t* partial_bytes, int* counters) {
+    int sms = device_sm_count();
+    if (sms <= 0) sms = 160;
+    Plan p = make_plan(tokens, n, k, sms);
+    *partial_bytes = p.splits > 1 ? (size_t)p.tiles_m * p.splits * BM * p.bn * sizeof(float) : 0;
+    *counters = p.swap ? p.tiles_m : 0;
+}
+
+size_t gemm_partial_bound_bytes() {
+    // weight form only: units <= max(tiles, 2 * 160 SMs * 1.5) and bn <= 64
+    return (size_t)(2 * 160 * 3 / 2 + 64) * BM * kSwapMaxTokens * sizeof(float);
+}
+
+int gemm_counter_bound(int n) { return ceil_div(n, BM); }
+
+cudaError_t launch_gemm(const GemmProblem& pr, cudaStream_t stream) {
+    int sms = device_sm_count();
+    if (sms <= 0) return cudaErrorNoDevice;
+    Plan p = make_plan(pr.tokens, pr.n, pr.k, sms);
+    GemmArgs a{};
+    a.ep = pr.ep;
+    a.swap = p.swap;
+    a.tokens = pr.tokens;
+    a.n = pr.n;
+    a.k = pr.k;
+    a.bn = p.bn;
+    a.tiles_m = p.tiles_m;
+    a.tiles_n = p.tiles_n;
+    a.splits = p.splits;
+    a.num_kb = p.num_kb;
+    a.units = p.units;
+    a.stages = p.stages;
+    a.stage_bytes = p.stage_bytes;
+    a.a_bytes = p.a_bytes;
+    a.tmem_cols = p.tmem_cols;
+    a.partials = pr.partials;
+    a.counters = pr.counters;
+    if (p.splits > 1) {
+        size_t need = (size_t)p.tiles_m * p.splits * BM * p.bn * sizeof(float);
+        if (!pr.partials || pr.partial_bytes < need || !pr.counters || pr.counter_cap < p.tiles_m)
+            return cudaErrorInvalidValue;
+    }
+    CUtensorMap tmA, tmB;
+    bool ok;
+    if (!p.swap) {
+        ok = make_tmap(&tmA, pr.act, pr.k, pr.tokens, BM) && make_tmap(&tmB, pr.w, pr.k, pr.n, p.bn);
+    } else {
+        ok = make_tmap(&tmA, pr.w, pr.k, pr.n, BM) && make_tmap(&tmB, pr.act, pr.k, pr.tokens, p.bn);
+    }
+    if (!ok) return cudaErrorInvalidValue;
+    static int configured_smem = 0;
+    if ((int)p.smem_bytes > configured_smem) {
+        cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             227 * 1024);
+        if (e != cudaSuccess) return e;
+        configured_smem = 227 * 1024;
+    }
+    int grid = std::min(p.units, sms * p.ctas_per_sm);
+    gemm_tc_kernel<<<grid, kThreads, p.smem_bytes, stream>>>(tmA, tmB, a);
+    return cudaGetLastError();
+}
+
+}  // namespace ll

@@ -1,0 +1,116 @@
+// Internal launcher interface between the C-ABI layer (api.cu) and the
+// kernels.  Not part of the public ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace ll {
+
+enum EpiKind : int {
+    EPI_STORE = 0,   // out = acc
+    EPI_RESID = 1,   // out = resid + acc                (O projection, down projection)
+    EPI_SWIGLU = 2,  // out[j] = silu(acc[2j]) * acc[2j+1] (merged gate/up, rows interleaved)
+    EPI_QKV = 3,     // RoPE on Q/K, Q -> q_out, K/V -> paged pool (merged QKV)
+};
+
+struct EpiParams {
+    int kind;
+    __nv_bfloat16* out;            // STORE / RESID / SWIGLU destination [tokens, ld_out]
+    int ld_out;
+    const __nv_bfloat16* resid;    // RESID: [tokens, n]
+    // EPI_QKV
+    __nv_bfloat16* q_out;          // [tokens, n_heads * head_dim]
+    __nv_bfloat16* k_pool;
+    __nv_bfloat16* v_pool;
+    const int32_t* positions;      // prefill: position of each token (null in decode)
+    const int32_t* context_lens;   // decode: position = context_lens[token] - 1
+    const int32_t* block_table;
+    int max_blocks;
+    int seq_len;                   // tokens per sequence (decode: 1)
+    int num_blocks;
+    int block_size;
+    int n_heads;
+    int n_kv_heads;
+    int head_dim;
+    int max_position;
+    const float2* rope_cs;         // [max_position][head_dim / 2] (cos, sin)
+    int32_t* status;
+};
+
+struct GemmProblem {
+    const __nv_bfloat16* act;      // [tokens, k]
+    const __nv_bfloat16* w;        // [n, k]
+    int tokens, n, k;
+    EpiParams ep;
+    float* partials;               // split-K scratch (swap form), may be null when splits == 1
+    size_t partial_bytes;
+    int32_t* counters;             // one per output tile, zero on entry, left zero on exit
+    int counter_cap;
+};
+
+// Scratch the GEMM may need for a problem of this shape (bytes of float
+// partials, number of tile counters).
+void gemm_scratch_need(int tokens, int n, int k, size_t* partial_bytes, int* counters);
+size_t gemm_partial_bound_bytes();      // upper bound over all shapes with tokens <= 64
+int gemm_counter_bound(int n);          // counters needed for an output of n features
+
+cudaError_t launch_gemm(const GemmProblem& p, cudaStream_t stream);
+
+int device_sm_count();
+
+// RMSNorm: out[t] = bf16(x[t] / sqrt(mean(x[t]^2) + eps) * g); also zeroes
+// `zero_words` int32 words at `zero_ptr` (tile counters) when non-null.
+cudaError_t launch_rmsnorm(const __nv_bfloat16* x, const float* g, __nv_bfloat16* out, int tokens,
+                           int hidden, float eps, int32_t* zero_ptr, int zero_words,
+                           cudaStream_t stream);
+
+cudaError_t launch_reshape_and_cache(const __nv_bfloat16* k, const __nv_bfloat16* v,
+                                     const int32_t* slots, int tokens, int n_kv_heads, int head_dim,
+                                     int block_size, __nv_bfloat16* k_pool, __nv_bfloat16* v_pool,
+                                     int num_blocks, int32_t* status, cudaStream_t stream);
+
+struct AttnPrefillArgs {
+    const __nv_bfloat16* q;        // [tokens, n_heads, d]
+    const __nv_bfloat16* k_pool;
+    const __nv_bfloat16* v_pool;
+    const int32_t* positions;      // [tokens]
+    const int32_t* block_table;
+    int max_blocks, num_blocks, block_size;
+    int batch, seq_len, n_heads, n_kv_heads, head_dim;
+    float scale;
+    __nv_bfloat16* out;            // [tokens, n_heads, d]
+    int32_t* status;
+};
+cudaError_t launch_attn_prefill(const AttnPrefillArgs& a, cudaStream_t stream);
+
+struct AttnDecodeArgs {
+    const __nv_bfloat16* q;        // [batch, n_heads, d]
+    const __nv_bfloat16* k_pool;
+    const __nv_bfloat16* v_pool;
+    const int32_t* context_lens;
+    const int32_t* block_table;
+    int max_blocks, num_blocks, block_size;
+    int batch, n_heads, n_kv_heads, head_dim;
+    float scale;
+    __nv_bfloat16* out;            // [batch, n_heads, d]
+    float* part_o;                 // scratch [batch, n_heads, max_splits, d]
+    float* part_ml;                // scratch [batch, n_heads, max_splits, 2]
+    int32_t* status;
+};
+int attn_decode_max_splits(int max_blocks, int block_size);
+size_t attn_decode_scratch_bytes(int batch, int n_heads, int head_dim, int max_blocks,
+                                 int block_size);
+cudaError_t launch_attn_decode(const AttnDecodeArgs& a, cudaStream_t stream);
+
+// Weight packing helpers.
+cudaError_t launch_pack_rows(const __nv_bfloat16* src, __nv_bfloat16* dst, int rows, int cols,
+                             int mode, int head_dim, int q_k_rows, cudaStream_t stream);
+cudaError_t launch_interleave_rows(const __nv_bfloat16* a, const __nv_bfloat16* b,
+                                   __nv_bfloat16* dst, int rows, int cols, cudaStream_t stream);
+cudaError_t launch_rope_table(float2* cs, int max_position, int head_dim, double theta,
+                              cudaStream_t stream);
+
+}  // namespace ll

@@ -1,0 +1,189 @@
+// Bandwidth-bound kernels of the decoder layer: RMSNorm, the standalone
+// ReshapeAndCache scatter, and the setup-time weight packing / RoPE table.
+#include <algorithm>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace ll {
+
+namespace {
+
+constexpr int kNormThreads = 256;
+
+// RMSNorm of one token row per CTA (chain page: "x -> RMSNorm"):
+// out = bf16(x * r * g), r = 1 / sqrt(mean(x^2) + eps), sums in float32.
+// The row is read twice; the second read comes from L1/L2.
+__global__ void __launch_bounds__(kNormThreads) rmsnorm_kernel(const __nv_bfloat16* __restrict__ x,
+                                                               const float* __restrict__ g,
+                                                               __nv_bfloat16* __restrict__ out,
+                                                               int hidden, float eps,
+                                                               int32_t* zero_ptr, int zero_words) {
+    const int t = blockIdx.x;
+    if (zero_ptr && t == 0)
+        for (int i = threadIdx.x; i < zero_words; i += blockDim.x) zero_ptr[i] = 0;
+    const uint4* xr = reinterpret_cast<const uint4*>(x + (size_t)t * hidden);
+    const int nv = hidden >> 3;
+    float ss = 0.f;
+    for (int i = threadIdx.x; i < nv; i += blockDim.x) {
+        uint4 u = xr[i];
+        uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            float a = bf16_lo(w[j]), b = bf16_hi(w[j]);
+            ss += a * a + b * b;
+        }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    __shared__ float red[kNormThreads / 32];
+    __shared__ float r_s;
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        float s = 0.f;
+        for (int i = 0; i < (int)(blockDim.x >> 5); ++i) s += red[i];
+        r_s = 1.0f / sqrtf(s / (float)hidden + eps);
+    }
+    __syncthreads();
+    const float r = r_s;
+    uint4* orow = reinterpret_cast<uint4*>(out + (size_t)t * hidden);
+    const float4* g4 = reinterpret_cast<const float4*>(g);
+    for (int i = threadIdx.x; i < nv; i += blockDim.x) {
+        uint4 u = xr[i];
+        float4 ga = g4[2 * i], gb = g4[2 * i + 1];
+        uint4 o;
+        o.x = pack_bf16x2(bf16_lo(u.x) * r * ga.x, bf16_hi(u.x) * r * ga.y);
+        o.y = pack_bf16x2(bf16_lo(u.y) * r * ga.z, bf16_hi(u.y) * r * ga.w);
+        o.z = pack_bf16x2(bf16_lo(u.z) * r * gb.x, bf16_hi(u.z) * r * gb.y);
+        o.w = pack_bf16x2(bf16_lo(u.w) * r * gb.z, bf16_hi(u.w) * r * gb.w);
+        orow[i] = o;
+    }
+}
+
+// ReshapeAndCache (paging page, ReshapeAndCacheOperation): one thread moves one
+// 16-byte vector of K and the matching vector of V of one (token, head).
+__global__ void reshape_and_cache_kernel(const uint4* __restrict__ k, const uint4* __restrict__ v,
+                                         const int32_t* __restrict__ slots, int tokens,
+                                         int n_kv_heads, int vec_per_row, int block_size,
+                                         uint4* __restrict__ k_pool, uint4* __restrict__ v_pool,
+                                         long long num_slots, int32_t* status) {
+    const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    const long long per_tok = (long long)n_kv_heads * vec_per_row;
+    if (idx >= per_tok * tokens) return;
+    const int t = (int)(idx / per_tok);
+    const int rem = (int)(idx - (long long)t * per_tok);
+    const int h = rem / vec_per_row;
+    const int c = rem - h * vec_per_row;
+    const int slot = slots[t];
+    if (slot < 0) return;
+    if ((long long)slot >= num_slots) {
+        if (h == 0 && c == 0) flag_status(status, LL_DEV_BAD_SLOT);
+        return;
+    }
+    const long long blk = slot / block_size;
+    const int off = slot - (int)blk * block_size;
+    const size_t dst = (((size_t)blk * n_kv_heads + h) * block_size + off) * vec_per_row + c;
+    k_pool[dst] = k[idx];
+    v_pool[dst] = v[idx];
+}
+
+// Packs rows of a [rows, cols] matrix.  mode 0: copy.  mode 1: the merged QKV
+// weight, whose first q_k_rows rows (the Q and K heads) are reordered inside
+// each head so that packed row 2i holds element i and row 2i+1 holds element
+// i + head_dim/2 (the two halves RoPE rotates together).
+__global__ void pack_rows_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst, int rows,
+                                 int vec_per_row, int mode, int head_dim, int q_k_rows) {
+    const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    if (idx >= (long long)rows * vec_per_row) return;
+    const int r = (int)(idx / vec_per_row);
+    const int c = (int)(idx - (long long)r * vec_per_row);
+    int sr = r;
+    if (mode == 1 && r < q_k_rows) {
+        const int head = r / head_dim;
+        const int e = r - head * head_dim;
+        sr = head * head_dim + ((e & 1) ? (e >> 1) + (head_dim >> 1) : (e >> 1));
+    }
+    dst[idx] = src[(size_t)sr * vec_per_row + c];
+}
+
+// Merged gate/up weight: packed row 2j = gate row j, row 2j+1 = up row j.
+__global__ void interleave_rows_kernel(const uint4* __restrict__ a, const uint4* __restrict__ b,
+                                       uint4* __restrict__ dst, int rows, int vec_per_row) {
+    const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    if (idx >= (long long)2 * rows * vec_per_row) return;
+    const int r = (int)(idx / vec_per_row);
+    const int c = (int)(idx - (long long)r * vec_per_row);
+    const uint4* src = (r & 1) ? b : a;
+    dst[idx] = src[(size_t)(r >> 1) * vec_per_row + c];
+}
+
+// RoPE table: cs[pos][i] = (cos, sin)(pos * theta^(-2i/d)), evaluated in float64.
+__global__ void rope_table_kernel(float2* cs, int max_position, int head_dim, double theta) {
+    const int half = head_dim >> 1;
+    const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    if (idx >= (long long)max_position * half) return;
+    const int pos = (int)(idx / half);
+    const int i = (int)(idx - (long long)pos * half);
+    const double inv_freq = pow(theta, -(2.0 * i) / (double)head_dim);
+    const double ang = (double)pos * inv_freq;
+    double s, c;
+    sincos(ang, &s, &c);
+    cs[idx] = make_float2((float)c, (float)s);
+}
+
+unsigned blocks_for(long long n, int threads) { return (unsigned)((n + threads - 1) / threads); }
+
+}  // namespace
+
+cudaError_t launch_rmsnorm(const __nv_bfloat16* x, const float* g, __nv_bfloat16* out, int tokens,
+                           int hidden, float eps, int32_t* zero_ptr, int zero_words,
+                           cudaStream_t stream) {
+    if (tokens <= 0) return cudaSuccess;
+    const int threads = std::min(kNormThreads, std::max(32, ((hidden / 8 + 31) / 32) * 32));
+    rmsnorm_kernel<<<tokens, threads, 0, stream>>>(x, g, out, hidden, eps, zero_ptr, zero_words);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_reshape_and_cache(const __nv_bfloat16* k, const __nv_bfloat16* v,
+                                     const int32_t* slots, int tokens, int n_kv_heads, int head_dim,
+                                     int block_size, __nv_bfloat16* k_pool, __nv_bfloat16* v_pool,
+                                     int num_blocks, int32_t* status, cudaStream_t stream) {
+    if (tokens <= 0) return cudaSuccess;
+    const int vpr = head_dim / 8;
+    const long long n = (long long)tokens * n_kv_heads * vpr;
+    reshape_and_cache_kernel<<<blocks_for(n, 256), 256, 0, stream>>>(
+        reinterpret_cast<const uint4*>(k), reinterpret_cast<const uint4*>(v), slots, tokens,
+        n_kv_heads, vpr, block_size, reinterpret_cast<uint4*>(k_pool), reinterpret_cast<uint4*>(v_pool),
+        (long long)num_blocks * block_size, status);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_pack_rows(const __nv_bfloat16* src, __nv_bfloat16* dst, int rows, int cols,
+                             int mode, int head_dim, int q_k_rows, cudaStream_t stream) {
+    const int vpr = cols / 8;
+    const long long n = (long long)rows * vpr;
+    pack_rows_kernel<<<blocks_for(n, 256), 256, 0, stream>>>(reinterpret_cast<const uint4*>(src),
+                                                             reinterpret_cast<uint4*>(dst), rows, vpr,
+                                                             mode, head_dim, q_k_rows);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_interleave_rows(const __nv_bfloat16* a, const __nv_bfloat16* b,
+                                   __nv_bfloat16* dst, int rows, int cols, cudaStream_t stream) {
+    const int vpr = cols / 8;
+    const long long n = 2LL * rows * vpr;
+    interleave_rows_kernel<<<blocks_for(n, 256), 256, 0, stream>>>(
+        reinterpret_cast<const uint4*>(a), reinterpret_cast<const uint4*>(b),
+        reinterpret_cast<uint4*>(dst), rows, vpr);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_rope_table(float2* cs, int max_position, int head_dim, double theta,
+                              cudaStream_t stream) {
+    const long long n = (long long)max_position * (head_dim / 2);
+    rope_table_kernel<<<blocks_for(n, 256), 256, 0, stream>>>(cs, max_position, head_dim, theta);
+    return cudaGetLastError();
+}
+
+}  // namespace ll
