@@ -58,8 +58,8 @@ extern "C" {
 #define LL_DEV_TIMEOUT 8       /* a bounded in-kernel wait gave up */
 
 /* Layer shape.  head_dim must be 64 or 128; n_heads % n_kv_heads == 0;
- * hidden and intermediate multiples of 16 (>= 64); block_size a power of two
- * in [16, 256]; max_position = rows of the RoPE table (largest position + 1).
+ * n_heads / n_kv_heads <= 16; hidden and intermediate multiples of 16;
+ * block_size >= 1; max_position = rows of the RoPE table (largest position + 1).
  * RoPE uses half-split pairs and angle pos * rope_theta^(-2i/head_dim). */
 typedef struct {
     int32_t hidden;
@@ -97,6 +97,11 @@ typedef struct {
 /* Human-readable name of an LL_ERR_* code (static string). */
 const char* ll_strerror(int code);
 
+/* Description of the last failure behind an LL_ERR_* return on the calling
+ * thread (the failing step and CUDA's message), or "" if none.  Valid until
+ * the thread's next library call. */
+const char* ll_last_error(void);
+
 /* Bytes of the packed-weight buffer for `cfg` (0 if cfg is invalid). */
 size_t ll_packed_weights_size(const ll_config* cfg);
 
@@ -132,7 +137,7 @@ int ll_layer_prefill(const ll_config* cfg, const void* packed, const void* x,
  * context_lens (int32 [batch]) counts each sequence's cache INCLUDING the new
  * token, which is written at position context_lens[b] - 1; its query attends
  * over positions 0..context_lens[b]-1.  y BF16 [batch, hidden].  The chain
- * page's decode path (one-row query against the cached K/V); batch <= 256. */
+ * page's decode path (one-row query against the cached K/V). */
 int ll_layer_decode_step(const ll_config* cfg, const void* packed, const void* x,
                          const ll_kv_pool* pool, const int32_t* block_table, int32_t max_blocks,
                          const int32_t* context_lens, int32_t batch, void* y, void* workspace,

@@ -26,7 +26,7 @@ LL_DEV_BAD_POSITION = 4
 LL_DEV_TIMEOUT = 8
 
 EXPORTED = [
-    "ll_strerror", "ll_packed_weights_size", "ll_pack_weights", "ll_workspace_size",
+    "ll_strerror", "ll_last_error", "ll_packed_weights_size", "ll_pack_weights", "ll_workspace_size",
     "ll_layer_prefill", "ll_layer_decode_step", "ll_reshape_and_cache",
     "ll_attention_workspace_size", "ll_paged_attention_decode", "ll_linear_workspace_size",
     "ll_linear", "ll_device_sm_count",
@@ -61,6 +61,7 @@ def _load():
     poolp = ctypes.POINTER(ll_kv_pool)
     sig = {
         "ll_strerror": (ctypes.c_char_p, [ctypes.c_int]),
+        "ll_last_error": (ctypes.c_char_p, []),
         "ll_packed_weights_size": (S, [cfgp]),
         "ll_pack_weights": (ctypes.c_int, [cfgp, ctypes.POINTER(ll_weights), P, S, P]),
         "ll_workspace_size": (S, [cfgp, I32, I32]),
@@ -86,7 +87,9 @@ lib = _load()
 
 class LayerError(RuntimeError):
     def __init__(self, name, code):
-        super().__init__(f"{name}: {lib.ll_strerror(code).decode()} (code {code})")
+        detail = lib.ll_last_error().decode()
+        super().__init__(f"{name}: {lib.ll_strerror(code).decode()} (code {code})"
+                         + (f" -- {detail}" if detail else ""))
         self.code = code
 
 

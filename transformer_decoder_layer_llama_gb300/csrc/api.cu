@@ -16,6 +16,7 @@
 
 #include <algorithm>
 #include <cmath>
+#include <cstdio>
 #include <cstring>
 
 #include "../../include/llama_layer.h"
@@ -123,6 +124,8 @@ WsLayout ws_layout(const ll_config* c, int T, int max_blocks) {
 }
 
 int cuda_rc(cudaError_t e) { return e == cudaSuccess ? LL_OK : LL_ERR_CUDA; }
+
+thread_local char g_last_error[512];
 
 bool pool_ok(const ll_kv_pool* p) {
     return p && p->k && p->v && p->num_blocks > 0 && aligned16(p->k) && aligned16(p->v);
@@ -282,7 +285,20 @@ int run_layer(const ll_config* cfg, const void* packed, const void* x, const int
 
 }  // namespace
 
+namespace ll {
+void set_last_error(const char* where, const char* what) {
+    snprintf(g_last_error, sizeof(g_last_error), "%s: %s", where, what);
+}
+void clear_last_error() { g_last_error[0] = 0; }
+cudaError_t record(cudaError_t e, const char* where) {
+    if (e != cudaSuccess) set_last_error(where, cudaGetErrorString(e));
+    return e;
+}
+}  // namespace ll
+
 extern "C" {
+
+const char* ll_last_error(void) { return g_last_error; }
 
 const char* ll_strerror(int code) {
     switch (code) {
@@ -304,6 +320,7 @@ size_t ll_packed_weights_size(const ll_config* cfg) {
 
 int ll_pack_weights(const ll_config* cfg, const ll_weights* w, void* packed, size_t packed_bytes,
                     void* stream_) {
+    ll::clear_last_error();
     int rc = config_supported(cfg);
     if (rc != LL_OK) return rc;
     if (!w || !w->w_qkv || !w->w_o || !w->w_gate || !w->w_up || !w->w_down || !w->g_attn ||
@@ -338,15 +355,15 @@ int ll_pack_weights(const ll_config* cfg, const ll_weights* w, void* packed, siz
                                   reinterpret_cast<__nv_bfloat16*>(base + L.down), H, I, 0, d, 0,
                                   s)) != cudaSuccess)
         return LL_ERR_CUDA;
-    if (cudaMemcpyAsync(base + L.g_attn, w->g_attn, (size_t)H * 4, cudaMemcpyDeviceToDevice, s) !=
-            cudaSuccess ||
-        cudaMemcpyAsync(base + L.g_ffn, w->g_ffn, (size_t)H * 4, cudaMemcpyDeviceToDevice, s) !=
-            cudaSuccess)
+    if (ll::record(cudaMemcpyAsync(base + L.g_attn, w->g_attn, (size_t)H * 4,
+                                   cudaMemcpyDeviceToDevice, s), "cudaMemcpyAsync(g_attn)") != cudaSuccess ||
+        ll::record(cudaMemcpyAsync(base + L.g_ffn, w->g_ffn, (size_t)H * 4,
+                                   cudaMemcpyDeviceToDevice, s), "cudaMemcpyAsync(g_ffn)") != cudaSuccess)
         return LL_ERR_CUDA;
     if ((e = ll::launch_rope_table(reinterpret_cast<float2*>(base + L.rope), cfg->max_position, d,
                                    (double)cfg->rope_theta, s)) != cudaSuccess)
         return LL_ERR_CUDA;
-    return cuda_rc(cudaStreamSynchronize(s));
+    return cuda_rc(ll::record(cudaStreamSynchronize(s), "cudaStreamSynchronize(pack)"));
 }
 
 size_t ll_workspace_size(const ll_config* cfg, int32_t max_tokens, int32_t max_blocks) {
@@ -359,6 +376,7 @@ int ll_layer_prefill(const ll_config* cfg, const void* packed, const void* x,
                      const ll_kv_pool* pool, const int32_t* block_table, int32_t max_blocks,
                      void* y, void* workspace, size_t workspace_bytes, int32_t* status,
                      void* stream) {
+    ll::clear_last_error();
     int rc = config_supported(cfg);
     if (rc != LL_OK) return rc;
     if (!packed || !x || !positions || !block_table || !y || !status || !pool_ok(pool))
@@ -375,6 +393,7 @@ int ll_layer_decode_step(const ll_config* cfg, const void* packed, const void* x
                          const ll_kv_pool* pool, const int32_t* block_table, int32_t max_blocks,
                          const int32_t* context_lens, int32_t batch, void* y, void* workspace,
                          size_t workspace_bytes, int32_t* status, void* stream) {
+    ll::clear_last_error();
     int rc = config_supported(cfg);
     if (rc != LL_OK) return rc;
     if (!packed || !x || !context_lens || !block_table || !y || !status || !pool_ok(pool))
@@ -389,6 +408,7 @@ int ll_layer_decode_step(const ll_config* cfg, const void* packed, const void* x
 int ll_reshape_and_cache(const void* k, const void* v, const int32_t* slot_mapping, int32_t tokens,
                          int32_t n_kv_heads, int32_t head_dim, int32_t block_size,
                          const ll_kv_pool* pool, int32_t* status, void* stream) {
+    ll::clear_last_error();
     if (!k || !v || !slot_mapping || !status || !pool_ok(pool)) return LL_ERR_INVALID_ARG;
     if (tokens < 0 || n_kv_heads <= 0 || head_dim <= 0 || block_size <= 0)
         return LL_ERR_INVALID_ARG;
@@ -412,6 +432,7 @@ int ll_paged_attention_decode(const void* q, const ll_kv_pool* pool, const int32
                               int32_t n_heads, int32_t n_kv_heads, int32_t head_dim,
                               int32_t block_size, float scale, void* out, void* workspace,
                               size_t workspace_bytes, int32_t* status, void* stream) {
+    ll::clear_last_error();
     if (!q || !block_table || !context_lens || !out || !status || !pool_ok(pool))
         return LL_ERR_INVALID_ARG;
     if (batch <= 0 || n_heads <= 0 || n_kv_heads <= 0 || max_blocks <= 0 || block_size <= 0)
@@ -453,6 +474,7 @@ size_t ll_linear_workspace_size(int32_t m, int32_t n, int32_t k) {
 
 int ll_linear(const void* x, const void* w, void* y, int32_t m, int32_t n, int32_t k,
               void* workspace, size_t workspace_bytes, int32_t* status, void* stream) {
+    ll::clear_last_error();
     if (!x || !w || !y || !status) return LL_ERR_INVALID_ARG;
     if (m <= 0 || n <= 0 || k <= 0) return LL_ERR_INVALID_ARG;
     if (n % 16 != 0 || k % 16 != 0) return LL_ERR_UNSUPPORTED;
@@ -479,7 +501,8 @@ int ll_linear(const void* x, const void* w, void* y, int32_t m, int32_t n, int32
     g.ep.out = static_cast<__nv_bfloat16*>(y);
     g.ep.ld_out = n;
     g.ep.status = status;
-    if (cw > 0 && cudaMemsetAsync(g.counters, 0, (size_t)cw * 4, s) != cudaSuccess)
+    if (cw > 0 && ll::record(cudaMemsetAsync(g.counters, 0, (size_t)cw * 4, s),
+                             "cudaMemsetAsync(counters)") != cudaSuccess)
         return LL_ERR_CUDA;
     return cuda_rc(ll::launch_gemm(g, s));
 }

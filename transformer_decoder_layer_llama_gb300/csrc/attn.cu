@@ -513,12 +513,12 @@ cudaError_t prefill_for(const AttnPrefillArgs& a, cudaStream_t stream) {
     if (!configured) {
         cudaError_t e = cudaFuncSetAttribute(attn_prefill_kernel<D>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
+        if (e != cudaSuccess) return record(e, "cudaFuncSetAttribute(attn_prefill_kernel)");
         configured = true;
     }
     dim3 grid((a.seq_len + 127) / 128, a.n_heads, a.batch);
     attn_prefill_kernel<D><<<grid, 256, smem, stream>>>(a);
-    return cudaGetLastError();
+    return record(cudaGetLastError(), "attn_prefill_kernel launch");
 }
 
 template <int D>
@@ -529,15 +529,15 @@ cudaError_t decode_for(const AttnDecodeArgs& a, cudaStream_t stream) {
     if (!configured) {
         cudaError_t e = cudaFuncSetAttribute(attn_decode_split_kernel<D>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
+        if (e != cudaSuccess) return record(e, "cudaFuncSetAttribute(attn_decode_split_kernel)");
         configured = true;
     }
     dim3 grid(max_splits, a.n_kv_heads, a.batch);
     attn_decode_split_kernel<D><<<grid, 128, smem, stream>>>(a, max_splits);
     cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
+    if (e != cudaSuccess) return record(e, "attn_decode_split_kernel launch");
     attn_decode_combine_kernel<<<dim3(a.n_heads, a.batch), D, 0, stream>>>(a, max_splits);
-    return cudaGetLastError();
+    return record(cudaGetLastError(), "attn_decode_combine_kernel launch");
 }
 
 }  // namespace

@@ -26,6 +26,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <cstdio>
 #include <mutex>
 
 #include "common.cuh"
@@ -507,7 +508,10 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 // 2-D BF16 tensor [rows, inner] row-major, box [box_rows, 64] with the 128-byte swizzle.
 bool make_tmap(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t rows, uint32_t box_rows) {
     auto fn = encode_fn();
-    if (!fn) return false;
+    if (!fn) {
+        set_last_error("cuTensorMapEncodeTiled", "driver entry point not found");
+        return false;
+    }
     cuuint64_t dims[2] = {inner, rows};
     cuuint64_t strides[1] = {inner * 2};
     cuuint32_t box[2] = {(cuuint32_t)BK, box_rows};
@@ -515,7 +519,14 @@ bool make_tmap(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t rows, u
     CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides,
                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS;
+    if (r != CUDA_SUCCESS) {
+        char msg[160];
+        snprintf(msg, sizeof(msg), "CUresult %d (inner %llu, rows %llu, box %u x %u)", (int)r,
+                 (unsigned long long)inner, (unsigned long long)rows, (unsigned)BK, box_rows);
+        set_last_error("cuTensorMapEncodeTiled", msg);
+        return false;
+    }
+    return true;
 }
 
 int ceil_div(int a, int b) { return (a + b - 1) / b; }
@@ -614,8 +625,10 @@ cudaError_t launch_gemm(const GemmProblem& pr, cudaStream_t stream) {
     a.counters = pr.counters;
     if (p.splits > 1) {
         size_t need = (size_t)p.tiles_m * p.splits * BM * p.bn * sizeof(float);
-        if (!pr.partials || pr.partial_bytes < need || !pr.counters || pr.counter_cap < p.tiles_m)
+        if (!pr.partials || pr.partial_bytes < need || !pr.counters || pr.counter_cap < p.tiles_m) {
+            set_last_error("launch_gemm", "split-K scratch too small");
             return cudaErrorInvalidValue;
+        }
     }
     CUtensorMap tmA, tmB;
     bool ok;
@@ -627,14 +640,15 @@ cudaError_t launch_gemm(const GemmProblem& pr, cudaStream_t stream) {
     if (!ok) return cudaErrorInvalidValue;
     static int configured_smem = 0;
     if ((int)p.smem_bytes > configured_smem) {
+        // dynamic + static shared memory must fit the per-block opt-in limit
         cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             227 * 1024);
-        if (e != cudaSuccess) return e;
-        configured_smem = 227 * 1024;
+                                             (int)p.smem_bytes);
+        if (e != cudaSuccess) return record(e, "cudaFuncSetAttribute(gemm_tc_kernel)");
+        configured_smem = (int)p.smem_bytes;
     }
     int grid = std::min(p.units, sms * p.ctas_per_sm);
     gemm_tc_kernel<<<grid, kThreads, p.smem_bytes, stream>>>(tmA, tmB, a);
-    return cudaGetLastError();
+    return record(cudaGetLastError(), "gemm_tc_kernel launch");
 }
 
 }  // namespace ll

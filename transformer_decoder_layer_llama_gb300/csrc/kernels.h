@@ -61,6 +61,11 @@ cudaError_t launch_gemm(const GemmProblem& p, cudaStream_t stream);
 
 int device_sm_count();
 
+// Records why the current call failed (thread-local; read by ll_last_error).
+void set_last_error(const char* where, const char* what);
+void clear_last_error();
+cudaError_t record(cudaError_t e, const char* where);
+
 // RMSNorm: out[t] = bf16(x[t] / sqrt(mean(x[t]^2) + eps) * g); also zeroes
 // `zero_words` int32 words at `zero_ptr` (tile counters) when non-null.
 cudaError_t launch_rmsnorm(const __nv_bfloat16* x, const float* g, __nv_bfloat16* out, int tokens,

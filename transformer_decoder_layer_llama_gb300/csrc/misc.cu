@@ -142,7 +142,7 @@ cudaError_t launch_rmsnorm(const __nv_bfloat16* x, const float* g, __nv_bfloat16
     if (tokens <= 0) return cudaSuccess;
     const int threads = std::min(kNormThreads, std::max(32, ((hidden / 8 + 31) / 32) * 32));
     rmsnorm_kernel<<<tokens, threads, 0, stream>>>(x, g, out, hidden, eps, zero_ptr, zero_words);
-    return cudaGetLastError();
+    return record(cudaGetLastError(), "rmsnorm launch");
 }
 
 cudaError_t launch_reshape_and_cache(const __nv_bfloat16* k, const __nv_bfloat16* v,
@@ -156,7 +156,7 @@ cudaError_t launch_reshape_and_cache(const __nv_bfloat16* k, const __nv_bfloat16
         reinterpret_cast<const uint4*>(k), reinterpret_cast<const uint4*>(v), slots, tokens,
         n_kv_heads, vpr, block_size, reinterpret_cast<uint4*>(k_pool), reinterpret_cast<uint4*>(v_pool),
         (long long)num_blocks * block_size, status);
-    return cudaGetLastError();
+    return record(cudaGetLastError(), "reshape_and_cache launch");
 }
 
 cudaError_t launch_pack_rows(const __nv_bfloat16* src, __nv_bfloat16* dst, int rows, int cols,
@@ -166,7 +166,7 @@ cudaError_t launch_pack_rows(const __nv_bfloat16* src, __nv_bfloat16* dst, int r
     pack_rows_kernel<<<blocks_for(n, 256), 256, 0, stream>>>(reinterpret_cast<const uint4*>(src),
                                                              reinterpret_cast<uint4*>(dst), rows, vpr,
                                                              mode, head_dim, q_k_rows);
-    return cudaGetLastError();
+    return record(cudaGetLastError(), "pack_rows launch");
 }
 
 cudaError_t launch_interleave_rows(const __nv_bfloat16* a, const __nv_bfloat16* b,
@@ -176,14 +176,14 @@ cudaError_t launch_interleave_rows(const __nv_bfloat16* a, const __nv_bfloat16* 
     interleave_rows_kernel<<<blocks_for(n, 256), 256, 0, stream>>>(
         reinterpret_cast<const uint4*>(a), reinterpret_cast<const uint4*>(b),
         reinterpret_cast<uint4*>(dst), rows, vpr);
-    return cudaGetLastError();
+    return record(cudaGetLastError(), "interleave_rows launch");
 }
 
 cudaError_t launch_rope_table(float2* cs, int max_position, int head_dim, double theta,
                               cudaStream_t stream) {
     const long long n = (long long)max_position * (head_dim / 2);
     rope_table_kernel<<<blocks_for(n, 256), 256, 0, stream>>>(cs, max_position, head_dim, theta);
-    return cudaGetLastError();
+    return record(cudaGetLastError(), "rope_table launch");
 }
 
 }  // namespace ll
