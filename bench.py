@@ -1,0 +1,480 @@
+"""Throughput of one Llama-style decoder layer on GB300.
+
+Headline workload: a Llama-2-7B-shaped layer, prefill of one sequence of 2048
+tokens (hidden 4096, 32 heads x 128, FFN 11008, paged KV with 128-token
+blocks); `value` is its TFLOP/s (GEMM FLOPs + causal attention FLOPs per
+step / device time).  The same line carries the decode steps of the 7B layer
+(batch 64, context ~U[512, 4096]) and of the 70B-shaped GQA layer (batch 16,
+context ~U[4096, 32768]) as HBM GB/s and tokens/s, each with its fraction of
+the roofline max(FLOPs / BF16 peak, minimum bytes / HBM bandwidth).
+
+Weights are random-init BF16 ~ N(0, 0.02^2) (0.01 for 70B), inputs N(0, 1),
+drawn on the device from a seeded generator.  Between timed steps a 256 MB
+buffer is overwritten to flush the 129 MB L2; each step is timed with its own
+CUDA events on the launching stream, so the flush is outside the timed time.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun (N > 1) every rank runs an independent replica of the
+workload (the layer does not shard; there is no collective on the data
+path); rank 0 prints value = all ranks' work / the slowest rank's time.
+`--impl reference` times the CPU oracle instead (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from transformer_decoder_layer_llama_gb300 import synth  # noqa: E402
+
+METRIC = "decode-layer HBM GB/s & tok/s; prefill-layer TFLOP/s; % of roofline, 1×GB300"
+L2_FLUSH_BYTES = 256 << 20
+
+
+# ---------------------------------------------------------------- work accounting
+
+def gemm_flops(d, T):
+    nqkv = (d.n_heads + 2 * d.n_kv_heads) * d.head_dim
+    per_tok = nqkv * d.hidden + d.hidden * d.n_heads * d.head_dim + 2 * d.intermediate * d.hidden \
+        + d.hidden * d.intermediate
+    return 2.0 * T * per_tok
+
+
+def weight_bytes(d):
+    return gemm_flops(d, 1) / 2 * 2          # one BF16 per multiply-add of a single token
+
+
+def attn_flops(d, key_counts):
+    """QK^T and PV: 4 * head_dim flops per (query head, visible key)."""
+    return 4.0 * d.head_dim * d.n_heads * float(np.sum(key_counts, dtype=np.float64))
+
+
+def kv_bytes_read(d, ctx):
+    return 2.0 * d.n_kv_heads * d.head_dim * 2 * float(np.sum(ctx, dtype=np.float64))
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            j = json.load(f)
+        return {"hbm_gbs": float(j["hbm_gbs"]), "bf16_tflops": float(j["bf16_tflops"]),
+                "bf16_tflops_sustained": float(j.get("bf16_tflops_sustained", j["bf16_tflops"])),
+                "source": "measured"}
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+                "source": "fallback"}
+
+
+# ---------------------------------------------------------------- clocks
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"bench_clocks_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100", "-i", str(self.gpu)], stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.f.close()
+        return False
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return None
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": smax, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- device workloads
+
+def dev_normal(shape, std, gen, dtype=torch.bfloat16):
+    t = torch.randn(*shape, generator=gen, device="cuda", dtype=torch.float32)
+    if std != 1.0:
+        t.mul_(std)
+    return t.to(dtype)
+
+
+def device_layer(api, d, w_std, max_position, seed):
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(seed)
+    H, I = d.hidden, d.intermediate
+    W = {
+        "w_qkv": dev_normal((d.qkv_rows, H), w_std, gen),
+        "w_o": dev_normal((H, d.n_heads * d.head_dim), w_std, gen),
+        "w_gate": dev_normal((I, H), w_std, gen),
+        "w_up": dev_normal((I, H), w_std, gen),
+        "w_down": dev_normal((H, I), w_std, gen),
+        "g_attn": 1 + 0.1 * torch.randn(H, generator=gen, device="cuda"),
+        "g_ffn": 1 + 0.1 * torch.randn(H, generator=gen, device="cuda"),
+    }
+    cfg = api.make_config(d, max_position)
+    packed = api.pack_weights(cfg, W)
+    del W
+    torch.cuda.empty_cache()
+    return cfg, packed, gen
+
+
+class Prefill:
+    def __init__(self, api, wl, seed):
+        d = wl.dims
+        self.api, self.d = api, d
+        self.B, self.S = wl.batch, wl.prefill_len
+        self.T = self.B * self.S
+        self.cfg, self.packed, gen = device_layer(api, d, wl.w_std, self.S, seed)
+        table, nb = synth.make_block_table([self.S] * self.B, d.block_size, seed + 1, extra_blocks=4)
+        self.table = table.cuda()
+        shape = (nb, d.n_kv_heads, d.block_size, d.head_dim)
+        self.kp = torch.zeros(shape, dtype=torch.bfloat16, device="cuda")
+        self.vp = torch.zeros(shape, dtype=torch.bfloat16, device="cuda")
+        self.x = dev_normal((self.T, d.hidden), 1.0, gen)
+        self.pos = synth.prefill_positions(self.B, self.S).cuda()
+        self.y = torch.empty_like(self.x)
+        self.ws = api.new_workspace(self.cfg, self.T, self.table.shape[1])
+        self.status = api.new_status()
+        keys = np.tile(np.arange(1, self.S + 1), self.B)
+        self.flops = gemm_flops(d, self.T) + attn_flops(d, keys)
+        self.gemm_flops = gemm_flops(d, self.T)
+        self.min_bytes = weight_bytes(d) + 2 * self.T * d.hidden * 2 + kv_bytes_read(d, [self.T])
+
+    def step(self, stream):
+        self.api.layer_prefill(self.cfg, self.packed, self.x, self.pos, self.B, self.S, self.kp,
+                               self.vp, self.table, y=self.y, workspace=self.ws,
+                               status=self.status, stream=stream)
+
+    def roofline_s(self, peaks):
+        return max(self.flops / (peaks["bf16_tflops"] * 1e12), self.min_bytes / (peaks["hbm_gbs"] * 1e9))
+
+
+class Decode:
+    def __init__(self, api, wl, seed):
+        d = wl.dims
+        self.api, self.d = api, d
+        self.B = wl.batch
+        ctx = synth.make_context_lens(self.B, wl.ctx_lo, wl.ctx_hi, seed + 2)
+        self.ctx_np = ctx.numpy()
+        self.cfg, self.packed, gen = device_layer(api, d, wl.w_std, int(ctx.max()) + 1, seed)
+        table, nb = synth.make_block_table(ctx.tolist(), d.block_size, seed + 1, extra_blocks=4)
+        self.table = table.cuda()
+        shape = (nb, d.n_kv_heads, d.block_size, d.head_dim)
+        self.kp = dev_normal(shape, 1.0, gen)
+        self.vp = dev_normal(shape, 1.0, gen)
+        self.ctx = ctx.cuda()
+        self.x = dev_normal((self.B, d.hidden), 1.0, gen)
+        self.y = torch.empty_like(self.x)
+        self.ws = api.new_workspace(self.cfg, self.B, self.table.shape[1])
+        self.status = api.new_status()
+        self.flops = gemm_flops(d, self.B) + attn_flops(d, self.ctx_np)
+        self.kv_read = kv_bytes_read(d, self.ctx_np)
+        self.min_bytes = (weight_bytes(d) + self.kv_read + 2 * self.B * d.hidden * 2
+                          + self.B * 2 * d.n_kv_heads * d.head_dim * 2)
+
+    def step(self, stream):
+        self.api.layer_decode_step(self.cfg, self.packed, self.x, self.kp, self.vp, self.table,
+                                   self.ctx, y=self.y, workspace=self.ws, status=self.status,
+                                   stream=stream)
+
+    def roofline_s(self, peaks):
+        return max(self.flops / (peaks["bf16_tflops"] * 1e12), self.min_bytes / (peaks["hbm_gbs"] * 1e9))
+
+
+def timed_steps(work, steps, stream, flush):
+    """Device time of `steps` steps, each bracketed by its own events, L2 flushed between."""
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(steps)]
+    with torch.cuda.stream(stream):
+        for a, b in evs:
+            flush.fill_(1)
+            a.record(stream)
+            work.step(stream)
+            b.record(stream)
+    stream.synchronize()
+    return sum(a.elapsed_time(b) for a, b in evs)
+
+
+def traced_breakdown(api, work, steps, stream, flush):
+    with torch.cuda.stream(stream):
+        with api.trace(capacity=64 * steps) as tr:
+            for _ in range(steps):
+                flush.fill_(2)
+                work.step(stream)
+    stream.synchronize()
+    per = {}
+    for name, ms in tr.launches():
+        e = per.setdefault(name, {"launches": 0, "ms": 0.0})
+        e["launches"] += 1
+        e["ms"] += ms
+    total = sum(v["ms"] for v in per.values())
+    for v in per.values():
+        v["share"] = v["ms"] / total if total else 0.0
+    return per, tr.count // max(steps, 1)
+
+
+# ---------------------------------------------------------------- oracle (CPU) throughput
+
+def oracle_prefill_sample(wl, budget_s, chunk, seed=7, max_steps=None):
+    """Times the CPU oracle on chunks of `chunk` tokens of the 7B prefill workload, centred on
+    position S/2 (so the attention share matches the whole sequence's average), over a
+    pre-filled cache prefix; repeats until budget_s has passed.  Returns (TFLOP/s, steps,
+    description)."""
+    from oracle import llama_layer as O
+    d = wl.dims
+    S = wl.prefill_len
+    W = synth.make_weights(d, wl.w_std, seed)
+    Wn = {k: v.float().numpy().astype(np.float64) for k, v in W.items()}
+    start = S // 2 - chunk // 2
+    table, nb = synth.make_block_table([S], d.block_size, seed + 1)
+    kp, vp = synth.make_pool(nb, d, seed + 2)
+    kpo = kp.view(torch.int16).numpy().view(np.uint16)
+    vpo = vp.view(torch.int16).numpy().view(np.uint16)
+    x = synth.make_x(chunk, d.hidden, seed + 3).float().numpy().astype(np.float64)
+    pos = np.arange(start, start + chunk)
+    flops = gemm_flops(d, chunk) + attn_flops(d, pos + 1)
+    t_total, n = 0.0, 0
+    while True:
+        t0 = time.perf_counter()
+        O.layer_prefill(d, Wn, x, pos, 1, chunk, kpo, vpo, table.numpy())
+        t_total += time.perf_counter() - t0
+        n += 1
+        if (max_steps is not None and n >= max_steps) or (max_steps is None and t_total >= budget_s):
+            break
+    desc = (f"oracle (numpy float64) on {n} x {chunk}-token chunks of the 2048-token 7B prefill "
+            f"at positions {start}..{start + chunk - 1} over a pre-filled cache prefix")
+    return flops * n / t_total / 1e12, n, desc
+
+
+def host_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+# ---------------------------------------------------------------- main
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-extras", action="store_true", help="skip the decode workloads")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the oracle CPU baseline")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    wl = synth.WORKLOADS["llama2_7b_prefill"]
+    cfg_json = {"workload": "llama2_7b_layer_prefill", "hidden": 4096, "heads": 32, "kv_heads": 32,
+                "head_dim": 128, "intermediate": 11008, "batch": 1, "seq_len": 2048,
+                "block_size": 128, "parallelism": f"replicas{max(world, args.gpus)}",
+                "l2": "flushed between timed steps (256 MB write)"}
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        # bounded oracle sample per step: size the chunk so K + W steps end in ~3 minutes
+        probe, _, _ = oracle_prefill_sample(wl, 0.0, 16, max_steps=1)
+        per_tok_s = gemm_flops(wl.dims, 1) / (probe * 1e12)
+        chunk = int(max(4, min(256, 150.0 / max(args.steps + args.warmup, 1) / max(per_tok_s, 1e-6))))
+        oracle_prefill_sample(wl, 0.0, chunk, max_steps=args.warmup)
+        t0 = time.perf_counter()
+        v, n, desc = oracle_prefill_sample(wl, 0.0, chunk, max_steps=args.steps)
+        wall = time.perf_counter() - t0
+        line = {"metric": METRIC, "impl": "reference", "value": v, "unit": "TFLOP/s",
+                "n_gpus": 0, "steps": args.steps, "warmup": args.warmup,
+                "ms_per_step": wall / max(n, 1) * 1e3, "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+                "config": cfg_json,
+                "cpu_baseline": {"value": v, "unit": "TFLOP/s", "cores": host_cores(),
+                                 "kind": "oracle", "sample": desc},
+                "e2e": {"value": v, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}}
+        print(json.dumps(line))
+        return
+
+    from transformer_decoder_layer_llama_gb300 import api
+
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    else:
+        torch.cuda.set_device(0)
+    dev_index = torch.cuda.current_device()
+    peaks = load_peaks()
+    stream = torch.cuda.Stream()
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
+
+    work = Prefill(api, wl, seed=1234 + rank)
+    for _ in range(args.warmup):
+        work.step(stream)
+    stream.synchronize()
+
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(dev_index) as clocks:
+        ms = timed_steps(work, args.steps, stream, flush)
+    torch.cuda.synchronize()
+    if world > 1:
+        t = torch.tensor([ms], device="cuda", dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+        dist.barrier()
+    ms_step = ms / args.steps
+    value = world * work.flops / (ms_step * 1e-3) / 1e12
+    st = int(work.status.item())
+
+    per, launches_per_step = traced_breakdown(api, work, min(args.steps, 50), stream, flush)
+    g = per.get("gemm_tc", {"ms": 0.0, "launches": 0})
+    n_tr = min(args.steps, 50)
+    gemm_ms_step = g["ms"] / n_tr
+    gemm_tflops = work.gemm_flops / (gemm_ms_step * 1e-3) / 1e12 if gemm_ms_step > 0 else 0.0
+    roof = {"bound": "tensor", "kernel": "gemm_tc", "achieved": gemm_tflops,
+            "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+            "frac": gemm_tflops / peaks["bf16_tflops"], "traffic": None,
+            "peak_kind": f"{peaks['source']} burst cuBLAS bf16"}
+
+    # end to end through the public API with host buffers: H2D inputs, layer, D2H output
+    x_h = work.x.cpu().pin_memory()
+    pos_h = work.pos.cpu().pin_memory()
+    tab_h = work.table.cpu().pin_memory()
+    y_h = torch.empty_like(x_h).pin_memory()
+    e2e_steps = max(3, min(args.steps, 50))
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(e2e_steps)]
+    with torch.cuda.stream(stream):
+        for a, b in evs:
+            flush.fill_(3)
+            a.record(stream)
+            work.x.copy_(x_h, non_blocking=True)
+            work.pos.copy_(pos_h, non_blocking=True)
+            work.table.copy_(tab_h, non_blocking=True)
+            work.step(stream)
+            y_h.copy_(work.y, non_blocking=True)
+            b.record(stream)
+    stream.synchronize()
+    e2e_ms = sum(a.elapsed_time(b) for a, b in evs) / e2e_steps
+    h2d = x_h.numel() * 2 + pos_h.numel() * 4 + tab_h.numel() * 4
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic", "config": cfg_json,
+        "layer_roofline_frac": work.roofline_s(peaks) / (ms_step * 1e-3),
+        "roofline": roof,
+        "e2e": {"value": world * work.flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": y_h.numel() * 2},
+        "gpu_launches": launches_per_step * args.steps,
+        "kernels": {k: {"launches_per_step": v["launches"] // n_tr, "ms_per_step": v["ms"] / n_tr,
+                        "share": v["share"]} for k, v in per.items()},
+        "clocks": clocks.summary(),
+        "device_status": st,
+        "peaks": peaks,
+    }
+    del work
+    torch.cuda.empty_cache()
+
+    if not args.no_extras:
+        extras = {}
+        for name in ("llama2_7b_decode", "llama70b_gqa_decode"):
+            w2 = synth.WORKLOADS[name]
+            dw = Decode(api, w2, seed=99 + rank)
+            for _ in range(args.warmup):
+                dw.step(stream)
+            stream.synchronize()
+            k2 = max(args.steps // 2, 10)
+            with ClockSampler(dev_index) as ck2:
+                ms2 = timed_steps(dw, k2, stream, flush) / k2
+            per2, lps2 = traced_breakdown(api, dw, min(k2, 30), stream, flush)
+            n2 = min(k2, 30)
+            att_ms = (per2.get("attn_decode_split", {"ms": 0})["ms"]
+                      + per2.get("attn_decode_combine", {"ms": 0})["ms"]) / n2
+            gem_ms = per2.get("gemm_tc", {"ms": 0})["ms"] / n2
+            dom = "attn_decode" if att_ms >= gem_ms else "gemm_tc"
+            dom_bytes = dw.kv_read if dom == "attn_decode" else weight_bytes(dw.d)
+            dom_ms = att_ms if dom == "attn_decode" else gem_ms
+            extras[name] = {
+                "tok_per_s": world * dw.B / (ms2 * 1e-3),
+                "hbm_gbs": dw.min_bytes / (ms2 * 1e-3) / 1e9,
+                "ms_per_step": ms2,
+                "layer_roofline_frac": dw.roofline_s(peaks) / (ms2 * 1e-3),
+                "min_bytes_per_step": dw.min_bytes,
+                "roofline": {"bound": "hbm", "kernel": dom,
+                             "achieved": dom_bytes / (dom_ms * 1e-3) / 1e9 if dom_ms else 0.0,
+                             "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                             "frac": (dom_bytes / (dom_ms * 1e-3) / 1e9) / peaks["hbm_gbs"] if dom_ms else 0.0,
+                             "traffic": None},
+                "kernels": {k: {"launches_per_step": v["launches"] // n2, "ms_per_step": v["ms"] / n2,
+                                "share": v["share"]} for k, v in per2.items()},
+                "clocks": ck2.summary(),
+                "device_status": int(dw.status.item()),
+            }
+            del dw
+            torch.cuda.empty_cache()
+        line["decode"] = extras
+
+    if rank == 0 and world == 1 and not args.no_cpu:
+        v, n, desc = oracle_prefill_sample(wl, 12.0, 64)
+        line["cpu_baseline"] = {"value": v, "unit": "TFLOP/s", "cores": host_cores(),
+                                "kind": "oracle", "sample": desc}
+    if rank == 0:
+        print(json.dumps(line))
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

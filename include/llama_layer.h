@@ -178,6 +178,21 @@ size_t ll_linear_workspace_size(int32_t m, int32_t n, int32_t k);
 int ll_linear(const void* x, const void* w, void* y, int32_t m, int32_t n, int32_t k,
               void* workspace, size_t workspace_bytes, int32_t* status, void* stream);
 
+/* Launch tracing, for measurement (off by default).  ll_trace_begin creates
+ * 2 * capacity CUDA events on the current device; until ll_trace_end, each
+ * kernel launch the library makes is bracketed by two of them, recorded on
+ * the launch's stream, and its kernel name kept.  ll_trace_end returns the
+ * number of launches recorded (at most capacity; later ones are not traced).
+ * Once the stream has been synchronised, ll_trace_elapsed_ms(i) is launch i's
+ * duration in milliseconds (-1 on error) and ll_trace_name(i) its kernel.
+ * Process-wide state, not thread-safe.  This is a measuring aid the pages do
+ * not describe (their profiler is the graph timeline of the ATB debugging
+ * section). */
+int ll_trace_begin(int32_t capacity);
+int32_t ll_trace_end(void);
+float ll_trace_elapsed_ms(int32_t i);
+const char* ll_trace_name(int32_t i);
+
 /* Number of streaming multiprocessors the library sizes its grids for
  * (queried once per device), or -1 without a device. */
 int ll_device_sm_count(void);

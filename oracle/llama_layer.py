@@ -380,7 +380,8 @@ def layer_forward(dims, W, x, positions, seq_of_token, k_pool, v_pool, block_tab
     # 9. down projection + residual
     y = h1 + a @ w["w_down"].T
     if want is not None:
-        want.update(xh=xh, q=q, k=k, v=v, o=o, h=h1, a=a, slots=np.asarray(slots))
+        want.update(xh=xh, q=q, k=k, v=v, o=o, h=h1, hh=hh if form == "opbyop" or storage == "bf16" else None,
+                    a=a, slots=np.asarray(slots))
     return y
 
 

@@ -25,8 +25,8 @@ DEV = "cuda"
     (65, 256, 128), (128, 512, 256), (300, 1376, 688), (2048, 4096, 4096), (257, 12288, 4096),
 ])
 def test_linear_matches_float64_matmul(m, n, k):
-    x = synth.normal_bf16((m, k), 1.0, seed=m * 7 + 1)
-    w = synth.normal_bf16((n, k), 0.02, seed=n * 3 + k)
+    x = synth.normal_bf16((m, k), 1.0, seed=m * 7 + 1, tag="x")
+    w = synth.normal_bf16((n, k), 0.02, seed=n * 3 + k, tag="w")
     y = api.linear(x.to(DEV), w.to(DEV))
     torch.cuda.synchronize()
     ref = f64(x) @ f64(w).T
@@ -35,8 +35,8 @@ def test_linear_matches_float64_matmul(m, n, k):
 
 
 def test_linear_twice_same_buffers_is_repeatable():
-    x = synth.normal_bf16((64, 4096), 1.0, seed=1).to(DEV)
-    w = synth.normal_bf16((4096, 4096), 0.02, seed=2).to(DEV)
+    x = synth.normal_bf16((64, 4096), 1.0, seed=1, tag="x").to(DEV)
+    w = synth.normal_bf16((4096, 4096), 0.02, seed=2, tag="w").to(DEV)
     ws = torch.empty(api.lib.ll_linear_workspace_size(64, 4096, 4096), dtype=torch.uint8, device=DEV)
     y1 = api.linear(x, w, workspace=ws)
     y2 = api.linear(x, w, workspace=ws)
@@ -49,8 +49,8 @@ def test_linear_twice_same_buffers_is_repeatable():
 @pytest.mark.parametrize("T,Hkv,d,bs,nb", [(37, 2, 64, 16, 8), (300, 8, 128, 128, 5), (1, 32, 128, 128, 2)])
 def test_reshape_and_cache_bit_exact(T, Hkv, d, bs, nb):
     dims = synth.LayerDims(Hkv * d, Hkv, Hkv, d, 64, bs)
-    k = synth.normal_bf16((T, Hkv, d), 1.0, seed=T + 1)
-    v = synth.normal_bf16((T, Hkv, d), 1.0, seed=T + 2)
+    k = synth.normal_bf16((T, Hkv, d), 1.0, seed=T, tag="k")
+    v = synth.normal_bf16((T, Hkv, d), 1.0, seed=T, tag="v")
     slots = synth.make_slot_mapping(T, nb * bs, seed=T + 3, n_skip=min(3, T - 1))
     kp, vp = synth.make_pool(nb, dims, 0, fill="sentinel")
     kpd, vpd = kp.to(DEV), vp.to(DEV)
@@ -91,7 +91,7 @@ def test_paged_attention_decode(B, Hq, Hkv, d, bs, ctx_lo, ctx_hi):
     ctx[0] = ctx_lo
     table, nb = synth.make_block_table(ctx.tolist(), bs, seed=B * 13, extra_blocks=3)
     kp, vp = synth.make_pool(nb, dims, seed=B * 17)
-    q = synth.normal_bf16((B, Hq, d), 1.0, seed=B * 19)
+    q = synth.normal_bf16((B, Hq, d), 1.0, seed=B, tag="q")
     scale = 1 / math.sqrt(d)
     out = api.paged_attention_decode(q.to(DEV), kp.to(DEV), vp.to(DEV), table.to(DEV), ctx.to(DEV), scale)
     torch.cuda.synchronize()

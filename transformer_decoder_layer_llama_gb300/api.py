@@ -29,7 +29,8 @@ EXPORTED = [
     "ll_strerror", "ll_last_error", "ll_packed_weights_size", "ll_pack_weights", "ll_workspace_size",
     "ll_layer_prefill", "ll_layer_decode_step", "ll_reshape_and_cache",
     "ll_attention_workspace_size", "ll_paged_attention_decode", "ll_linear_workspace_size",
-    "ll_linear", "ll_device_sm_count",
+    "ll_linear", "ll_device_sm_count", "ll_trace_begin", "ll_trace_end", "ll_trace_elapsed_ms",
+    "ll_trace_name",
 ]
 
 
@@ -74,6 +75,10 @@ def _load():
         "ll_linear_workspace_size": (S, [I32, I32, I32]),
         "ll_linear": (ctypes.c_int, [P, P, P, I32, I32, I32, P, S, P, P]),
         "ll_device_sm_count": (ctypes.c_int, []),
+        "ll_trace_begin": (ctypes.c_int, [I32]),
+        "ll_trace_end": (I32, []),
+        "ll_trace_elapsed_ms": (ctypes.c_float, [I32]),
+        "ll_trace_name": (ctypes.c_char_p, [I32]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -282,3 +287,24 @@ def linear(x, w, y=None, workspace=None, status=None, stream=None):
     _check("ll_linear", lib.ll_linear(_ptr(x), _ptr(w), _ptr(y), m, n, k, _ptr(workspace),
                                       workspace.numel(), _ptr(status), _stream(stream)))
     return y
+
+
+class trace:
+    """Context manager over ll_trace_begin/ll_trace_end: records every kernel launch the
+    library makes inside the block.  After the stream is synchronised, `launches()`
+    returns [(kernel name, milliseconds), ...] in launch order."""
+
+    def __init__(self, capacity=4096):
+        self.capacity = capacity
+        self.count = 0
+
+    def __enter__(self):
+        _check("ll_trace_begin", lib.ll_trace_begin(self.capacity))
+        return self
+
+    def __exit__(self, *exc):
+        self.count = lib.ll_trace_end()
+        return False
+
+    def launches(self):
+        return [(lib.ll_trace_name(i).decode(), lib.ll_trace_elapsed_ms(i)) for i in range(self.count)]

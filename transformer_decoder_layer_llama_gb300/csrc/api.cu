@@ -16,6 +16,7 @@
 
 #include <algorithm>
 #include <cmath>
+#include <vector>
 #include <cstdio>
 #include <cstring>
 
@@ -294,11 +295,78 @@ cudaError_t record(cudaError_t e, const char* where) {
     if (e != cudaSuccess) set_last_error(where, cudaGetErrorString(e));
     return e;
 }
+
+namespace {
+struct Trace {
+    bool on = false;
+    int capacity = 0;
+    int count = 0;
+    std::vector<cudaEvent_t> ev;
+    std::vector<const char*> names;
+};
+Trace g_trace;
+
+void trace_free() {
+    for (cudaEvent_t e : g_trace.ev) cudaEventDestroy(e);
+    g_trace.ev.clear();
+    g_trace.names.clear();
+    g_trace.capacity = g_trace.count = 0;
+}
+}  // namespace
+
+void trace_before(const char* kernel, cudaStream_t stream) {
+    if (!g_trace.on || g_trace.count >= g_trace.capacity) return;
+    g_trace.names[g_trace.count] = kernel;
+    cudaEventRecord(g_trace.ev[2 * g_trace.count], stream);
+}
+
+void trace_after(cudaStream_t stream) {
+    if (!g_trace.on || g_trace.count >= g_trace.capacity) return;
+    cudaEventRecord(g_trace.ev[2 * g_trace.count + 1], stream);
+    ++g_trace.count;
+}
 }  // namespace ll
 
 extern "C" {
 
 const char* ll_last_error(void) { return g_last_error; }
+
+int ll_trace_begin(int32_t capacity) {
+    ll::clear_last_error();
+    if (capacity <= 0 || capacity > (1 << 20)) return LL_ERR_INVALID_ARG;
+    ll::trace_free();
+    ll::g_trace.ev.resize(2 * (size_t)capacity, nullptr);
+    ll::g_trace.names.resize(capacity, "");
+    for (auto& e : ll::g_trace.ev) {
+        if (ll::record(cudaEventCreate(&e), "cudaEventCreate(trace)") != cudaSuccess) {
+            e = nullptr;
+            ll::trace_free();
+            return LL_ERR_CUDA;
+        }
+    }
+    ll::g_trace.capacity = capacity;
+    ll::g_trace.count = 0;
+    ll::g_trace.on = true;
+    return LL_OK;
+}
+
+int32_t ll_trace_end(void) {
+    ll::g_trace.on = false;
+    return ll::g_trace.count;
+}
+
+float ll_trace_elapsed_ms(int32_t i) {
+    if (i < 0 || i >= ll::g_trace.count) return -1.f;
+    float ms = -1.f;
+    if (cudaEventElapsedTime(&ms, ll::g_trace.ev[2 * i], ll::g_trace.ev[2 * i + 1]) != cudaSuccess)
+        return -1.f;
+    return ms;
+}
+
+const char* ll_trace_name(int32_t i) {
+    if (i < 0 || i >= ll::g_trace.count) return "";
+    return ll::g_trace.names[i];
+}
 
 const char* ll_strerror(int code) {
     switch (code) {

@@ -517,7 +517,9 @@ cudaError_t prefill_for(const AttnPrefillArgs& a, cudaStream_t stream) {
         configured = true;
     }
     dim3 grid((a.seq_len + 127) / 128, a.n_heads, a.batch);
+    trace_before("attn_prefill", stream);
     attn_prefill_kernel<D><<<grid, 256, smem, stream>>>(a);
+    trace_after(stream);
     return record(cudaGetLastError(), "attn_prefill_kernel launch");
 }
 
@@ -533,10 +535,14 @@ cudaError_t decode_for(const AttnDecodeArgs& a, cudaStream_t stream) {
         configured = true;
     }
     dim3 grid(max_splits, a.n_kv_heads, a.batch);
+    trace_before("attn_decode_split", stream);
     attn_decode_split_kernel<D><<<grid, 128, smem, stream>>>(a, max_splits);
+    trace_after(stream);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return record(e, "attn_decode_split_kernel launch");
+    trace_before("attn_decode_combine", stream);
     attn_decode_combine_kernel<<<dim3(a.n_heads, a.batch), D, 0, stream>>>(a, max_splits);
+    trace_after(stream);
     return record(cudaGetLastError(), "attn_decode_combine_kernel launch");
 }
 

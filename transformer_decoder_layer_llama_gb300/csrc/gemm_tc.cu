@@ -647,7 +647,9 @@ cudaError_t launch_gemm(const GemmProblem& pr, cudaStream_t stream) {
         configured_smem = (int)p.smem_bytes;
     }
     int grid = std::min(p.units, sms * p.ctas_per_sm);
+    trace_before("gemm_tc", stream);
     gemm_tc_kernel<<<grid, kThreads, p.smem_bytes, stream>>>(tmA, tmB, a);
+    trace_after(stream);
     return record(cudaGetLastError(), "gemm_tc_kernel launch");
 }
 

@@ -66,6 +66,10 @@ void set_last_error(const char* where, const char* what);
 void clear_last_error();
 cudaError_t record(cudaError_t e, const char* where);
 
+// Launch tracing hooks (no-ops unless ll_trace_begin is active).
+void trace_before(const char* kernel, cudaStream_t stream);
+void trace_after(cudaStream_t stream);
+
 // RMSNorm: out[t] = bf16(x[t] / sqrt(mean(x[t]^2) + eps) * g); also zeroes
 // `zero_words` int32 words at `zero_ptr` (tile counters) when non-null.
 cudaError_t launch_rmsnorm(const __nv_bfloat16* x, const float* g, __nv_bfloat16* out, int tokens,

@@ -141,7 +141,9 @@ cudaError_t launch_rmsnorm(const __nv_bfloat16* x, const float* g, __nv_bfloat16
                            cudaStream_t stream) {
     if (tokens <= 0) return cudaSuccess;
     const int threads = std::min(kNormThreads, std::max(32, ((hidden / 8 + 31) / 32) * 32));
+    trace_before("rmsnorm", stream);
     rmsnorm_kernel<<<tokens, threads, 0, stream>>>(x, g, out, hidden, eps, zero_ptr, zero_words);
+    trace_after(stream);
     return record(cudaGetLastError(), "rmsnorm launch");
 }
 
@@ -152,10 +154,12 @@ cudaError_t launch_reshape_and_cache(const __nv_bfloat16* k, const __nv_bfloat16
     if (tokens <= 0) return cudaSuccess;
     const int vpr = head_dim / 8;
     const long long n = (long long)tokens * n_kv_heads * vpr;
+    trace_before("reshape_and_cache", stream);
     reshape_and_cache_kernel<<<blocks_for(n, 256), 256, 0, stream>>>(
         reinterpret_cast<const uint4*>(k), reinterpret_cast<const uint4*>(v), slots, tokens,
         n_kv_heads, vpr, block_size, reinterpret_cast<uint4*>(k_pool), reinterpret_cast<uint4*>(v_pool),
         (long long)num_blocks * block_size, status);
+    trace_after(stream);
     return record(cudaGetLastError(), "reshape_and_cache launch");
 }
 

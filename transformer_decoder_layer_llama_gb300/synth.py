@@ -18,6 +18,7 @@ random permutations of the pool's blocks.
 from __future__ import annotations
 
 import dataclasses
+import zlib
 
 import torch
 
@@ -70,15 +71,18 @@ WORKLOADS = {
 }
 
 
-def _gen(seed: int) -> torch.Generator:
+def _gen(seed: int, tag: str) -> torch.Generator:
+    """CPU generator of stream `tag` for a user seed.  Different tags give independent
+    streams for the same seed (the seed is hashed with the tag), so two tensors can never
+    be drawn from one stream by accident (e.g. an input equal to a scaled weight row)."""
     g = torch.Generator()
-    g.manual_seed(int(seed))
+    g.manual_seed(zlib.crc32(f"{tag}:{int(seed)}".encode()) * 2654435761 % (1 << 63))
     return g
 
 
-def normal_bf16(shape, std: float, seed: int) -> torch.Tensor:
+def normal_bf16(shape, std: float, seed: int, tag: str = "normal") -> torch.Tensor:
     """BF16 tensor of N(0, std^2) draws (drawn in fp32, rounded to nearest BF16)."""
-    t = torch.randn(*shape, generator=_gen(seed), dtype=torch.float32)
+    t = torch.randn(*shape, generator=_gen(seed, tag), dtype=torch.float32)
     if std != 1.0:
         t.mul_(std)
     return t.to(BF16)
@@ -92,22 +96,22 @@ def make_weights(d: LayerDims, w_std: float, seed: int) -> dict:
     """
     H, I = d.hidden, d.intermediate
     return {
-        "w_qkv": normal_bf16((d.qkv_rows, H), w_std, seed + 1),
-        "w_o": normal_bf16((H, d.n_heads * d.head_dim), w_std, seed + 2),
-        "w_gate": normal_bf16((I, H), w_std, seed + 3),
-        "w_up": normal_bf16((I, H), w_std, seed + 4),
-        "w_down": normal_bf16((H, I), w_std, seed + 5),
-        "g_attn": 1.0 + 0.1 * torch.randn(H, generator=_gen(seed + 6), dtype=torch.float32),
-        "g_ffn": 1.0 + 0.1 * torch.randn(H, generator=_gen(seed + 7), dtype=torch.float32),
+        "w_qkv": normal_bf16((d.qkv_rows, H), w_std, seed, "w_qkv"),
+        "w_o": normal_bf16((H, d.n_heads * d.head_dim), w_std, seed, "w_o"),
+        "w_gate": normal_bf16((I, H), w_std, seed, "w_gate"),
+        "w_up": normal_bf16((I, H), w_std, seed, "w_up"),
+        "w_down": normal_bf16((H, I), w_std, seed, "w_down"),
+        "g_attn": 1.0 + 0.1 * torch.randn(H, generator=_gen(seed, "g_attn"), dtype=torch.float32),
+        "g_ffn": 1.0 + 0.1 * torch.randn(H, generator=_gen(seed, "g_ffn"), dtype=torch.float32),
     }
 
 
 def make_x(tokens: int, hidden: int, seed: int) -> torch.Tensor:
-    return normal_bf16((tokens, hidden), 1.0, seed)
+    return normal_bf16((tokens, hidden), 1.0, seed, "x")
 
 
 def make_context_lens(batch: int, lo: int, hi: int, seed: int) -> torch.Tensor:
-    return torch.randint(lo, hi + 1, (batch,), generator=_gen(seed), dtype=torch.int32)
+    return torch.randint(lo, hi + 1, (batch,), generator=_gen(seed, "context_lens"), dtype=torch.int32)
 
 
 def blocks_needed(tokens: int, block_size: int) -> int:
@@ -126,7 +130,7 @@ def make_block_table(seq_tokens, block_size: int, seed: int, extra_blocks: int =
     need = [blocks_needed(t, block_size) for t in seq_tokens]
     num_blocks = sum(need) + int(extra_blocks)
     w = max(need) if width is None else int(width)
-    perm = torch.randperm(num_blocks, generator=_gen(seed)).to(torch.int32)
+    perm = torch.randperm(num_blocks, generator=_gen(seed, "block_table")).to(torch.int32)
     table = torch.full((len(need), max(w, 1)), -1, dtype=torch.int32)
     at = 0
     for b, n in enumerate(need):
@@ -143,7 +147,7 @@ def make_pool(num_blocks: int, d: LayerDims, seed: int, fill: str = "normal"):
     """
     shape = (num_blocks, d.n_kv_heads, d.block_size, d.head_dim)
     if fill == "normal":
-        return normal_bf16(shape, 1.0, seed), normal_bf16(shape, 1.0, seed + 1)
+        return normal_bf16(shape, 1.0, seed, "k_pool"), normal_bf16(shape, 1.0, seed, "v_pool")
     if fill == "sentinel":
         return (torch.full(shape, -1024.0, dtype=BF16), torch.full(shape, -1024.0, dtype=BF16))
     raise ValueError(fill)
@@ -157,7 +161,7 @@ def prefill_positions(batch: int, seq_len: int, start: int = 0) -> torch.Tensor:
 def make_slot_mapping(tokens: int, num_slots: int, seed: int, n_skip: int = 0) -> torch.Tensor:
     """Distinct random destination slots for `tokens` tokens, drawn from range(num_slots);
     `n_skip` of them (at seeded random positions) are -1, meaning "write nothing"."""
-    g = _gen(seed)
+    g = _gen(seed, "slot_mapping")
     slots = torch.randperm(num_slots, generator=g)[:tokens].to(torch.int32)
     if n_skip:
         idx = torch.randperm(tokens, generator=g)[:n_skip]
