@@ -38,12 +38,14 @@ Readings where the pages are silent (each is listed in the design doc):
 * Attention scale 1/sqrt(d); a query at position p sees cache positions 0..p
   of its own sequence (causal); no bias anywhere (Llama).
 * SwiGLU: a = silu(x W_gate^T) * (x W_up^T), silu(z) = z / (1 + e^-z).
-* Storage precision ("bf16" mode, the default): every tensor one fused
-  operator of the chain hands to the next through memory is BF16 -- the
-  normalised input, q/k/v after RoPE (k/v are what the cache holds), the
-  attention output, h after the first residual, the normalised h, the SwiGLU
-  output.  Each is computed exactly (float64) and then rounded once to the
-  nearest BF16 (ties to even).  The final y is returned unrounded.  "exact"
+* Storage precision ("bf16" mode, the default).  The pages name no precision
+  for the intermediates.  Reading: every tensor that feeds a MatMul is BF16
+  (the BF16 tensor cores take nothing else): the normalised input, q after
+  RoPE, the attention output, the normalised h and the SwiGLU output; k/v
+  after RoPE are BF16 because the KV cache holds BF16.  Each is computed
+  exactly (float64) and then rounded once to the nearest BF16 (ties to even).
+  The residual stream h = x + o W_o^T feeds no MatMul, so it is not rounded
+  (it stays float32 on the GPU).  The final y is returned unrounded.  "exact"
   mode rounds nothing (pools then hold float64) and serves the invariant pins.
 
 Two forms of the same layer are implemented: "opbyop" materialises every
@@ -359,8 +361,8 @@ def layer_forward(dims, W, x, positions, seq_of_token, k_pool, v_pool, block_tab
                                                       scale, attn_chunk, attn_splits)
     o = rnd(o)
 
-    # 6. O projection + residual
-    h1 = rnd(x + o.reshape(T, Hq * d) @ w["w_o"].T)
+    # 6. O projection + residual (the residual stream is not a MatMul operand: not rounded)
+    h1 = x + o.reshape(T, Hq * d) @ w["w_o"].T
 
     # 7-8. RMSNorm, merged gate/up projection, SwiGLU
     if form == "opbyop":

@@ -29,3 +29,25 @@ def assert_close(got, ref, name="", atol=ATOL, rtol=RTOL):
         raise AssertionError(f"{name}: {int(bad.sum())}/{bad.size} elements outside "
                              f"{atol}+{rtol}|ref|; worst at {i}: got {got[i]} ref {ref[i]}")
     assert np.isfinite(got).all(), name
+
+
+# Full-size workloads: the per-element bound above must hold on all but a small
+# fraction of elements, and every element must stay within a hard bound derived
+# from the BF16 operand-rounding cascade (tests/tolerance_model.py measures the
+# spread a correct BF16 implementation shows against the float64 oracle: at the
+# 7B prefill size its rms is ~4e-3 and its worst element ~0.045).
+FULL_MAX_FRAC_OUTSIDE = 2e-3
+FULL_HARD_ATOL = 6e-2
+
+
+def assert_close_fullsize(got, ref, name=""):
+    got = np.asarray(got, np.float64)
+    ref = np.asarray(ref, np.float64)
+    assert got.shape == ref.shape, (name, got.shape, ref.shape)
+    assert np.isfinite(got).all(), name
+    err = np.abs(got - ref)
+    frac = float((err > ATOL + RTOL * np.abs(ref)).mean())
+    assert frac <= FULL_MAX_FRAC_OUTSIDE, (
+        f"{name}: {frac:.2e} of elements outside {ATOL}+{RTOL}|ref| (allowed {FULL_MAX_FRAC_OUTSIDE})")
+    assert_close(got, ref, name + " [hard bound]", atol=FULL_HARD_ATOL, rtol=RTOL)
+    return frac

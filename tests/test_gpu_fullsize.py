@@ -6,13 +6,17 @@ configuration bench.py times (same entry points, same shapes).
 * Llama-2-7B layer decode step, batch 64, context ~U[512, 4096].
 * 70B-shaped GQA layer decode step, batch 16, context ~U[4096, 32768]
   (several 1024-key splits per sequence).
+
+Layer outputs use the two-tier check of tests/helpers.py (the per-element
+bound on all but a small fraction, a derived hard bound on every element);
+the cache writes are checked slot by slot.
 """
 import numpy as np
 import pytest
 import torch
 
 from oracle import llama_layer as O
-from tests.helpers import assert_close, bits, f64
+from tests.helpers import assert_close, assert_close_fullsize, bits, f64
 from transformer_decoder_layer_llama_gb300 import synth
 
 pytestmark = pytest.mark.gpu
@@ -46,7 +50,7 @@ def test_llama2_7b_prefill_full():
     assert int(status.item()) == 0
     ko, vo = bits(kp), bits(vp)
     y_ref = O.layer_prefill(d, Wn, f64(x), pos.numpy(), B, S, ko, vo, table.numpy())
-    assert_close(f64(y), y_ref, "7B prefill y")
+    assert_close_fullsize(f64(y), y_ref, "7B prefill y")
     kg, vg = bits(kpd), bits(vpd)
     np.testing.assert_array_equal(kg == 0xC480, ko == 0xC480)
     assert_close(O.bf16_value(kg), O.bf16_value(ko), "7B K cache")
@@ -74,7 +78,7 @@ def test_decode_step_full(name):
     ko, vo = bits(kp), bits(vp)
     want = {}
     y_ref = O.layer_decode_step(d, Wn, f64(x), ko, vo, table.numpy(), ctx.numpy(), want=want)
-    assert_close(f64(y), y_ref, f"{name} y")
+    assert_close_fullsize(f64(y), y_ref, f"{name} y")
     # the appended K/V rows: same slots, values within tolerance; everything else untouched
     kg, vg = bits(kpd), bits(vpd)
     changed = np.any(kg != bits(kp), axis=(1, 3)) | np.any(ko != bits(kp), axis=(1, 3))

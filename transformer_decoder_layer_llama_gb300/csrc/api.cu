@@ -109,7 +109,7 @@ WsLayout ws_layout(const ll_config* c, int T, int max_blocks) {
     L.xh = at; at = align_up(at + (size_t)T * H * 2);
     L.q = at;  at = align_up(at + (size_t)T * nq * 2);
     L.o = at;  at = align_up(at + (size_t)T * nq * 2);
-    L.h = at;  at = align_up(at + (size_t)T * H * 2);
+    L.h = at;  at = align_up(at + (size_t)T * H * 4);   // float32 residual stream
     L.hh = at; at = align_up(at + (size_t)T * H * 2);
     L.a = at;  at = align_up(at + (size_t)T * I * 2);
     L.partial_bytes = ll::gemm_partial_bound_bytes();
@@ -143,7 +143,7 @@ int run_layer(const ll_config* cfg, const void* packed, const void* x, const int
     auto* xh = reinterpret_cast<__nv_bfloat16*>(ws + L.xh);
     auto* q = reinterpret_cast<__nv_bfloat16*>(ws + L.q);
     auto* o = reinterpret_cast<__nv_bfloat16*>(ws + L.o);
-    auto* h = reinterpret_cast<__nv_bfloat16*>(ws + L.h);
+    auto* h = reinterpret_cast<float*>(ws + L.h);
     auto* hh = reinterpret_cast<__nv_bfloat16*>(ws + L.hh);
     auto* a = reinterpret_cast<__nv_bfloat16*>(ws + L.a);
     auto* partials = reinterpret_cast<float*>(ws + L.partials);
@@ -243,14 +243,13 @@ int run_layer(const ll_config* cfg, const void* packed, const void* x, const int
     go.counters = counters + L.counter_words;
     go.ep = EpiParams{};
     go.ep.kind = ll::EPI_RESID;
-    go.ep.out = h;
+    go.ep.out_f32 = h;
     go.ep.ld_out = H;
     go.ep.resid = xb;
     go.ep.status = status;
     if ((e = ll::launch_gemm(go, stream)) != cudaSuccess) return LL_ERR_CUDA;
 
-    if ((e = ll::launch_rmsnorm(h, P.g_ffn, hh, T, H, cfg->rms_eps, nullptr, 0, stream)) !=
-        cudaSuccess)
+    if ((e = ll::launch_rmsnorm_f32(h, P.g_ffn, hh, T, H, cfg->rms_eps, stream)) != cudaSuccess)
         return LL_ERR_CUDA;
 
     // merged gate/up + SwiGLU
@@ -278,7 +277,7 @@ int run_layer(const ll_config* cfg, const void* packed, const void* x, const int
     gd.ep.kind = ll::EPI_RESID;
     gd.ep.out = yb;
     gd.ep.ld_out = H;
-    gd.ep.resid = h;
+    gd.ep.resid_f32 = h;
     gd.ep.status = status;
     if ((e = ll::launch_gemm(gd, stream)) != cudaSuccess) return LL_ERR_CUDA;
     return LL_OK;

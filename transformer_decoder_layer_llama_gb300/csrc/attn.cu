@@ -13,6 +13,8 @@
 // rows; 64-key tiles double-buffered in shared memory with cp.async (16-byte
 // vectors, XOR-swizzled rows so ldmatrix is conflict-free); QK^T and PV on
 // the tensor cores with mma.sync m16n8k16 (BF16 in, float32 accumulate).
+// The probabilities P enter the PV product as two BF16 parts (hi + lo), so P
+// keeps about 16 significant bits instead of BF16's 8; V stays exact.
 //
 // Decode: the context of each (sequence, KV head) is cut into 1024-key
 // splits, one CTA each; the CTA's 4 warps share the G = n_heads / n_kv_heads
@@ -216,21 +218,14 @@ __global__ void __launch_bounds__(256, 1)
             m0 = mn0;
             m1 = mn1;
             float rs0 = 0.f, rs1 = 0.f;
-            uint32_t pf[BN / 16][4];
 #pragma unroll
             for (int nt = 0; nt < BN / 8; ++nt) {
-                const float p0 = exp2f(s[nt][0] - base0), p1 = exp2f(s[nt][1] - base0);
-                const float p2 = exp2f(s[nt][2] - base1), p3 = exp2f(s[nt][3] - base1);
-                rs0 += p0 + p1;
-                rs1 += p2 + p3;
-                const int kk = nt >> 1;
-                if ((nt & 1) == 0) {
-                    pf[kk][0] = pack_bf16x2(p0, p1);
-                    pf[kk][1] = pack_bf16x2(p2, p3);
-                } else {
-                    pf[kk][2] = pack_bf16x2(p0, p1);
-                    pf[kk][3] = pack_bf16x2(p2, p3);
-                }
+                s[nt][0] = exp2f(s[nt][0] - base0);
+                s[nt][1] = exp2f(s[nt][1] - base0);
+                s[nt][2] = exp2f(s[nt][2] - base1);
+                s[nt][3] = exp2f(s[nt][3] - base1);
+                rs0 += s[nt][0] + s[nt][1];
+                rs1 += s[nt][2] + s[nt][3];
             }
             l0 = l0 * al0 + rs0;
             l1 = l1 * al1 + rs1;
@@ -241,16 +236,24 @@ __global__ void __launch_bounds__(256, 1)
                 acc[i][2] *= al1;
                 acc[i][3] *= al1;
             }
+            // P V with P carried as hi + lo BF16 parts (about 16 bits): two MMAs per V fragment
 #pragma unroll
             for (int kk = 0; kk < BN / 16; ++kk) {
+                uint32_t ph[4], pl[4];
+                split_bf16x2(s[2 * kk][0], s[2 * kk][1], ph[0], pl[0]);
+                split_bf16x2(s[2 * kk][2], s[2 * kk][3], ph[1], pl[1]);
+                split_bf16x2(s[2 * kk + 1][0], s[2 * kk + 1][1], ph[2], pl[2]);
+                split_bf16x2(s[2 * kk + 1][2], s[2 * kk + 1][3], ph[3], pl[3]);
 #pragma unroll
                 for (int dp = 0; dp < D / 16; ++dp) {
                     uint32_t bfr[4];
                     const int r = kk * 16 + (lane & 7) + (((lane >> 3) & 1) << 3);
                     const int c = dp * 2 + (lane >> 4);
                     ldmatrix_x4_trans(bfr, vb + swz<D>(r, c));
-                    mma_bf16_16816(acc[2 * dp], pf[kk], bfr[0], bfr[1]);
-                    mma_bf16_16816(acc[2 * dp + 1], pf[kk], bfr[2], bfr[3]);
+                    mma_bf16_16816(acc[2 * dp], ph, bfr[0], bfr[1]);
+                    mma_bf16_16816(acc[2 * dp + 1], ph, bfr[2], bfr[3]);
+                    mma_bf16_16816(acc[2 * dp], pl, bfr[0], bfr[1]);
+                    mma_bf16_16816(acc[2 * dp + 1], pl, bfr[2], bfr[3]);
                 }
             }
         }
@@ -398,7 +401,7 @@ __global__ void __launch_bounds__(128)
         const float al0 = exp2f(m0 - base0), al1 = exp2f(m1 - base1);
         m0 = mn0;
         m1 = mn1;
-        uint32_t pf[4];
+        uint32_t ph[4], pl[4];
         float rs0 = 0.f, rs1 = 0.f;
         {
             float p[2][4];
@@ -411,10 +414,11 @@ __global__ void __launch_bounds__(128)
                 rs0 += p[nt][0] + p[nt][1];
                 rs1 += p[nt][2] + p[nt][3];
             }
-            pf[0] = pack_bf16x2(p[0][0], p[0][1]);
-            pf[1] = pack_bf16x2(p[0][2], p[0][3]);
-            pf[2] = pack_bf16x2(p[1][0], p[1][1]);
-            pf[3] = pack_bf16x2(p[1][2], p[1][3]);
+            // P carried as hi + lo BF16 parts (about 16 bits)
+            split_bf16x2(p[0][0], p[0][1], ph[0], pl[0]);
+            split_bf16x2(p[0][2], p[0][3], ph[1], pl[1]);
+            split_bf16x2(p[1][0], p[1][1], ph[2], pl[2]);
+            split_bf16x2(p[1][2], p[1][3], ph[3], pl[3]);
         }
         l0 = l0 * al0 + rs0;
         l1 = l1 * al1 + rs1;
@@ -431,8 +435,10 @@ __global__ void __launch_bounds__(128)
             const int r = warp * 16 + (lane & 7) + (((lane >> 3) & 1) << 3);
             const int c = dp * 2 + (lane >> 4);
             ldmatrix_x4_trans(bfr, vb + swz<D>(r, c));
-            mma_bf16_16816(acc[2 * dp], pf, bfr[0], bfr[1]);
-            mma_bf16_16816(acc[2 * dp + 1], pf, bfr[2], bfr[3]);
+            mma_bf16_16816(acc[2 * dp], ph, bfr[0], bfr[1]);
+            mma_bf16_16816(acc[2 * dp + 1], ph, bfr[2], bfr[3]);
+            mma_bf16_16816(acc[2 * dp], pl, bfr[0], bfr[1]);
+            mma_bf16_16816(acc[2 * dp + 1], pl, bfr[2], bfr[3]);
         }
         __syncthreads();
     }

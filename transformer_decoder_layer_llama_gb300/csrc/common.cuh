@@ -24,6 +24,13 @@ LL_DEVINL uint32_t pack_bf16x2(float lo, float hi) {
 LL_DEVINL float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
 LL_DEVINL float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xffff0000u); }
 
+// Two BF16 pairs whose sum carries (a, b) to about 16 significant bits:
+// hi = bf16(a, b), lo = bf16(a - hi.a, b - hi.b).
+LL_DEVINL void split_bf16x2(float a, float b, uint32_t& hi, uint32_t& lo) {
+    hi = pack_bf16x2(a, b);
+    lo = pack_bf16x2(a - bf16_lo(hi), b - bf16_hi(hi));
+}
+
 LL_DEVINL void flag_status(int32_t* status, int32_t bits) {
     if (status) atomicOr(status, bits);
 }

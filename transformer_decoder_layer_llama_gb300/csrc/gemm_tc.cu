@@ -112,16 +112,38 @@ LL_DEVINL void epi_token_chunk(const EpiParams& ep, int t, bool row_ok, int n0, 
             break;
         }
         case EPI_RESID: {
-            const uint4* rp = reinterpret_cast<const uint4*>(ep.resid + (size_t)t * N + n0);
-            uint4 r0 = rp[0], r1 = rp[1];
-            uint32_t rr[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
-            uint32_t oo[8];
+            float r[16];
+            if (ep.resid_f32) {
+                const float4* rp = reinterpret_cast<const float4*>(ep.resid_f32 + (size_t)t * N + n0);
 #pragma unroll
-            for (int j = 0; j < 8; ++j)
-                oo[j] = pack_bf16x2(bf16_lo(rr[j]) + v[2 * j], bf16_hi(rr[j]) + v[2 * j + 1]);
-            uint4* dst = reinterpret_cast<uint4*>(ep.out + (size_t)t * ep.ld_out + n0);
-            dst[0] = make_uint4(oo[0], oo[1], oo[2], oo[3]);
-            dst[1] = make_uint4(oo[4], oo[5], oo[6], oo[7]);
+                for (int j = 0; j < 4; ++j) {
+                    float4 f = rp[j];
+                    r[4 * j] = f.x; r[4 * j + 1] = f.y; r[4 * j + 2] = f.z; r[4 * j + 3] = f.w;
+                }
+            } else {
+                const uint4* rp = reinterpret_cast<const uint4*>(ep.resid + (size_t)t * N + n0);
+                uint4 r0 = rp[0], r1 = rp[1];
+                uint32_t rr[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    r[2 * j] = bf16_lo(rr[j]);
+                    r[2 * j + 1] = bf16_hi(rr[j]);
+                }
+            }
+            if (ep.out_f32) {
+                float4* dst = reinterpret_cast<float4*>(ep.out_f32 + (size_t)t * N + n0);
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    dst[j] = make_float4(r[4 * j] + v[4 * j], r[4 * j + 1] + v[4 * j + 1],
+                                         r[4 * j + 2] + v[4 * j + 2], r[4 * j + 3] + v[4 * j + 3]);
+            } else {
+                uint32_t oo[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) oo[j] = pack_bf16x2(r[2 * j] + v[2 * j], r[2 * j + 1] + v[2 * j + 1]);
+                uint4* dst = reinterpret_cast<uint4*>(ep.out + (size_t)t * ep.ld_out + n0);
+                dst[0] = make_uint4(oo[0], oo[1], oo[2], oo[3]);
+                dst[1] = make_uint4(oo[4], oo[5], oo[6], oo[7]);
+            }
             break;
         }
         case EPI_SWIGLU: {
@@ -205,8 +227,12 @@ LL_DEVINL void epi_weight_chunk(const EpiParams& ep, int n, int N, int t0, int T
 #pragma unroll
                 for (int j = 0; j < 16; ++j)
                     if (t0 + j < T) {
-                        float r = __bfloat162float(ep.resid[(size_t)(t0 + j) * N + n]);
-                        ep.out[(size_t)(t0 + j) * ep.ld_out + n] = __float2bfloat16_rn(r + v[j]);
+                        const size_t at = (size_t)(t0 + j) * N + n;
+                        const float r = ep.resid_f32 ? ep.resid_f32[at] : __bfloat162float(ep.resid[at]);
+                        if (ep.out_f32)
+                            ep.out_f32[at] = r + v[j];
+                        else
+                            ep.out[(size_t)(t0 + j) * ep.ld_out + n] = __float2bfloat16_rn(r + v[j]);
                     }
             break;
         case EPI_SWIGLU:

@@ -11,7 +11,7 @@ namespace ll {
 
 enum EpiKind : int {
     EPI_STORE = 0,   // out = acc
-    EPI_RESID = 1,   // out = resid + acc                (O projection, down projection)
+    EPI_RESID = 1,   // out = resid + acc (O projection, down projection); resid and out may be fp32
     EPI_SWIGLU = 2,  // out[j] = silu(acc[2j]) * acc[2j+1] (merged gate/up, rows interleaved)
     EPI_QKV = 3,     // RoPE on Q/K, Q -> q_out, K/V -> paged pool (merged QKV)
 };
@@ -20,7 +20,9 @@ struct EpiParams {
     int kind;
     __nv_bfloat16* out;            // STORE / RESID / SWIGLU destination [tokens, ld_out]
     int ld_out;
-    const __nv_bfloat16* resid;    // RESID: [tokens, n]
+    const __nv_bfloat16* resid;    // RESID: [tokens, n] BF16 residual, or
+    const float* resid_f32;        //        [tokens, n] float32 residual (one of the two)
+    float* out_f32;                // RESID: float32 destination [tokens, n] instead of `out`
     // EPI_QKV
     __nv_bfloat16* q_out;          // [tokens, n_heads * head_dim]
     __nv_bfloat16* k_pool;
@@ -70,11 +72,14 @@ cudaError_t record(cudaError_t e, const char* where);
 void trace_before(const char* kernel, cudaStream_t stream);
 void trace_after(cudaStream_t stream);
 
-// RMSNorm: out[t] = bf16(x[t] / sqrt(mean(x[t]^2) + eps) * g); also zeroes
-// `zero_words` int32 words at `zero_ptr` (tile counters) when non-null.
+// RMSNorm: out[t] = bf16(x[t] / sqrt(mean(x[t]^2) + eps) * g) of a BF16 or a
+// float32 input; also zeroes `zero_words` int32 words at `zero_ptr` (tile
+// counters) when non-null.
 cudaError_t launch_rmsnorm(const __nv_bfloat16* x, const float* g, __nv_bfloat16* out, int tokens,
                            int hidden, float eps, int32_t* zero_ptr, int zero_words,
                            cudaStream_t stream);
+cudaError_t launch_rmsnorm_f32(const float* x, const float* g, __nv_bfloat16* out, int tokens,
+                               int hidden, float eps, cudaStream_t stream);
 
 cudaError_t launch_reshape_and_cache(const __nv_bfloat16* k, const __nv_bfloat16* v,
                                      const int32_t* slots, int tokens, int n_kv_heads, int head_dim,

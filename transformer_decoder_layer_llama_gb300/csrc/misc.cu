@@ -13,8 +13,37 @@ constexpr int kNormThreads = 256;
 
 // RMSNorm of one token row per CTA (chain page: "x -> RMSNorm"):
 // out = bf16(x * r * g), r = 1 / sqrt(mean(x^2) + eps), sums in float32.
-// The row is read twice; the second read comes from L1/L2.
-__global__ void __launch_bounds__(kNormThreads) rmsnorm_kernel(const __nv_bfloat16* __restrict__ x,
+// The input row is BF16 (the layer input) or float32 (the residual stream
+// after the attention block).  The row is read twice; the second read comes
+// from L1/L2.
+template <typename In>
+struct RowIO;
+template <>
+struct RowIO<__nv_bfloat16> {
+    static constexpr int kVec = 8;   // elements per 16-byte load
+    LL_DEVINL static void load(const __nv_bfloat16* row, int i, float (&f)[8]) {
+        uint4 u = reinterpret_cast<const uint4*>(row)[i];
+        uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            f[2 * j] = bf16_lo(w[j]);
+            f[2 * j + 1] = bf16_hi(w[j]);
+        }
+    }
+};
+template <>
+struct RowIO<float> {
+    static constexpr int kVec = 8;
+    LL_DEVINL static void load(const float* row, int i, float (&f)[8]) {
+        float4 a = reinterpret_cast<const float4*>(row)[2 * i];
+        float4 b = reinterpret_cast<const float4*>(row)[2 * i + 1];
+        f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w;
+        f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
+    }
+};
+
+template <typename In>
+__global__ void __launch_bounds__(kNormThreads) rmsnorm_kernel(const In* __restrict__ x,
                                                                const float* __restrict__ g,
                                                                __nv_bfloat16* __restrict__ out,
                                                                int hidden, float eps,
@@ -22,17 +51,14 @@ __global__ void __launch_bounds__(kNormThreads) rmsnorm_kernel(const __nv_bfloat
     const int t = blockIdx.x;
     if (zero_ptr && t == 0)
         for (int i = threadIdx.x; i < zero_words; i += blockDim.x) zero_ptr[i] = 0;
-    const uint4* xr = reinterpret_cast<const uint4*>(x + (size_t)t * hidden);
+    const In* xr = x + (size_t)t * hidden;
     const int nv = hidden >> 3;
     float ss = 0.f;
     for (int i = threadIdx.x; i < nv; i += blockDim.x) {
-        uint4 u = xr[i];
-        uint32_t w[4] = {u.x, u.y, u.z, u.w};
+        float f[8];
+        RowIO<In>::load(xr, i, f);
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            float a = bf16_lo(w[j]), b = bf16_hi(w[j]);
-            ss += a * a + b * b;
-        }
+        for (int j = 0; j < 8; ++j) ss += f[j] * f[j];
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
@@ -50,13 +76,14 @@ __global__ void __launch_bounds__(kNormThreads) rmsnorm_kernel(const __nv_bfloat
     uint4* orow = reinterpret_cast<uint4*>(out + (size_t)t * hidden);
     const float4* g4 = reinterpret_cast<const float4*>(g);
     for (int i = threadIdx.x; i < nv; i += blockDim.x) {
-        uint4 u = xr[i];
+        float f[8];
+        RowIO<In>::load(xr, i, f);
         float4 ga = g4[2 * i], gb = g4[2 * i + 1];
         uint4 o;
-        o.x = pack_bf16x2(bf16_lo(u.x) * r * ga.x, bf16_hi(u.x) * r * ga.y);
-        o.y = pack_bf16x2(bf16_lo(u.y) * r * ga.z, bf16_hi(u.y) * r * ga.w);
-        o.z = pack_bf16x2(bf16_lo(u.z) * r * gb.x, bf16_hi(u.z) * r * gb.y);
-        o.w = pack_bf16x2(bf16_lo(u.w) * r * gb.z, bf16_hi(u.w) * r * gb.w);
+        o.x = pack_bf16x2(f[0] * r * ga.x, f[1] * r * ga.y);
+        o.y = pack_bf16x2(f[2] * r * ga.z, f[3] * r * ga.w);
+        o.z = pack_bf16x2(f[4] * r * gb.x, f[5] * r * gb.y);
+        o.w = pack_bf16x2(f[6] * r * gb.z, f[7] * r * gb.w);
         orow[i] = o;
     }
 }
@@ -142,9 +169,20 @@ cudaError_t launch_rmsnorm(const __nv_bfloat16* x, const float* g, __nv_bfloat16
     if (tokens <= 0) return cudaSuccess;
     const int threads = std::min(kNormThreads, std::max(32, ((hidden / 8 + 31) / 32) * 32));
     trace_before("rmsnorm", stream);
-    rmsnorm_kernel<<<tokens, threads, 0, stream>>>(x, g, out, hidden, eps, zero_ptr, zero_words);
+    rmsnorm_kernel<__nv_bfloat16><<<tokens, threads, 0, stream>>>(x, g, out, hidden, eps, zero_ptr,
+                                                                   zero_words);
     trace_after(stream);
     return record(cudaGetLastError(), "rmsnorm launch");
+}
+
+cudaError_t launch_rmsnorm_f32(const float* x, const float* g, __nv_bfloat16* out, int tokens,
+                               int hidden, float eps, cudaStream_t stream) {
+    if (tokens <= 0) return cudaSuccess;
+    const int threads = std::min(kNormThreads, std::max(32, ((hidden / 8 + 31) / 32) * 32));
+    trace_before("rmsnorm", stream);
+    rmsnorm_kernel<float><<<tokens, threads, 0, stream>>>(x, g, out, hidden, eps, nullptr, 0);
+    trace_after(stream);
+    return record(cudaGetLastError(), "rmsnorm_f32 launch");
 }
 
 cudaError_t launch_reshape_and_cache(const __nv_bfloat16* k, const __nv_bfloat16* v,
