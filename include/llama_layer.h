@@ -168,6 +168,31 @@ int ll_paged_attention_decode(const void* q, const ll_kv_pool* pool, const int32
                               int32_t block_size, float scale, void* out, void* workspace,
                               size_t workspace_bytes, int32_t* status, void* stream);
 
+/* ll_paged_attention_decode for callers that cannot allocate device memory.
+ * The pages have no counterpart of this call.  Some callers only own the
+ * buffers they pass in: a plugin that receives input and output tensors from
+ * a host framework with no hook for extra workspace, or code running where a
+ * device allocation would synchronise the device or bypass the allocator that
+ * owns the memory.  This variant takes the same arguments minus the workspace
+ * and keeps the per-split partial results in a fixed device array inside the
+ * library (32 MiB; every GPU that loads the library holds it until the
+ * process exits).  It allocates nothing and calls no allocator.
+ *  - Limit: batch * n_heads * ceil(max_blocks * block_size / 1024) *
+ *    (head_dim + 2) * 4 bytes must not exceed 32 MiB, else it returns
+ *    LL_ERR_UNSUPPORTED (ll_last_error gives the sizes) and launches nothing.
+ *  - The first call on a device resolves the array's device address (this may
+ *    load the library's device code); make that first call before any stream
+ *    capture on the device.
+ *  - All calls share the one array and each overwrites what it uses (nothing
+ *    in it needs to start at zero): calls that may overlap on the GPU (other
+ *    streams, other host threads) race on it and must be serialised.
+ * Results equal ll_paged_attention_decode's for the same inputs. */
+int ll_paged_attention_decode_noalloc(const void* q, const ll_kv_pool* pool,
+                                      const int32_t* block_table, int32_t max_blocks,
+                                      const int32_t* context_lens, int32_t batch, int32_t n_heads,
+                                      int32_t n_kv_heads, int32_t head_dim, int32_t block_size,
+                                      float scale, void* out, int32_t* status, void* stream);
+
 /* Workspace bytes for ll_linear. */
 size_t ll_linear_workspace_size(int32_t m, int32_t n, int32_t k);
 

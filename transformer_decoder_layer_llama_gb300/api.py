@@ -30,7 +30,7 @@ EXPORTED = [
     "ll_layer_prefill", "ll_layer_decode_step", "ll_reshape_and_cache",
     "ll_attention_workspace_size", "ll_paged_attention_decode", "ll_linear_workspace_size",
     "ll_linear", "ll_device_sm_count", "ll_trace_begin", "ll_trace_end", "ll_trace_elapsed_ms",
-    "ll_trace_name",
+    "ll_trace_name", "ll_paged_attention_decode_noalloc",
 ]
 
 
@@ -72,6 +72,8 @@ def _load():
         "ll_attention_workspace_size": (S, [I32, I32, I32, I32, I32]),
         "ll_paged_attention_decode": (ctypes.c_int, [P, poolp, P, I32, P, I32, I32, I32, I32, I32,
                                                      ctypes.c_float, P, P, S, P, P]),
+        "ll_paged_attention_decode_noalloc": (ctypes.c_int, [P, poolp, P, I32, P, I32, I32, I32, I32,
+                                                             I32, ctypes.c_float, P, P, P]),
         "ll_linear_workspace_size": (S, [I32, I32, I32]),
         "ll_linear": (ctypes.c_int, [P, P, P, I32, I32, I32, P, S, P, P]),
         "ll_device_sm_count": (ctypes.c_int, []),
@@ -266,6 +268,26 @@ def paged_attention_decode(q, k_pool, v_pool, block_table, context_lens, scale, 
         _ptr(q), ctypes.byref(pool), _ptr(block_table), block_table.shape[1], _ptr(context_lens), B,
         Hq, k_pool.shape[1], d, bs, float(scale), _ptr(out), _ptr(workspace), workspace.numel(),
         _ptr(status), _stream(stream)))
+    return out
+
+
+def paged_attention_decode_noalloc(q, k_pool, v_pool, block_table, context_lens, scale, out=None,
+                                   status=None, stream=None):
+    """ll_paged_attention_decode_noalloc: as paged_attention_decode, but the library keeps
+    the split partials in its own fixed device array, so no workspace is passed or made."""
+    _need(q, "q", torch.bfloat16)
+    B, Hq, d = q.shape
+    _need(block_table, "block_table", torch.int32)
+    _need(context_lens, "context_lens", torch.int32, shape=(B,))
+    pool = _pool(k_pool, v_pool)
+    if out is None:
+        out = torch.empty_like(q)
+    if status is None:
+        status = new_status(q.device)
+    _check("ll_paged_attention_decode_noalloc", lib.ll_paged_attention_decode_noalloc(
+        _ptr(q), ctypes.byref(pool), _ptr(block_table), block_table.shape[1], _ptr(context_lens), B,
+        Hq, k_pool.shape[1], d, k_pool.shape[2], float(scale), _ptr(out), _ptr(status),
+        _stream(stream)))
     return out
 
 

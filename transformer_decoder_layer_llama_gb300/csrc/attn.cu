@@ -23,9 +23,18 @@
 // memory, splits merge in a second kernel through their log-sum-exp.
 #include <algorithm>
 #include <cfloat>
+#include <cstdio>
+#include <mutex>
 
 #include "common.cuh"
 #include "kernels.h"
+
+// Scratch for ll_paged_attention_decode_noalloc: the per-split partial
+// results of decode attention live in this fixed device array instead of a
+// caller-provided workspace.  Every GPU that loads the library holds it until
+// the process exits.
+constexpr size_t kNoAllocScratchBytes = size_t(32) << 20;
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
 namespace ll {
 
@@ -579,4 +588,81 @@ cudaError_t launch_attn_decode(const AttnDecodeArgs& a, cudaStream_t stream) {
     return cudaErrorInvalidValue;
 }
 
+namespace {
+// Device address of g_noalloc_scratch, resolved once per device.  In host
+// code the array's name is only a host-side stand-in, never a device address.
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mu;
+void* g_noalloc_addr[kMaxDevices] = {};
+
+cudaError_t noalloc_scratch_address(void** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return record(e, "cudaGetDevice(noalloc)");
+    if (dev < 0 || dev >= kMaxDevices) {
+        set_last_error("ll_paged_attention_decode_noalloc", "device index beyond 63");
+        return cudaErrorInvalidDevice;
+    }
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (!g_noalloc_addr[dev]) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess) return record(e, "cudaGetSymbolAddress(g_noalloc_scratch)");
+        g_noalloc_addr[dev] = p;
+    }
+    *out = g_noalloc_addr[dev];
+    return cudaSuccess;
+}
+}  // namespace
+
 }  // namespace ll
+
+extern "C" int ll_paged_attention_decode_noalloc(const void* q, const ll_kv_pool* pool,
+                                                 const int32_t* block_table, int32_t max_blocks,
+                                                 const int32_t* context_lens, int32_t batch,
+                                                 int32_t n_heads, int32_t n_kv_heads,
+                                                 int32_t head_dim, int32_t block_size, float scale,
+                                                 void* out, int32_t* status, void* stream) {
+    ll::clear_last_error();
+    if (!q || !block_table || !context_lens || !out || !status || !pool || !pool->k || !pool->v ||
+        pool->num_blocks <= 0)
+        return LL_ERR_INVALID_ARG;
+    if (batch <= 0 || n_heads <= 0 || n_kv_heads <= 0 || max_blocks <= 0 || block_size <= 0)
+        return LL_ERR_INVALID_ARG;
+    if (head_dim != 64 && head_dim != 128) return LL_ERR_UNSUPPORTED;
+    if (n_heads % n_kv_heads != 0 || n_heads / n_kv_heads > 16) return LL_ERR_UNSUPPORTED;
+    if (((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(out) |
+          reinterpret_cast<uintptr_t>(pool->k) | reinterpret_cast<uintptr_t>(pool->v)) & 15u) != 0)
+        return LL_ERR_INVALID_ARG;
+    const size_t need = ll::attn_decode_scratch_bytes(batch, n_heads, head_dim, max_blocks, block_size);
+    if (need > kNoAllocScratchBytes) {
+        char msg[160];
+        snprintf(msg, sizeof(msg), "needs %zu bytes of scratch, the fixed array holds %zu", need,
+                 kNoAllocScratchBytes);
+        ll::set_last_error("ll_paged_attention_decode_noalloc", msg);
+        return LL_ERR_UNSUPPORTED;
+    }
+    void* scratch = nullptr;
+    if (ll::noalloc_scratch_address(&scratch) != cudaSuccess) return LL_ERR_CUDA;
+    ll::AttnDecodeArgs at{};
+    at.q = static_cast<const __nv_bfloat16*>(q);
+    at.k_pool = static_cast<const __nv_bfloat16*>(pool->k);
+    at.v_pool = static_cast<const __nv_bfloat16*>(pool->v);
+    at.context_lens = context_lens;
+    at.block_table = block_table;
+    at.max_blocks = max_blocks;
+    at.num_blocks = pool->num_blocks;
+    at.block_size = block_size;
+    at.batch = batch;
+    at.n_heads = n_heads;
+    at.n_kv_heads = n_kv_heads;
+    at.head_dim = head_dim;
+    at.scale = scale;
+    at.out = static_cast<__nv_bfloat16*>(out);
+    const size_t rows = (size_t)batch * n_heads * ll::attn_decode_max_splits(max_blocks, block_size);
+    at.part_o = static_cast<float*>(scratch);
+    at.part_ml = at.part_o + rows * head_dim;
+    at.status = status;
+    return ll::launch_attn_decode(at, static_cast<cudaStream_t>(stream)) == cudaSuccess ? LL_OK
+                                                                                          : LL_ERR_CUDA;
+}
