@@ -248,13 +248,22 @@ def traced_breakdown(api, work, steps, stream, flush):
                 work.step(stream)
     stream.synchronize()
     per = {}
-    for name, ms in tr.launches():
+    launches = tr.launches()
+    per_step = len(launches) // max(steps, 1)
+    for i, (name, ms) in enumerate(launches):
         e = per.setdefault(name, {"launches": 0, "ms": 0.0})
         e["launches"] += 1
         e["ms"] += ms
-    total = sum(v["ms"] for v in per.values())
+        # the k-th GEMM of a step (QKV, O, gate/up, down), averaged over steps
+        if name == "gemm_tc" and per_step:
+            k = sum(1 for n, _ in launches[(i // per_step) * per_step:i] if n == "gemm_tc")
+            g = per.setdefault("gemm_by_position_ms", [0.0] * 4)
+            if k < 4:
+                g[k] += ms / steps
+    total = sum(v["ms"] for k, v in per.items() if isinstance(v, dict))
     for v in per.values():
-        v["share"] = v["ms"] / total if total else 0.0
+        if isinstance(v, dict):
+            v["share"] = v["ms"] / total if total else 0.0
     return per, tr.count // max(steps, 1)
 
 
@@ -418,7 +427,8 @@ def main():
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": y_h.numel() * 2},
         "gpu_launches": launches_per_step * args.steps,
         "kernels": {k: {"launches_per_step": v["launches"] // n_tr, "ms_per_step": v["ms"] / n_tr,
-                        "share": v["share"]} for k, v in per.items()},
+                        "share": v["share"]} for k, v in per.items() if isinstance(v, dict)},
+        "gemm_ms_qkv_o_gu_down": per.get("gemm_by_position_ms"),
         "clocks": clocks.summary(),
         "device_status": st,
         "peaks": peaks,
@@ -457,7 +467,8 @@ def main():
                              "frac": (dom_bytes / (dom_ms * 1e-3) / 1e9) / peaks["hbm_gbs"] if dom_ms else 0.0,
                              "traffic": None},
                 "kernels": {k: {"launches_per_step": v["launches"] // n2, "ms_per_step": v["ms"] / n2,
-                                "share": v["share"]} for k, v in per2.items()},
+                                "share": v["share"]} for k, v in per2.items() if isinstance(v, dict)},
+                "gemm_ms_qkv_o_gu_down": per2.get("gemm_by_position_ms"),
                 "clocks": ck2.summary(),
                 "device_status": int(dw.status.item()),
             }

@@ -34,6 +34,10 @@ size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// The decode attention loads K/V in boxes of min(block_size, 64) rows that must
+// tile a 64-key span exactly and keep the 1024-byte swizzle alignment.
+bool block_size_ok(int bs) { return bs >= 16 && bs <= 256 && (bs & (bs - 1)) == 0; }
+
 bool config_ok(const ll_config* c) {
     if (!c) return false;
     if (c->hidden <= 0 || c->n_heads <= 0 || c->n_kv_heads <= 0 || c->intermediate <= 0 ||
@@ -49,6 +53,7 @@ int config_supported(const ll_config* c) {
     if (c->n_heads % c->n_kv_heads != 0) return LL_ERR_UNSUPPORTED;
     if (c->n_heads / c->n_kv_heads > 16) return LL_ERR_UNSUPPORTED;
     if (c->hidden % 16 != 0 || c->intermediate % 16 != 0) return LL_ERR_UNSUPPORTED;
+    if (!block_size_ok(c->block_size)) return LL_ERR_UNSUPPORTED;
     return LL_OK;
 }
 
@@ -506,6 +511,7 @@ int ll_paged_attention_decode(const void* q, const ll_kv_pool* pool, const int32
         return LL_ERR_INVALID_ARG;
     if (head_dim != 64 && head_dim != 128) return LL_ERR_UNSUPPORTED;
     if (n_heads % n_kv_heads != 0 || n_heads / n_kv_heads > 16) return LL_ERR_UNSUPPORTED;
+    if (!block_size_ok(block_size)) return LL_ERR_UNSUPPORTED;
     if (!aligned16(q) || !aligned16(out)) return LL_ERR_INVALID_ARG;
     const size_t need = ll_attention_workspace_size(batch, n_heads, head_dim, max_blocks, block_size);
     if (!workspace || workspace_bytes < need || !aligned16(workspace)) return LL_ERR_WORKSPACE;

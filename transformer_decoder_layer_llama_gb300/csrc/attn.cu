@@ -17,10 +17,11 @@
 // keeps about 16 significant bits instead of BF16's 8; V stays exact.
 //
 // Decode: the context of each (sequence, KV head) is cut into 1024-key
-// splits, one CTA each; the CTA's 4 warps share the G = n_heads / n_kv_heads
-// query rows of the group (padded to 16 MMA rows) and each takes 16 keys of
-// every 64-key tile from a 3-stage cp.async pipeline.  Warps merge in shared
-// memory, splits merge in a second kernel through their log-sum-exp.
+// splits, one CTA each; a producer warp streams the split's K/V tiles from the
+// paged pool with TMA into a 3-stage mbarrier ring; 4 consumer warps share
+// the G = n_heads / n_kv_heads query rows of the group (padded to 16 MMA rows)
+// and each takes 16 keys of every 64-key tile.  Warps merge in shared memory,
+// splits merge in a second kernel through their log-sum-exp.
 #include <algorithm>
 #include <cfloat>
 #include <cstdio>
@@ -294,16 +295,35 @@ __global__ void __launch_bounds__(256, 1)
 
 // ---------------------------------------------------------------- decode
 
+// Byte offset of 16-byte chunk c of row r in a K/V tile that TMA wrote with the
+// 128-byte swizzle: the tile is [D/64 column halves][ROWS rows][128 bytes] and
+// chunk (c & 7) of a row sits at position (c & 7) ^ (r & 7).
+template <int ROWS>
+LL_DEVINL uint32_t tswz(int r, int c) {
+    return (uint32_t)((c >> 3) * (ROWS * 128) + r * 128 + (((c & 7) ^ (r & 7)) << 4));
+}
+
+// One CTA = one (sequence, KV head, 1024-key split).  Warp 4 is the producer:
+// one lane loads each 64-key K and V tile of the split with TMA, as boxes of
+// min(block_size, 64) rows x 64 columns taken straight from the paged pool at
+// the block_table's physical block, into a 3-stage ring guarded by mbarriers.
+// Warps 0-3 consume: each owns 16 keys of every tile, multiplies the group's
+// query rows (padded to 16) with them on the tensor cores and keeps its own
+// online-softmax state; the four merge in shared memory at the end.
 template <int D>
-__global__ void __launch_bounds__(128)
-    attn_decode_split_kernel(const AttnDecodeArgs a, int max_splits) {
-    constexpr int BN = 64, NT = 128, STAGES = 3;
+__global__ void __launch_bounds__(160, 2)
+    attn_decode_split_kernel(const __grid_constant__ CUtensorMap tmK,
+                             const __grid_constant__ CUtensorMap tmV, const AttnDecodeArgs a,
+                             int max_splits) {
+    constexpr int BN = 64, STAGES = 3, NCONS = 128;
     constexpr int TILE = BN * D * 2;
     extern __shared__ uint8_t smem_raw[];
-    uint8_t* sbase = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
-    uint8_t* sq = sbase;                       // [16][D]
-    uint8_t* sk = sq + 16 * D * 2;             // [STAGES][BN][D]
-    uint8_t* sv = sk + STAGES * TILE;          // [STAGES][BN][D]
+    uint8_t* sbase = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* sk = sbase;                       // [STAGES][TILE]
+    uint8_t* sv = sk + STAGES * TILE;          // [STAGES][TILE]
+    uint8_t* sq = sv + STAGES * TILE;          // [16][D], XOR-swizzled rows
+    __shared__ uint64_t full_bar[STAGES], empty_bar[STAGES];
+    __shared__ int abort_s;
 
     const int split = blockIdx.x, hk = blockIdx.y, b = blockIdx.z;
     const int G = a.n_heads / a.n_kv_heads;
@@ -317,7 +337,6 @@ __global__ void __launch_bounds__(128)
     const int k_end = min(ctx, k_begin + kDecodeChunk);
     const size_t part_row = ((size_t)b * a.n_heads + (size_t)hk * G) * max_splits + split;
     if (k_begin >= k_end) {
-        // nothing to do: an empty split (ignored by the combine, which sees m = -inf)
         if (threadIdx.x < G) {
             float* ml = a.part_ml + 2 * (part_row + (size_t)threadIdx.x * max_splits);
             ml[0] = -INFINITY;
@@ -327,24 +346,79 @@ __global__ void __launch_bounds__(128)
     }
     const int32_t* table_row = a.block_table + (size_t)b * a.max_blocks;
     const int n_kt = (k_end - k_begin + BN - 1) / BN;
+    const int kt_rows = min(a.block_size, BN);
 
-    // query rows of the group, padded to 16 with zeros
+    if (threadIdx.x == 0) {
+        for (int st = 0; st < STAGES; ++st) {
+            mbar_init(&full_bar[st], 1);
+            mbar_init(&empty_bar[st], 4);
+        }
+        abort_s = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+
+    if (warp == 4) {
+        // ------------------------------------------------ producer
+        if (lane == 0) {
+            tma_prefetch_desc(&tmK);
+            tma_prefetch_desc(&tmV);
+            uint32_t issued[STAGES] = {0, 0, 0};
+            for (int kt = 0; kt < n_kt; ++kt) {
+                const int st = kt % STAGES;
+                const uint32_t ph = (uint32_t)(kt / STAGES) & 1u;
+                if (!mbar_wait_bounded(&empty_bar[st], ph ^ 1u, &abort_s, a.status)) break;
+                const int p0 = k_begin + kt * BN;
+                uint32_t bytes = 0;
+                for (int p = p0; p < p0 + BN && p < k_end; p += kt_rows) {
+                    const int blk = table_row[p / a.block_size];
+                    if (blk >= 0 && blk < a.num_blocks) bytes += 2u * (D / 64) * kt_rows * 128u;
+                }
+                mbar_arrive_expect_tx(&full_bar[st], bytes);
+                for (int p = p0, sb = 0; p < p0 + BN && p < k_end; p += kt_rows, ++sb) {
+                    const int blk = table_row[p / a.block_size];
+                    if (blk < 0 || blk >= a.num_blocks) {
+                        flag_status(a.status, LL_DEV_BAD_BLOCK);
+                        continue;
+                    }
+                    const int row = (blk * a.n_kv_heads + hk) * a.block_size + (p % a.block_size);
+#pragma unroll
+                    for (int h = 0; h < D / 64; ++h) {
+                        const uint32_t off = (uint32_t)(st * TILE + h * (BN * 128) + sb * kt_rows * 128);
+                        tma_load_2d(sk + off, &tmK, h * 64, row, &full_bar[st]);
+                        tma_load_2d(sv + off, &tmV, h * 64, row, &full_bar[st]);
+                    }
+                }
+                ++issued[st];
+            }
+            if (abort_s) {
+                volatile int never = 0;
+                for (int st = 0; st < STAGES; ++st)
+                    if (issued[st]) mbar_wait_bounded(&full_bar[st], (issued[st] - 1) & 1u, &never, nullptr);
+            }
+        }
+        __syncwarp();
+        return;
+    }
+
+    // ---------------------------------------------------- consumers (warps 0-3)
     {
         constexpr int CPR = D / 8;
-        for (int i = threadIdx.x; i < 16 * CPR; i += NT) {
+        for (int i = threadIdx.x; i < 16 * CPR; i += NCONS) {
             const int r = i / CPR, c = i % CPR;
             const bool ok = r < G;
             const __nv_bfloat16* src = a.q + ((size_t)b * a.n_heads + hk * G + (ok ? r : 0)) * D + c * 8;
             cp_async16(sq + swz<D>(r, c), src, ok);
         }
-    }
-#pragma unroll
-    for (int s = 0; s < STAGES - 1; ++s) {
-        if (s < n_kt)
-            load_kv_tile<D, NT>(sk + s * TILE, sv + s * TILE, a.k_pool, a.v_pool, table_row,
-                                k_begin + s * BN, k_end, hk, a.n_kv_heads, a.block_size,
-                                a.num_blocks, a.status);
         cp_async_commit();
+        cp_async_wait<0>();
+    }
+    asm volatile("bar.sync 1, 128;" ::: "memory");
+    uint32_t qf[D / 16][4];
+    {
+        const uint32_t qb = smem_u32(sq);
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) ldmatrix_x4(qf[ks], qb + swz<D>(lane & 15, ks * 2 + (lane >> 4)));
     }
 
     const float sl2 = a.scale * kLog2e;
@@ -353,49 +427,54 @@ __global__ void __launch_bounds__(128)
 #pragma unroll
     for (int i = 0; i < D / 8; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
     float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
-    uint32_t qf[D / 16][4];
-    bool q_loaded = false;
 
     for (int kt = 0; kt < n_kt; ++kt) {
         const int st = kt % STAGES;
-        {
-            const int nk = kt + STAGES - 1;
-            if (nk < n_kt)
-                load_kv_tile<D, NT>(sk + (nk % STAGES) * TILE, sv + (nk % STAGES) * TILE, a.k_pool,
-                                    a.v_pool, table_row, k_begin + nk * BN, k_end, hk, a.n_kv_heads,
-                                    a.block_size, a.num_blocks, a.status);
-            cp_async_commit();
+        const uint32_t ph = (uint32_t)(kt / STAGES) & 1u;
+        if (!mbar_wait_bounded(&full_bar[st], ph, &abort_s, a.status)) break;
+        uint8_t* kbp = sk + st * TILE;
+        uint8_t* vbp = sv + st * TILE;
+        // validity of this warp's 16 keys: inside the split and backed by a valid block
+        const int pbase = k_begin + kt * BN + warp * 16;
+        bool my_ok = false;
+        if (lane < 16) {
+            const int p = pbase + lane;
+            if (p < k_end) {
+                const int blk = table_row[p / a.block_size];
+                my_ok = blk >= 0 && blk < a.num_blocks;
+            }
         }
-        cp_async_wait<STAGES - 1>();
-        __syncthreads();
-        if (!q_loaded) {
-            const uint32_t qb = smem_u32(sq);
-#pragma unroll
-            for (int ks = 0; ks < D / 16; ++ks)
-                ldmatrix_x4(qf[ks], qb + swz<D>(lane & 15, ks * 2 + (lane >> 4)));
-            q_loaded = true;
+        const uint32_t okmask = __ballot_sync(0xffffffffu, my_ok) & 0xffffu;
+        if (okmask != 0xffffu) {
+            // rows that hold no valid key: zero their V so 0 * garbage cannot be NaN
+            for (int i = lane; i < 16 * (D / 8); i += 32) {
+                const int r = i / (D / 8), c = i % (D / 8);
+                if (!((okmask >> r) & 1u))
+                    *reinterpret_cast<uint4*>(vbp + tswz<BN>(warp * 16 + r, c)) = make_uint4(0, 0, 0, 0);
+            }
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            __syncwarp();
         }
-        const uint32_t kb = smem_u32(sk + st * TILE);
-        const uint32_t vb = smem_u32(sv + st * TILE);
-        // this warp's 16 keys: tile rows 16*warp .. +15
+        const uint32_t kb = smem_u32(kbp), vb = smem_u32(vbp);
         float s[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
             uint32_t bfr[4];
             const int r = warp * 16 + (lane & 7) + ((lane >> 4) << 3);
             const int c = ks * 2 + ((lane >> 3) & 1);
-            ldmatrix_x4(bfr, kb + swz<D>(r, c));
+            ldmatrix_x4(bfr, kb + tswz<BN>(r, c));
             mma_bf16_16816(s[0], qf[ks], bfr[0], bfr[1]);
             mma_bf16_16816(s[1], qf[ks], bfr[2], bfr[3]);
         }
         float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt) {
-            const int kp = k_begin + kt * BN + warp * 16 + nt * 8 + 2 * cq;
-            s[nt][0] = (kp < k_end) ? s[nt][0] * sl2 : -INFINITY;
-            s[nt][1] = (kp + 1 < k_end) ? s[nt][1] * sl2 : -INFINITY;
-            s[nt][2] = (kp < k_end) ? s[nt][2] * sl2 : -INFINITY;
-            s[nt][3] = (kp + 1 < k_end) ? s[nt][3] * sl2 : -INFINITY;
+            const int kk = nt * 8 + 2 * cq;   // key index within the warp's 16
+            const bool v0 = (okmask >> kk) & 1u, v1 = (okmask >> (kk + 1)) & 1u;
+            s[nt][0] = v0 ? s[nt][0] * sl2 : -INFINITY;
+            s[nt][1] = v1 ? s[nt][1] * sl2 : -INFINITY;
+            s[nt][2] = v0 ? s[nt][2] * sl2 : -INFINITY;
+            s[nt][3] = v1 ? s[nt][3] * sl2 : -INFINITY;
             mx0 = fmaxf(mx0, fmaxf(s[nt][0], s[nt][1]));
             mx1 = fmaxf(mx1, fmaxf(s[nt][2], s[nt][3]));
         }
@@ -410,7 +489,7 @@ __global__ void __launch_bounds__(128)
         const float al0 = exp2f(m0 - base0), al1 = exp2f(m1 - base1);
         m0 = mn0;
         m1 = mn1;
-        uint32_t ph[4], pl[4];
+        uint32_t phi[4], plo[4];
         float rs0 = 0.f, rs1 = 0.f;
         {
             float p[2][4];
@@ -424,10 +503,10 @@ __global__ void __launch_bounds__(128)
                 rs1 += p[nt][2] + p[nt][3];
             }
             // P carried as hi + lo BF16 parts (about 16 bits)
-            split_bf16x2(p[0][0], p[0][1], ph[0], pl[0]);
-            split_bf16x2(p[0][2], p[0][3], ph[1], pl[1]);
-            split_bf16x2(p[1][0], p[1][1], ph[2], pl[2]);
-            split_bf16x2(p[1][2], p[1][3], ph[3], pl[3]);
+            split_bf16x2(p[0][0], p[0][1], phi[0], plo[0]);
+            split_bf16x2(p[0][2], p[0][3], phi[1], plo[1]);
+            split_bf16x2(p[1][0], p[1][1], phi[2], plo[2]);
+            split_bf16x2(p[1][2], p[1][3], phi[3], plo[3]);
         }
         l0 = l0 * al0 + rs0;
         l1 = l1 * al1 + rs1;
@@ -443,23 +522,23 @@ __global__ void __launch_bounds__(128)
             uint32_t bfr[4];
             const int r = warp * 16 + (lane & 7) + (((lane >> 3) & 1) << 3);
             const int c = dp * 2 + (lane >> 4);
-            ldmatrix_x4_trans(bfr, vb + swz<D>(r, c));
-            mma_bf16_16816(acc[2 * dp], ph, bfr[0], bfr[1]);
-            mma_bf16_16816(acc[2 * dp + 1], ph, bfr[2], bfr[3]);
-            mma_bf16_16816(acc[2 * dp], pl, bfr[0], bfr[1]);
-            mma_bf16_16816(acc[2 * dp + 1], pl, bfr[2], bfr[3]);
+            ldmatrix_x4_trans(bfr, vb + tswz<BN>(r, c));
+            mma_bf16_16816(acc[2 * dp], phi, bfr[0], bfr[1]);
+            mma_bf16_16816(acc[2 * dp + 1], phi, bfr[2], bfr[3]);
+            mma_bf16_16816(acc[2 * dp], plo, bfr[0], bfr[1]);
+            mma_bf16_16816(acc[2 * dp + 1], plo, bfr[2], bfr[3]);
         }
-        __syncthreads();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty_bar[st]);
     }
-    cp_async_wait<0>();
 #pragma unroll
     for (int o = 1; o <= 2; o <<= 1) {
         l0 += __shfl_xor_sync(0xffffffffu, l0, o);
         l1 += __shfl_xor_sync(0xffffffffu, l1, o);
     }
 
-    // merge the 4 warps: smem [4][16] (m, l) and [4][16][D] acc, reusing the K/V stages
-    __syncthreads();
+    // merge the 4 consumer warps: [4][16] (m, l) and [4][16][D] acc, over the K ring
+    asm volatile("bar.sync 1, 128;" ::: "memory");
     float* s_ml = reinterpret_cast<float*>(sk);            // [4][16][2]
     float* s_acc = s_ml + 4 * 16 * 2;                      // [4][16][D]
     if (cq == 0) {
@@ -476,8 +555,8 @@ __global__ void __launch_bounds__(128)
         s_acc[(warp * 16 + g + 8) * D + col] = acc[i][2];
         s_acc[(warp * 16 + g + 8) * D + col + 1] = acc[i][3];
     }
-    __syncthreads();
-    for (int i = threadIdx.x; i < G * D; i += NT) {
+    asm volatile("bar.sync 1, 128;" ::: "memory");
+    for (int i = threadIdx.x; i < G * D; i += NCONS) {
         const int r = i / D, col = i % D;
         float M = -INFINITY;
 #pragma unroll
@@ -541,7 +620,7 @@ cudaError_t prefill_for(const AttnPrefillArgs& a, cudaStream_t stream) {
 template <int D>
 cudaError_t decode_for(const AttnDecodeArgs& a, cudaStream_t stream) {
     const int max_splits = attn_decode_max_splits(a.max_blocks, a.block_size);
-    const size_t smem = (size_t)(16 * D * 2) + 2 * 3 * (64 * D * 2) + 128;
+    const size_t smem = (size_t)2 * 3 * (64 * D * 2) + 16 * D * 2 + 1024;
     static bool configured = false;
     if (!configured) {
         cudaError_t e = cudaFuncSetAttribute(attn_decode_split_kernel<D>,
@@ -549,9 +628,15 @@ cudaError_t decode_for(const AttnDecodeArgs& a, cudaStream_t stream) {
         if (e != cudaSuccess) return record(e, "cudaFuncSetAttribute(attn_decode_split_kernel)");
         configured = true;
     }
+    CUtensorMap tmK, tmV;
+    const uint64_t rows = (uint64_t)a.num_blocks * a.n_kv_heads * a.block_size;
+    const uint32_t box_rows = (uint32_t)std::min(a.block_size, 64);
+    if (!make_tmap_bf16_sw128(&tmK, a.k_pool, D, rows, box_rows) ||
+        !make_tmap_bf16_sw128(&tmV, a.v_pool, D, rows, box_rows))
+        return cudaErrorInvalidValue;
     dim3 grid(max_splits, a.n_kv_heads, a.batch);
     trace_before("attn_decode_split", stream);
-    attn_decode_split_kernel<D><<<grid, 128, smem, stream>>>(a, max_splits);
+    attn_decode_split_kernel<D><<<grid, 160, smem, stream>>>(tmK, tmV, a, max_splits);
     trace_after(stream);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return record(e, "attn_decode_split_kernel launch");
@@ -631,6 +716,8 @@ extern "C" int ll_paged_attention_decode_noalloc(const void* q, const ll_kv_pool
         return LL_ERR_INVALID_ARG;
     if (head_dim != 64 && head_dim != 128) return LL_ERR_UNSUPPORTED;
     if (n_heads % n_kv_heads != 0 || n_heads / n_kv_heads > 16) return LL_ERR_UNSUPPORTED;
+    if (block_size < 16 || block_size > 256 || (block_size & (block_size - 1)) != 0)
+        return LL_ERR_UNSUPPORTED;
     if (((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(out) |
           reinterpret_cast<uintptr_t>(pool->k) | reinterpret_cast<uintptr_t>(pool->v)) & 15u) != 0)
         return LL_ERR_INVALID_ARG;

@@ -36,6 +36,8 @@ namespace ll {
 
 namespace {
 
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn();
+
 constexpr int BM = 128;          // rows of the A block = MMA M
 constexpr int BK = 64;           // K per pipeline stage: one 128-byte swizzle row of BF16
 constexpr int UK = 16;           // K of one tcgen05.mma kind::f16
@@ -213,7 +215,7 @@ LL_DEVINL void epi_token_chunk(const EpiParams& ep, int t, bool row_ok, int n0, 
 // One thread owns one output feature n (its TMEM lane) and 16 consecutive
 // tokens t0..t0+15.  All 32 lanes of the warp call this together (shuffles).
 LL_DEVINL void epi_weight_chunk(const EpiParams& ep, int n, int N, int t0, int T,
-                                const float (&v)[16]) {
+                                const float (&v)[16], const int* s_pos, const long long* s_row) {
     const bool n_ok = n < N;
     switch (ep.kind) {
         case EPI_STORE:
@@ -254,23 +256,31 @@ LL_DEVINL void epi_weight_chunk(const EpiParams& ep, int n, int N, int t0, int T
             else { sec = 2; head = (n - nq - nk) / d; e = n - nq - nk - head * d; }
             const int pair = e >> 1;
             const int orig = (sec == 2) ? e : ((e & 1) ? pair + (d >> 1) : pair);
-#pragma unroll 4
-            for (int j = 0; j < 16; ++j) {
-                float other = __shfl_xor_sync(0xffffffffu, v[j], 1);
-                int t = t0 + j;
-                if (!n_ok || t >= T) continue;
-                TokenSlot ts = token_slot(ep, t);
-                if (ts.pos < 0) continue;
-                float val = v[j];
-                if (sec != 2) {
-                    float2 c = ep.rope_cs[(size_t)ts.pos * (d >> 1) + pair];
-                    val = (e & 1) ? (v[j] * c.x + other * c.y) : (v[j] * c.x - other * c.y);
+            float other[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) other[j] = __shfl_xor_sync(0xffffffffu, v[j], 1);
+            if (!n_ok) break;
+            float2 cs[16];
+            if (sec != 2) {
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    const int p = (t0 + j < T) ? s_pos[t0 + j] : -1;
+                    cs[j] = p >= 0 ? ep.rope_cs[(size_t)p * (d >> 1) + pair] : make_float2(0.f, 0.f);
                 }
-                __nv_bfloat16 bv = __float2bfloat16_rn(val);
+            }
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                const int t = t0 + j;
+                if (t >= T || s_pos[t] < 0) continue;
+                float val = v[j];
+                if (sec != 2)
+                    val = (e & 1) ? (v[j] * cs[j].x + other[j] * cs[j].y)
+                                  : (v[j] * cs[j].x - other[j] * cs[j].y);
+                const __nv_bfloat16 bv = __float2bfloat16_rn(val);
                 if (sec == 0) {
                     ep.q_out[(size_t)t * nq + (size_t)head * d + orig] = bv;
-                } else if (ts.kv_row >= 0) {
-                    size_t row = (size_t)ts.kv_row + (size_t)head * ep.block_size;
+                } else if (s_row[t] >= 0) {
+                    const size_t row = (size_t)s_row[t] + (size_t)head * ep.block_size;
                     (sec == 1 ? ep.k_pool : ep.v_pool)[row * d + orig] = bv;
                 }
             }
@@ -300,6 +310,8 @@ __global__ void __launch_bounds__(kThreads, 2)
     __shared__ uint32_t tmem_base_s;
     __shared__ int abort_s;
     __shared__ int last_s;
+    __shared__ int tok_pos_s[kSwapMaxTokens];        // weight form, EPI_QKV: per-token position
+    __shared__ long long tok_row_s[kSwapMaxTokens];  // ... and pool row of KV head 0 (or -1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -426,6 +438,16 @@ __global__ void __launch_bounds__(kThreads, 2)
         const int q = warp & 3;
         const int r = q * 32 + lane;             // TMEM lane = row of the A block
         const uint32_t lane_base = (uint32_t)(q * 32) << 16;
+        if (a.swap && a.ep.kind == EPI_QKV) {
+            // each token's position and cache row, once per CTA (the tokens are few)
+            const int et = threadIdx.x - 64;
+            if (et < a.tokens) {
+                TokenSlot ts = token_slot(a.ep, et);
+                tok_pos_s[et] = ts.pos;
+                tok_row_s[et] = ts.kv_row;
+            }
+            epi_bar();
+        }
         int local = 0;
         for (int u = blockIdx.x; u < a.units; u += gridDim.x, ++local) {
             int a_blk, b_blk, split, kb0, kb1;
@@ -463,7 +485,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                     for (int c = 0; c < a.bn; c += 16) {
                         float v[16];
                         tmem_ld16(taddr + (uint32_t)c, v);
-                        epi_weight_chunk(a.ep, n, a.n, c, T, v);
+                        epi_weight_chunk(a.ep, n, a.n, c, T, v, tok_pos_s, tok_row_s);
                     }
                     tc_fence_before();
                     mbar_arrive(&tempty_bar[buf]);
@@ -494,14 +516,17 @@ __global__ void __launch_bounds__(kThreads, 2)
                         for (int c = 0; c < a.bn; c += 16) {
                             float v[16];
 #pragma unroll
-                            for (int j = 0; j < 16; ++j) {
-                                float s = 0.f;
-                                if (c + j < T)
-                                    for (int sp = 0; sp < a.splits; ++sp)
-                                        s += __ldcg(p0 + (size_t)sp * (BM * a.bn) + (size_t)(c + j) * BM + r);
-                                v[j] = s;
+                            for (int j = 0; j < 16; ++j) v[j] = 0.f;
+                            // 16 independent loads in flight per split
+                            for (int sp = 0; sp < a.splits; ++sp) {
+                                const float* ps = p0 + (size_t)sp * (BM * a.bn) + (size_t)c * BM + r;
+                                float t16[16];
+#pragma unroll
+                                for (int j = 0; j < 16; ++j) t16[j] = (c + j < T) ? __ldcg(ps + j * BM) : 0.f;
+#pragma unroll
+                                for (int j = 0; j < 16; ++j) v[j] += t16[j];
                             }
-                            epi_weight_chunk(a.ep, n, a.n, c, T, v);
+                            epi_weight_chunk(a.ep, n, a.n, c, T, v, tok_pos_s, tok_row_s);
                         }
                     }
                 }
@@ -533,26 +558,7 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 
 // 2-D BF16 tensor [rows, inner] row-major, box [box_rows, 64] with the 128-byte swizzle.
 bool make_tmap(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t rows, uint32_t box_rows) {
-    auto fn = encode_fn();
-    if (!fn) {
-        set_last_error("cuTensorMapEncodeTiled", "driver entry point not found");
-        return false;
-    }
-    cuuint64_t dims[2] = {inner, rows};
-    cuuint64_t strides[1] = {inner * 2};
-    cuuint32_t box[2] = {(cuuint32_t)BK, box_rows};
-    cuuint32_t estr[2] = {1, 1};
-    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides,
-                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    if (r != CUDA_SUCCESS) {
-        char msg[160];
-        snprintf(msg, sizeof(msg), "CUresult %d (inner %llu, rows %llu, box %u x %u)", (int)r,
-                 (unsigned long long)inner, (unsigned long long)rows, (unsigned)BK, box_rows);
-        set_last_error("cuTensorMapEncodeTiled", msg);
-        return false;
-    }
-    return true;
+    return make_tmap_bf16_sw128(m, ptr, inner, rows, box_rows);
 }
 
 int ceil_div(int a, int b) { return (a + b - 1) / b; }
@@ -604,6 +610,30 @@ Plan make_plan(int tokens, int n, int k, int sms) {
 }
 
 }  // namespace
+
+bool make_tmap_bf16_sw128(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t rows,
+                          uint32_t box_rows) {
+    auto fn = encode_fn();
+    if (!fn) {
+        set_last_error("cuTensorMapEncodeTiled", "driver entry point not found");
+        return false;
+    }
+    cuuint64_t dims[2] = {inner, rows};
+    cuuint64_t strides[1] = {inner * 2};
+    cuuint32_t box[2] = {(cuuint32_t)BK, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides,
+                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        char msg[160];
+        snprintf(msg, sizeof(msg), "CUresult %d (inner %llu, rows %llu, box %u x %u)", (int)r,
+                 (unsigned long long)inner, (unsigned long long)rows, (unsigned)BK, box_rows);
+        set_last_error("cuTensorMapEncodeTiled", msg);
+        return false;
+    }
+    return true;
+}
 
 int device_sm_count() {
     int dev = 0, sms = 0;

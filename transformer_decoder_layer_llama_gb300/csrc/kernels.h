@@ -61,6 +61,12 @@ int gemm_counter_bound(int n);          // counters needed for an output of n fe
 
 cudaError_t launch_gemm(const GemmProblem& p, cudaStream_t stream);
 
+// Tensor map of a row-major BF16 matrix [rows, inner] read in boxes of
+// box_rows x 64 elements with the 128-byte swizzle (the layout tcgen05 and
+// the ldmatrix readers expect).  Records the reason and returns false on error.
+bool make_tmap_bf16_sw128(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t rows,
+                          uint32_t box_rows);
+
 int device_sm_count();
 
 // Records why the current call failed (thread-local; read by ll_last_error).
