@@ -60,8 +60,6 @@ struct GemmArgs {
     uint32_t stage_bytes;
     uint32_t a_bytes;
     uint32_t tmem_cols;
-    float* partials;
-    int32_t* counters;
 };
 
 LL_DEVINL void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
@@ -212,11 +210,14 @@ LL_DEVINL void epi_token_chunk(const EpiParams& ep, int t, bool row_ok, int n0, 
 }
 
 // ---------------------------------------------------------------- weight-form epilogue
-// One thread owns one output feature n (its TMEM lane) and 16 consecutive
-// tokens t0..t0+15.  All 32 lanes of the warp call this together (shuffles).
+// One thread owns one output feature n (its TMEM lane) and up to 16
+// consecutive tokens t0..t0+tcount-1.  All 32 lanes of the warp call this
+// together (shuffles).
 LL_DEVINL void epi_weight_chunk(const EpiParams& ep, int n, int N, int t0, int T,
-                                const float (&v)[16], const int* s_pos, const long long* s_row) {
+                                const float (&v)[16], const int* s_pos, const long long* s_row,
+                                int tcount = 16) {
     const bool n_ok = n < N;
+    T = min(T, t0 + tcount);   // this call covers tokens t0 .. min(T, t0 + tcount) - 1
     switch (ep.kind) {
         case EPI_STORE:
             if (n_ok)
@@ -289,19 +290,18 @@ LL_DEVINL void epi_weight_chunk(const EpiParams& ep, int n, int N, int t0, int T
     }
 }
 
-LL_DEVINL void unit_coords(const GemmArgs& a, int u, int& a_blk, int& b_blk, int& split, int& kb0,
-                           int& kb1) {
-    split = u % a.splits;
-    int tile = u / a.splits;
-    a_blk = tile % a.tiles_m;
-    b_blk = tile / a.tiles_m;
-    kb0 = (int)((long long)split * a.num_kb / a.splits);
-    kb1 = (int)((long long)(split + 1) * a.num_kb / a.splits);
+LL_DEVINL void unit_coords(const GemmArgs& a, int u, int& a_blk, int& b_blk, int& kb0, int& kb1) {
+    a_blk = u % a.tiles_m;
+    b_blk = u / a.tiles_m;
+    kb0 = 0;
+    kb1 = a.num_kb;
 }
 
-__global__ void __launch_bounds__(kThreads, 2)
-    gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                   const GemmArgs a) {
+// ---------------------------------------------------------------- token form
+// Persistent CTAs over output tiles of tokens x features.
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_token_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                      const GemmArgs a) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~uintptr_t(1023));
@@ -309,9 +309,6 @@ __global__ void __launch_bounds__(kThreads, 2)
     __shared__ uint64_t tfull_bar[2], tempty_bar[2], drain_bar;
     __shared__ uint32_t tmem_base_s;
     __shared__ int abort_s;
-    __shared__ int last_s;
-    __shared__ int tok_pos_s[kSwapMaxTokens];        // weight form, EPI_QKV: per-token position
-    __shared__ long long tok_row_s[kSwapMaxTokens];  // ... and pool row of KV head 0 (or -1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -328,7 +325,6 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
         mbar_init(&drain_bar, 1);
         abort_s = 0;
-        last_s = 0;
         fence_mbar_init();
     }
     if (warp == 0 && lane == 0) {
@@ -351,11 +347,10 @@ __global__ void __launch_bounds__(kThreads, 2)
             uint32_t phase = 0;
             uint32_t issued[MAX_STAGES];
             for (int s = 0; s < MAX_STAGES; ++s) issued[s] = 0;
-            const uint64_t pol_w = l2_policy_evict_first();
             bool ok = true;
             for (int u = blockIdx.x; u < a.units && ok; u += gridDim.x) {
-                int a_blk, b_blk, split, kb0, kb1;
-                unit_coords(a, u, a_blk, b_blk, split, kb0, kb1);
+                int a_blk, b_blk, kb0, kb1;
+                unit_coords(a, u, a_blk, b_blk, kb0, kb1);
                 for (int kb = kb0; kb < kb1; ++kb) {
                     if (!mbar_wait_bounded(&empty_bar[stage], phase ^ 1, &abort_s, status)) {
                         ok = false;
@@ -364,14 +359,8 @@ __global__ void __launch_bounds__(kThreads, 2)
                     uint8_t* sa = smem + (size_t)stage * a.stage_bytes;
                     uint8_t* sb = sa + a.a_bytes;
                     mbar_arrive_expect_tx(&full_bar[stage], a.stage_bytes);
-                    if (a.swap) {
-                        // weights stream once: keep them from pushing the activations out of L2
-                        tma_load_2d_hint(sa, &tmA, kb * BK, a_blk * BM, &full_bar[stage], pol_w);
-                        tma_load_2d(sb, &tmB, kb * BK, b_blk * a.bn, &full_bar[stage]);
-                    } else {
-                        tma_load_2d(sa, &tmA, kb * BK, a_blk * BM, &full_bar[stage]);
-                        tma_load_2d(sb, &tmB, kb * BK, b_blk * a.bn, &full_bar[stage]);
-                    }
+                    tma_load_2d(sa, &tmA, kb * BK, a_blk * BM, &full_bar[stage]);
+                    tma_load_2d(sb, &tmB, kb * BK, b_blk * a.bn, &full_bar[stage]);
                     for (int s = 0; s < MAX_STAGES; ++s) issued[s] += (s == stage);
                     if (++stage == a.stages) {
                         stage = 0;
@@ -396,8 +385,8 @@ __global__ void __launch_bounds__(kThreads, 2)
             int local = 0;
             bool ok = true;
             for (int u = blockIdx.x; u < a.units && ok; u += gridDim.x, ++local) {
-                int a_blk, b_blk, split, kb0, kb1;
-                unit_coords(a, u, a_blk, b_blk, split, kb0, kb1);
+                int a_blk, b_blk, kb0, kb1;
+                unit_coords(a, u, a_blk, b_blk, kb0, kb1);
                 const int buf = local & 1;
                 const uint32_t accp = (local >> 1) & 1;
                 if (!mbar_wait_bounded(&tempty_bar[buf], accp ^ 1, &abort_s, status)) break;
@@ -436,102 +425,227 @@ __global__ void __launch_bounds__(kThreads, 2)
     } else {
         // ---------------------------------------------------- epilogue warps
         const int q = warp & 3;
-        const int r = q * 32 + lane;             // TMEM lane = row of the A block
+        const int r = q * 32 + lane;             // TMEM lane = token row of the tile
         const uint32_t lane_base = (uint32_t)(q * 32) << 16;
-        if (a.swap && a.ep.kind == EPI_QKV) {
-            // each token's position and cache row, once per CTA (the tokens are few)
-            const int et = threadIdx.x - 64;
-            if (et < a.tokens) {
-                TokenSlot ts = token_slot(a.ep, et);
-                tok_pos_s[et] = ts.pos;
-                tok_row_s[et] = ts.kv_row;
-            }
-            epi_bar();
-        }
         int local = 0;
         for (int u = blockIdx.x; u < a.units; u += gridDim.x, ++local) {
-            int a_blk, b_blk, split, kb0, kb1;
-            unit_coords(a, u, a_blk, b_blk, split, kb0, kb1);
+            int a_blk, b_blk, kb0, kb1;
+            unit_coords(a, u, a_blk, b_blk, kb0, kb1);
             const int buf = local & 1;
             const uint32_t accp = (local >> 1) & 1;
-            const bool got = mbar_wait_bounded(&tfull_bar[buf], accp, &abort_s, status);
-            if (a.swap && a.splits > 1) {
-                // this path meets again at named barriers: leave together or not at all
-                epi_bar();
-                if (abort_s) break;
-            } else if (!got) {
-                break;
-            }
+            if (!mbar_wait_bounded(&tfull_bar[buf], accp, &abort_s, status)) break;
             tc_fence_after();
             const uint32_t taddr = tmem + lane_base + (uint32_t)(buf * a.bn);
-            if (!a.swap) {
-                const int t = a_blk * BM + r;
-                const bool row_ok = t < a.tokens;
-                TokenSlot ts{-1, -1};
-                if (a.ep.kind == EPI_QKV && row_ok) ts = token_slot(a.ep, t);
-                for (int c = 0; c < a.bn; c += 16) {
-                    const int n0 = b_blk * a.bn + c;
-                    if (n0 >= a.n) break;
-                    float v[16];
-                    tmem_ld16(taddr + (uint32_t)c, v);
-                    epi_token_chunk(a.ep, t, row_ok, n0, a.n, ts, v);
+            const int t = a_blk * BM + r;
+            const bool row_ok = t < a.tokens;
+            TokenSlot ts{-1, -1};
+            if (a.ep.kind == EPI_QKV && row_ok) ts = token_slot(a.ep, t);
+            for (int c = 0; c < a.bn; c += 16) {
+                const int n0 = b_blk * a.bn + c;
+                if (n0 >= a.n) break;
+                float v[16];
+                tmem_ld16(taddr + (uint32_t)c, v);
+                epi_token_chunk(a.ep, t, row_ok, n0, a.n, ts, v);
+            }
+            tc_fence_before();
+            mbar_arrive(&tempty_bar[buf]);
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem, a.tmem_cols);
+}
+
+// ---------------------------------------------------------------- weight form
+// One CTA = one (128-feature tile, K split); the splits of a tile form one
+// thread-block cluster (cluster rank = split).  Each CTA accumulates its K
+// range in TMEM, drains the float32 partial [tokens][128] into its own
+// shared memory, and after a cluster barrier reduces its share of the tokens
+// over all the cluster's partials through distributed shared memory, then
+// runs the fused epilogue on them.  Deterministic; no global scratch.
+
+LL_DEVINL void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
+}
+
+// shared::cluster address of `local_smem_addr` in the CTA of cluster rank `rank`
+LL_DEVINL uint32_t dsmem_map(uint32_t local_smem_addr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local_smem_addr), "r"(rank));
+    return r;
+}
+
+LL_DEVINL float dsmem_ld(uint32_t cluster_addr) {
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(cluster_addr) : "memory");
+    return v;
+}
+
+__global__ void __launch_bounds__(kThreads, 2)
+    gemm_weight_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
+                       const GemmArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                               ~uintptr_t(1023));
+    __shared__ uint64_t full_bar[MAX_STAGES], empty_bar[MAX_STAGES];
+    __shared__ uint64_t tfull_bar, drain_bar;
+    __shared__ uint32_t tmem_base_s;
+    __shared__ int abort_s;
+    __shared__ int tok_pos_s[kSwapMaxTokens];        // EPI_QKV: per-token position
+    __shared__ long long tok_row_s[kSwapMaxTokens];  // ... and pool row of KV head 0 (or -1)
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    int32_t* status = a.ep.status;
+    const int split = blockIdx.x;                    // == cluster rank (cluster = the tile's splits)
+    const int tile = blockIdx.y;
+    const int kb0 = (int)((long long)split * a.num_kb / a.splits);
+    const int kb1 = (int)((long long)(split + 1) * a.num_kb / a.splits);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < a.stages; ++s) {
+            mbar_init(&full_bar[s], 1);
+            mbar_init(&empty_bar[s], 1);
+        }
+        mbar_init(&tfull_bar, 1);
+        mbar_init(&drain_bar, 1);
+        abort_s = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tmW);
+        tma_prefetch_desc(&tmX);
+    }
+    if (warp == 1) {
+        tmem_alloc(&tmem_base_s, a.tmem_cols);
+        tmem_relinquish();
+    }
+    if (warp >= 2 && a.ep.kind == EPI_QKV) {
+        // each token's position and cache row, once per CTA (the tokens are few)
+        const int et = threadIdx.x - 64;
+        if (et < a.tokens) {
+            TokenSlot ts = token_slot(a.ep, et);
+            tok_pos_s[et] = ts.pos;
+            tok_row_s[et] = ts.kv_row;
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_base_s;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // weights stream once: keep them from pushing the activations out of L2
+            const uint64_t pol_w = l2_policy_evict_first();
+            int stage = 0;
+            uint32_t phase = 0;
+            uint32_t issued[MAX_STAGES];
+            for (int s = 0; s < MAX_STAGES; ++s) issued[s] = 0;
+            for (int kb = kb0; kb < kb1; ++kb) {
+                if (!mbar_wait_bounded(&empty_bar[stage], phase ^ 1, &abort_s, status)) break;
+                uint8_t* sa = smem + (size_t)stage * a.stage_bytes;
+                uint8_t* sb = sa + a.a_bytes;
+                mbar_arrive_expect_tx(&full_bar[stage], a.stage_bytes);
+                tma_load_2d_hint(sa, &tmW, kb * BK, tile * BM, &full_bar[stage], pol_w);
+                tma_load_2d(sb, &tmX, kb * BK, 0, &full_bar[stage]);
+                for (int s = 0; s < MAX_STAGES; ++s) issued[s] += (s == stage);
+                if (++stage == a.stages) {
+                    stage = 0;
+                    phase ^= 1;
                 }
-                tc_fence_before();
-                mbar_arrive(&tempty_bar[buf]);
-            } else {
-                const int n = a_blk * BM + r;
-                const int T = a.tokens;
+            }
+            if (abort_s) {
+                volatile int never = 0;
+                for (int s = 0; s < a.stages; ++s)
+                    if (issued[s]) mbar_wait_bounded(&full_bar[s], (issued[s] - 1) & 1, &never, nullptr);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        if (lane == 0) {
+            const uint32_t idesc = umma_idesc_bf16(BM, a.bn);
+            int stage = 0;
+            uint32_t phase = 0;
+            bool ok = true;
+            for (int kb = kb0; kb < kb1; ++kb) {
+                if (!mbar_wait_bounded(&full_bar[stage], phase, &abort_s, status)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t sa = smem_u32(smem + (size_t)stage * a.stage_bytes);
+                const uint32_t sb = sa + a.a_bytes;
+                const uint64_t da = umma_desc_sw128(sa);
+                const uint64_t db = umma_desc_sw128(sb);
+#pragma unroll
+                for (int kk = 0; kk < BK / UK; ++kk)
+                    tc_mma_bf16(tmem, da + (uint64_t)(kk * 2), db + (uint64_t)(kk * 2), idesc,
+                                (kb > kb0 || kk > 0) ? 1u : 0u);
+                tc_commit(&empty_bar[stage]);
+                if (++stage == a.stages) {
+                    stage = 0;
+                    phase ^= 1;
+                }
+            }
+            if (ok) tc_commit(&tfull_bar);
+            tc_commit(&drain_bar);
+            volatile int never = 0;
+            mbar_wait_bounded(&drain_bar, 0, &never, status);
+        }
+        __syncwarp();
+    }
+
+    // ---------------------------------------------------- epilogue warps: drain TMEM
+    const int q = warp & 3;
+    const int r = q * 32 + lane;                 // TMEM lane = feature row of the tile
+    const int n = tile * BM + r;
+    const int T = a.tokens;
+    float* part = reinterpret_cast<float*>(smem);   // [bn][128] float32, over the idle ring
+    bool have = false;
+    if (warp >= 2) {
+        have = mbar_wait_bounded(&tfull_bar, 0, &abort_s, status);
+        if (have) {
+            tc_fence_after();
+            const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16);
+            for (int c = 0; c < a.bn; c += 16) {
+                float v[16];
+                tmem_ld16(taddr + (uint32_t)c, v);
                 if (a.splits == 1) {
-                    for (int c = 0; c < a.bn; c += 16) {
-                        float v[16];
-                        tmem_ld16(taddr + (uint32_t)c, v);
-                        epi_weight_chunk(a.ep, n, a.n, c, T, v, tok_pos_s, tok_row_s);
-                    }
-                    tc_fence_before();
-                    mbar_arrive(&tempty_bar[buf]);
+                    epi_weight_chunk(a.ep, n, a.n, c, T, v, tok_pos_s, tok_row_s);
                 } else {
-                    const int tile = a_blk;
-                    float* part = a.partials + (size_t)(tile * a.splits + split) * (size_t)(BM * a.bn);
-                    for (int c = 0; c < a.bn; c += 16) {
-                        float v[16];
-                        tmem_ld16(taddr + (uint32_t)c, v);
 #pragma unroll
-                        for (int j = 0; j < 16; ++j)
-                            if (c + j < T) __stcg(part + (size_t)(c + j) * BM + r, v[j]);
-                    }
-                    tc_fence_before();
-                    mbar_arrive(&tempty_bar[buf]);
-                    __threadfence();
-                    epi_bar();
-                    if (threadIdx.x == 64) {
-                        int old = atomicAdd(&a.counters[tile], 1);
-                        int last = (old == a.splits - 1);
-                        if (last) atomicExch(&a.counters[tile], 0);
-                        last_s = last;
-                    }
-                    epi_bar();
-                    if (last_s) {
-                        __threadfence();
-                        const float* p0 = a.partials + (size_t)(tile * a.splits) * (size_t)(BM * a.bn);
-                        for (int c = 0; c < a.bn; c += 16) {
-                            float v[16];
-#pragma unroll
-                            for (int j = 0; j < 16; ++j) v[j] = 0.f;
-                            // 16 independent loads in flight per split
-                            for (int sp = 0; sp < a.splits; ++sp) {
-                                const float* ps = p0 + (size_t)sp * (BM * a.bn) + (size_t)c * BM + r;
-                                float t16[16];
-#pragma unroll
-                                for (int j = 0; j < 16; ++j) t16[j] = (c + j < T) ? __ldcg(ps + j * BM) : 0.f;
-#pragma unroll
-                                for (int j = 0; j < 16; ++j) v[j] += t16[j];
-                            }
-                            epi_weight_chunk(a.ep, n, a.n, c, T, v, tok_pos_s, tok_row_s);
-                        }
-                    }
+                    for (int j = 0; j < 16; ++j) part[(c + j) * BM + r] = v[j];
                 }
             }
         }
+    }
+    if (a.splits > 1) {
+        cluster_sync_all();                      // every partial of the tile is in shared memory
+        if (warp >= 2 && !abort_s) {
+            // this CTA's tokens: [t_lo, t_hi), summed over the cluster's partials
+            const int t_lo = split * T / a.splits, t_hi = (split + 1) * T / a.splits;
+            const uint32_t my_part = smem_u32(part);
+            for (int t0 = t_lo; t0 < t_hi; t0 += 16) {
+                const int cnt = min(16, t_hi - t0);
+                float v[16];
+#pragma unroll
+                for (int j = 0; j < 16; ++j) v[j] = 0.f;
+                for (int sp = 0; sp < a.splits; ++sp) {
+                    const uint32_t base = dsmem_map(my_part, (uint32_t)sp);
+                    float t16[16];
+#pragma unroll
+                    for (int j = 0; j < 16; ++j)
+                        t16[j] = j < cnt ? dsmem_ld(base + (uint32_t)(((t0 + j) * BM + r) * 4)) : 0.f;
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) v[j] += t16[j];
+                }
+                epi_weight_chunk(a.ep, n, a.n, t0, T, v, tok_pos_s, tok_row_s, cnt);
+            }
+        }
+        cluster_sync_all();                      // nobody leaves while others read its partial
     }
 
     tc_fence_before();
@@ -576,6 +690,24 @@ struct Plan {
     size_t smem_bytes;
 };
 
+// Weight form: split count s in [1, 8] (one cluster per tile) minimising
+// waves(s) / s, the time of a pass over the weights when every CTA streams
+// 1/s of a tile; ties go to fewer splits.  Each split keeps >= 4 K blocks.
+int choose_splits(int tiles, int num_kb, int slots) {
+    const int s_max = std::max(1, std::min(8, num_kb / 4));
+    int best = 1;
+    double best_cost = 1e30;
+    for (int sp = 1; sp <= s_max; ++sp) {
+        const double waves = (double)((tiles * sp + slots - 1) / slots);
+        const double cost = waves / sp;
+        if (cost < best_cost - 1e-9) {
+            best_cost = cost;
+            best = sp;
+        }
+    }
+    return best;
+}
+
 Plan make_plan(int tokens, int n, int k, int sms) {
     Plan p{};
     p.swap = tokens <= kSwapMaxTokens;
@@ -589,22 +721,20 @@ Plan make_plan(int tokens, int n, int k, int sms) {
         p.stage_bytes = p.a_bytes + p.bn * BK * 2;
         p.stages = 4;
         p.ctas_per_sm = 1;
+        p.units = p.tiles_m * p.tiles_n;
+        p.tmem_cols = pow2_at_least(2u * (uint32_t)p.bn);
     } else {
         p.bn = std::max(16, ceil_div(tokens, 16) * 16);
         p.tiles_m = ceil_div(n, BM);
         p.tiles_n = 1;
         p.stage_bytes = p.a_bytes + p.bn * BK * 2;
         p.ctas_per_sm = 2;
-        int budget = (227 * 1024) / p.ctas_per_sm - 1024 - 1024;
+        const int budget = (227 * 1024) / p.ctas_per_sm - 2048;
         p.stages = std::min(MAX_STAGES, budget / (int)p.stage_bytes);
-        int target = sms * p.ctas_per_sm;
-        int splits = std::max(1, (target + p.tiles_m / 2) / p.tiles_m);
-        splits = std::min(splits, std::max(1, p.num_kb / 4));
-        splits = std::min(splits, 16);
-        p.splits = splits;
+        p.splits = choose_splits(p.tiles_m, p.num_kb, sms * p.ctas_per_sm);
+        p.units = p.tiles_m * p.splits;
+        p.tmem_cols = pow2_at_least((uint32_t)p.bn);
     }
-    p.units = p.tiles_m * p.tiles_n * p.splits;
-    p.tmem_cols = pow2_at_least(2u * (uint32_t)p.bn);
     p.smem_bytes = (size_t)p.stages * p.stage_bytes + 1024;
     return p;
 }
@@ -643,23 +773,19 @@ int device_sm_count() {
 }
 
 void gemm_scratch_need(int tokens, int n, int k, size_t* partial_bytes, int* counters) {
-    int sms = device_sm_count();
-    if (sms <= 0) sms = 160;
-    Plan p = make_plan(tokens, n, k, sms);
-    *partial_bytes = p.splits > 1 ? (size_t)p.tiles_m * p.splits * BM * p.bn * sizeof(float) : 0;
-    *counters = p.swap ? p.tiles_m : 0;
+    (void)tokens; (void)n; (void)k;
+    // split-K partials stay in the cluster's shared memory: no global scratch
+    *partial_bytes = 0;
+    *counters = 0;
 }
 
-size_t gemm_partial_bound_bytes() {
-    // weight form only: units <= max(tiles, 2 * 160 SMs * 1.5) and bn <= 64
-    return (size_t)(2 * 160 * 3 / 2 + 64) * BM * kSwapMaxTokens * sizeof(float);
-}
+size_t gemm_partial_bound_bytes() { return 0; }
 
-int gemm_counter_bound(int n) { return ceil_div(n, BM); }
+int gemm_counter_bound(int n) { (void)n; return 0; }
 
 cudaError_t launch_gemm(const GemmProblem& pr, cudaStream_t stream) {
     int sms = device_sm_count();
-    if (sms <= 0) return cudaErrorNoDevice;
+    if (sms <= 0) return record(cudaErrorNoDevice, "launch_gemm");
     Plan p = make_plan(pr.tokens, pr.n, pr.k, sms);
     GemmArgs a{};
     a.ep = pr.ep;
@@ -677,15 +803,6 @@ cudaError_t launch_gemm(const GemmProblem& pr, cudaStream_t stream) {
     a.stage_bytes = p.stage_bytes;
     a.a_bytes = p.a_bytes;
     a.tmem_cols = p.tmem_cols;
-    a.partials = pr.partials;
-    a.counters = pr.counters;
-    if (p.splits > 1) {
-        size_t need = (size_t)p.tiles_m * p.splits * BM * p.bn * sizeof(float);
-        if (!pr.partials || pr.partial_bytes < need || !pr.counters || pr.counter_cap < p.tiles_m) {
-            set_last_error("launch_gemm", "split-K scratch too small");
-            return cudaErrorInvalidValue;
-        }
-    }
     CUtensorMap tmA, tmB;
     bool ok;
     if (!p.swap) {
@@ -694,19 +811,47 @@ cudaError_t launch_gemm(const GemmProblem& pr, cudaStream_t stream) {
         ok = make_tmap(&tmA, pr.w, pr.k, pr.n, BM) && make_tmap(&tmB, pr.act, pr.k, pr.tokens, p.bn);
     }
     if (!ok) return cudaErrorInvalidValue;
-    static int configured_smem = 0;
-    if ((int)p.smem_bytes > configured_smem) {
-        // dynamic + static shared memory must fit the per-block opt-in limit
-        cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)p.smem_bytes);
-        if (e != cudaSuccess) return record(e, "cudaFuncSetAttribute(gemm_tc_kernel)");
-        configured_smem = (int)p.smem_bytes;
+    if (!p.swap) {
+        static int configured_smem = 0;
+        if ((int)p.smem_bytes > configured_smem) {
+            // dynamic + static shared memory must fit the per-block opt-in limit
+            cudaError_t e = cudaFuncSetAttribute(gemm_token_kernel,
+                                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 (int)p.smem_bytes);
+            if (e != cudaSuccess) return record(e, "cudaFuncSetAttribute(gemm_token_kernel)");
+            configured_smem = (int)p.smem_bytes;
+        }
+        const int grid = std::min(p.units, sms * p.ctas_per_sm);
+        trace_before("gemm_tc", stream);
+        gemm_token_kernel<<<grid, kThreads, p.smem_bytes, stream>>>(tmA, tmB, a);
+        trace_after(stream);
+        return record(cudaGetLastError(), "gemm_token_kernel launch");
     }
-    int grid = std::min(p.units, sms * p.ctas_per_sm);
+    static int configured_smem_w = 0;
+    if ((int)p.smem_bytes > configured_smem_w) {
+        cudaError_t e = cudaFuncSetAttribute(gemm_weight_kernel,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)p.smem_bytes);
+        if (e != cudaSuccess) return record(e, "cudaFuncSetAttribute(gemm_weight_kernel)");
+        configured_smem_w = (int)p.smem_bytes;
+    }
+    cudaLaunchConfig_t lc = {};
+    lc.gridDim = dim3((unsigned)p.splits, (unsigned)p.tiles_m, 1);
+    lc.blockDim = dim3(kThreads, 1, 1);
+    lc.dynamicSmemBytes = p.smem_bytes;
+    lc.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)p.splits;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    lc.attrs = attr;
+    lc.numAttrs = 1;
     trace_before("gemm_tc", stream);
-    gemm_tc_kernel<<<grid, kThreads, p.smem_bytes, stream>>>(tmA, tmB, a);
+    cudaError_t e = cudaLaunchKernelEx(&lc, gemm_weight_kernel, tmA, tmB, a);
     trace_after(stream);
-    return record(cudaGetLastError(), "gemm_tc_kernel launch");
+    if (e != cudaSuccess) return record(e, "gemm_weight_kernel launch");
+    return record(cudaGetLastError(), "gemm_weight_kernel launch");
 }
 
 }  // namespace ll
