@@ -42,6 +42,36 @@ from transformer_decoder_layer_llama_gb300 import synth  # noqa: E402
 METRIC = "decode-layer HBM GB/s & tok/s; prefill-layer TFLOP/s; % of roofline, 1×GB300"
 L2_FLUSH_BYTES = 256 << 20
 
+# DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) of the dominant
+# kernels, from the ncu captures summarised in profiles/, with the SHA-256 of the source
+# file the kernel was built from at capture time.  A changed source makes the figure stale
+# and the bench reports traffic as null.
+NCU_TRAFFIC = {
+    # gemm_token_kernel, 7B prefill layer: mean over its 4 launches (QKV, O, gate/up, down)
+    "prefill_gemm": {"file": "transformer_decoder_layer_llama_gb300/csrc/gemm_tc.cu",
+                     "sha256": "3471b371352cecf0c9876ccf137179dbc494e25bcecedcf780c3dffb35124269", "bytes_per_launch": 166.96e6},
+    # attn_decode_split_kernel, 7B decode (batch 64)
+    "llama2_7b_decode_attn": {"file": "transformer_decoder_layer_llama_gb300/csrc/attn.cu",
+                              "sha256": "1fe45d5f7900fc5aa93b3e50982462b484b3bdbf3faf77d4dde5ff4e6891b1ea", "bytes_per_launch": 2245.9e6},
+    # gemm_weight_kernel, 70B decode: mean over its 4 launches
+    "llama70b_gqa_decode_gemm": {"file": "transformer_decoder_layer_llama_gb300/csrc/gemm_tc.cu",
+                                 "sha256": "3471b371352cecf0c9876ccf137179dbc494e25bcecedcf780c3dffb35124269", "bytes_per_launch": 429.7e6},
+}
+
+
+def ncu_traffic(key):
+    import hashlib
+    e = NCU_TRAFFIC.get(key)
+    if not e or not e["sha256"]:
+        return None
+    try:
+        with open(os.path.join(ROOT, e["file"]), "rb") as f:
+            if hashlib.sha256(f.read()).hexdigest() != e["sha256"]:
+                return None
+    except OSError:
+        return None
+    return e["bytes_per_launch"]
+
 
 # ---------------------------------------------------------------- work accounting
 
@@ -317,7 +347,23 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-extras", action="store_true", help="skip the decode workloads")
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle CPU baseline")
+    ap.add_argument("--ncu-target", choices=["llama2_7b_prefill", "llama2_7b_decode",
+                                             "llama70b_gqa_decode"],
+                    help="set up one workload, run --calls untimed layer calls and exit (for ncu)")
+    ap.add_argument("--calls", type=int, default=2)
     args = ap.parse_args()
+    if args.ncu_target:
+        from transformer_decoder_layer_llama_gb300 import api
+        torch.cuda.set_device(0)
+        st = torch.cuda.Stream()
+        wl = synth.WORKLOADS[args.ncu_target]
+        w = Prefill(api, wl, 1234) if wl.prefill_len else Decode(api, wl, 99)
+        for _ in range(args.calls):
+            w.step(st)
+        st.synchronize()
+        print(json.dumps({"ncu_target": args.ncu_target, "calls": args.calls,
+                          "device_status": int(w.status.item())}))
+        return
     args.warmup = max(args.warmup, 3)
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -392,7 +438,7 @@ def main():
     gemm_tflops = work.gemm_flops / (gemm_ms_step * 1e-3) / 1e12 if gemm_ms_step > 0 else 0.0
     roof = {"bound": "tensor", "kernel": "gemm_tc", "achieved": gemm_tflops,
             "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-            "frac": gemm_tflops / peaks["bf16_tflops"], "traffic": None,
+            "frac": gemm_tflops / peaks["bf16_tflops"], "traffic": ncu_traffic("prefill_gemm"),
             "peak_kind": f"{peaks['source']} burst cuBLAS bf16"}
 
     # end to end through the public API with host buffers: H2D inputs, layer, D2H output
@@ -465,7 +511,7 @@ def main():
                              "achieved": dom_bytes / (dom_ms * 1e-3) / 1e9 if dom_ms else 0.0,
                              "peak": peaks["hbm_gbs"], "unit": "GB/s",
                              "frac": (dom_bytes / (dom_ms * 1e-3) / 1e9) / peaks["hbm_gbs"] if dom_ms else 0.0,
-                             "traffic": None},
+                             "traffic": ncu_traffic(f"{name}_{'attn' if dom == 'attn_decode' else 'gemm'}")},
                 "kernels": {k: {"launches_per_step": v["launches"] // n2, "ms_per_step": v["ms"] / n2,
                                 "share": v["share"]} for k, v in per2.items() if isinstance(v, dict)},
                 "gemm_ms_qkv_o_gu_down": per2.get("gemm_by_position_ms"),
