@@ -214,7 +214,7 @@ int run_layer(const ll_config* cfg, const void* packed, const void* x, const int
         at.scale = scale;
         at.out = o;
         at.status = status;
-        if ((e = ll::launch_attn_prefill(at, stream)) != cudaSuccess) return LL_ERR_CUDA;
+        if ((e = ll::launch_attn_prefill_tc(at, stream)) != cudaSuccess) return LL_ERR_CUDA;
     } else {
         ll::AttnDecodeArgs at{};
         at.q = q;

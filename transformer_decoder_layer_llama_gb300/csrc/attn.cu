@@ -1,20 +1,14 @@
-// Attention over the paged KV cache: the prefill (FlashAttention) and the
-// decode (flash_attention_decode) variants of the Llama2-7B operator chain
-// (page "Which ops-transformer operators one Llama2-7B layer calls", sections
-// "single-layer operator call chain" and "KV Cache and the operators").
-//
-// Both read K/V through block_table from the pool [num_blocks, n_kv_heads,
-// block_size, head_dim] (paging page, section "KV Cache memory wall"), never
-// materialise the score matrix, and keep a running max / denominator per
-// query row (online softmax, exp2 with the scale folded into log2 e).
-// Query head h reads KV head h / (n_heads / n_kv_heads).
-//
-// Prefill: one CTA = 128 queries of one sequence and one head, 8 warps of 16
-// rows; 64-key tiles double-buffered in shared memory with cp.async (16-byte
-// vectors, XOR-swizzled rows so ldmatrix is conflict-free); QK^T and PV on
-// the tensor cores with mma.sync m16n8k16 (BF16 in, float32 accumulate).
-// The probabilities P enter the PV product as two BF16 parts (hi + lo), so P
-// keeps about 16 significant bits instead of BF16's 8; V stays exact.
+// Decode attention over the paged KV cache: the flash_attention_decode
+// variant of the Llama2-7B operator chain (page "Which ops-transformer
+// operators one Llama2-7B layer calls", section "KV Cache and the operators":
+// a one-row query per head against the cached K/V).  K/V are read through
+// block_table from the pool [num_blocks, n_kv_heads, block_size, head_dim]
+// (paging page, section "KV Cache memory wall"); the score matrix is never
+// materialised and each query row keeps a running max / denominator (online
+// softmax, exp2 with the scale folded into log2 e).  Query head h reads KV
+// head h / (n_heads / n_kv_heads).  The probabilities P enter the P V product
+// as two BF16 parts (hi + lo), so P keeps about 16 significant bits; V stays
+// exact.  (The prefill variant lives in attn_tc.cu.)
 //
 // Decode: the context of each (sequence, KV head) is cut into 1024-key
 // splits, one CTA each; a producer warp streams the split's K/V tiles from the
@@ -49,248 +43,6 @@ constexpr int kDecodeChunk = 1024;
 template <int D>
 LL_DEVINL uint32_t swz(int r, int c) {
     return (uint32_t)(r * (D * 2) + ((c ^ (r & 7)) << 4));
-}
-
-// Loads rows [0, nrows) of a KV tile covering cache positions p0..p0+63 of one
-// sequence/head.  Thread i handles row i / TPR and chunks (i % TPR) * CPT ..
-template <int D, int NTHREADS>
-LL_DEVINL void load_kv_tile(uint8_t* sk, uint8_t* sv, const __nv_bfloat16* __restrict__ kp,
-                            const __nv_bfloat16* __restrict__ vp, const int32_t* __restrict__ table_row,
-                            int p0, int p_end, int hk, int n_kv_heads, int block_size, int num_blocks,
-                            int32_t* status) {
-    constexpr int CPR = D / 8;                  // 16-byte chunks per row
-    constexpr int TPR = NTHREADS / 64;          // threads per row
-    constexpr int CPT = CPR / TPR;              // chunks per thread
-    const int row = threadIdx.x / TPR;
-    const int c0 = (threadIdx.x % TPR) * CPT;
-    const int p = p0 + row;
-    bool valid = p < p_end;
-    size_t off = 0;
-    if (valid) {
-        const int blk = table_row[p / block_size];
-        if (blk < 0 || blk >= num_blocks) {
-            valid = false;
-            flag_status(status, LL_DEV_BAD_BLOCK);
-        } else {
-            off = (((size_t)blk * n_kv_heads + hk) * block_size + (p % block_size)) * D;
-        }
-    }
-#pragma unroll
-    for (int j = 0; j < CPT; ++j) {
-        const int c = c0 + j;
-        cp_async16(sk + swz<D>(row, c), kp + off + c * 8, valid);
-        cp_async16(sv + swz<D>(row, c), vp + off + c * 8, valid);
-    }
-}
-
-// ---------------------------------------------------------------- prefill
-
-template <int D>
-__global__ void __launch_bounds__(256, 1)
-    attn_prefill_kernel(const AttnPrefillArgs a) {
-    constexpr int BMQ = 128, BN = 64, NT = 256;
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t* sq = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
-    uint8_t* sk = sq + BMQ * D * 2;                  // [2][BN][D]
-    uint8_t* sv = sk + 2 * BN * D * 2;               // [2][BN][D]
-    __shared__ int max_pos_s;
-    __shared__ int warp_max_pos[8];
-
-    const int b = blockIdx.z;
-    const int h = blockIdx.y;
-    // heavy (late) query tiles first
-    const int mt = gridDim.x - 1 - blockIdx.x;
-    const int G = a.n_heads / a.n_kv_heads;
-    const int hk = h / G;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int row0 = mt * BMQ;
-    const size_t tok0 = (size_t)b * a.seq_len;
-    const int32_t* table_row = a.block_table + (size_t)b * a.max_blocks;
-
-    if (threadIdx.x == 0) max_pos_s = -1;
-    __syncthreads();
-    // positions of this tile's rows
-    int my_pos = -1;
-    if (threadIdx.x < BMQ && row0 + (int)threadIdx.x < a.seq_len)
-        my_pos = a.positions[tok0 + row0 + threadIdx.x];
-    if (my_pos >= a.max_blocks * a.block_size) {
-        flag_status(a.status, LL_DEV_BAD_POSITION);
-        my_pos = -1;
-    }
-    if (threadIdx.x < BMQ) atomicMax(&max_pos_s, my_pos);
-    {
-        // rows 32p .. 32p+15 (lanes 0-15 of warp p) belong to MMA warp 2p, the next 16 to 2p+1
-        int v = my_pos;
-#pragma unroll
-        for (int o = 8; o > 0; o >>= 1) v = max(v, __shfl_xor_sync(0xffffffffu, v, o));
-        if (threadIdx.x < BMQ && (lane & 15) == 0) warp_max_pos[threadIdx.x >> 4] = v;
-    }
-
-    // Q tile: 128 rows x D
-
-    {
-        constexpr int CPR = D / 8;
-        for (int i = threadIdx.x; i < BMQ * CPR; i += NT) {
-            const int r = i / CPR, c = i % CPR;
-            const bool ok = row0 + r < a.seq_len;
-            const __nv_bfloat16* src =
-                a.q + ((tok0 + row0 + (ok ? r : 0)) * a.n_heads + h) * D + c * 8;
-            cp_async16(sq + swz<D>(r, c), src, ok);
-        }
-        cp_async_commit();
-    }
-    __syncthreads();
-    const int max_pos = max_pos_s;
-    const int n_kt = (max_pos + BN) / BN;   // key tiles covering positions 0..max_pos
-    const int wmax = warp_max_pos[warp];
-
-    if (n_kt > 0)
-        load_kv_tile<D, NT>(sk, sv, a.k_pool, a.v_pool, table_row, 0, max_pos + 1, hk, a.n_kv_heads,
-                            a.block_size, a.num_blocks, a.status);
-    cp_async_commit();
-
-    const float sl2 = a.scale * kLog2e;
-    const int g = lane >> 2, cq = lane & 3;
-    const int qr0 = warp * 16 + g, qr1 = qr0 + 8;
-    const int pos_cap = a.max_blocks * a.block_size;
-    int qpos0 = -1, qpos1 = -1;
-    if (row0 + qr0 < a.seq_len) qpos0 = a.positions[tok0 + row0 + qr0];
-    if (row0 + qr1 < a.seq_len) qpos1 = a.positions[tok0 + row0 + qr1];
-    if (qpos0 >= pos_cap) qpos0 = -1;
-    if (qpos1 >= pos_cap) qpos1 = -1;
-
-    float acc[D / 8][4];
-#pragma unroll
-    for (int i = 0; i < D / 8; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
-    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
-    uint32_t qf[D / 16][4];
-
-    cp_async_wait<1>();   // Q landed
-    __syncthreads();
-    {
-        const uint32_t qb = smem_u32(sq);
-#pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) {
-            const int r = warp * 16 + (lane & 15);
-            const int c = ks * 2 + (lane >> 4);
-            ldmatrix_x4(qf[ks], qb + swz<D>(r, c));
-        }
-    }
-
-    for (int kt = 0; kt < n_kt; ++kt) {
-        const int buf = kt & 1;
-        if (kt + 1 < n_kt)
-            load_kv_tile<D, NT>(sk + (buf ^ 1) * BN * D * 2, sv + (buf ^ 1) * BN * D * 2, a.k_pool,
-                                a.v_pool, table_row, (kt + 1) * BN, max_pos + 1, hk, a.n_kv_heads,
-                                a.block_size, a.num_blocks, a.status);
-        cp_async_commit();
-        cp_async_wait<1>();
-        __syncthreads();
-        if (kt * BN <= wmax) {
-            const uint32_t kb = smem_u32(sk + buf * BN * D * 2);
-            const uint32_t vb = smem_u32(sv + buf * BN * D * 2);
-            float s[BN / 8][4];
-#pragma unroll
-            for (int i = 0; i < BN / 8; ++i) s[i][0] = s[i][1] = s[i][2] = s[i][3] = 0.f;
-#pragma unroll
-            for (int ks = 0; ks < D / 16; ++ks) {
-#pragma unroll
-                for (int np = 0; np < BN / 16; ++np) {
-                    uint32_t bfr[4];
-                    const int r = np * 16 + (lane & 7) + ((lane >> 4) << 3);
-                    const int c = ks * 2 + ((lane >> 3) & 1);
-                    ldmatrix_x4(bfr, kb + swz<D>(r, c));
-                    mma_bf16_16816(s[2 * np], qf[ks], bfr[0], bfr[1]);
-                    mma_bf16_16816(s[2 * np + 1], qf[ks], bfr[2], bfr[3]);
-                }
-            }
-            // scale, causal mask, online softmax (rows qr0 -> s[.][0..1], qr1 -> s[.][2..3])
-            float mx0 = -INFINITY, mx1 = -INFINITY;
-#pragma unroll
-            for (int nt = 0; nt < BN / 8; ++nt) {
-                const int kp = kt * BN + nt * 8 + 2 * cq;
-                s[nt][0] = (kp <= qpos0) ? s[nt][0] * sl2 : -INFINITY;
-                s[nt][1] = (kp + 1 <= qpos0) ? s[nt][1] * sl2 : -INFINITY;
-                s[nt][2] = (kp <= qpos1) ? s[nt][2] * sl2 : -INFINITY;
-                s[nt][3] = (kp + 1 <= qpos1) ? s[nt][3] * sl2 : -INFINITY;
-                mx0 = fmaxf(mx0, fmaxf(s[nt][0], s[nt][1]));
-                mx1 = fmaxf(mx1, fmaxf(s[nt][2], s[nt][3]));
-            }
-#pragma unroll
-            for (int o = 1; o <= 2; o <<= 1) {
-                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
-                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
-            }
-            const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-            const float base0 = (mn0 == -INFINITY) ? 0.f : mn0;
-            const float base1 = (mn1 == -INFINITY) ? 0.f : mn1;
-            const float al0 = exp2f(m0 - base0), al1 = exp2f(m1 - base1);
-            m0 = mn0;
-            m1 = mn1;
-            float rs0 = 0.f, rs1 = 0.f;
-#pragma unroll
-            for (int nt = 0; nt < BN / 8; ++nt) {
-                s[nt][0] = exp2f(s[nt][0] - base0);
-                s[nt][1] = exp2f(s[nt][1] - base0);
-                s[nt][2] = exp2f(s[nt][2] - base1);
-                s[nt][3] = exp2f(s[nt][3] - base1);
-                rs0 += s[nt][0] + s[nt][1];
-                rs1 += s[nt][2] + s[nt][3];
-            }
-            l0 = l0 * al0 + rs0;
-            l1 = l1 * al1 + rs1;
-#pragma unroll
-            for (int i = 0; i < D / 8; ++i) {
-                acc[i][0] *= al0;
-                acc[i][1] *= al0;
-                acc[i][2] *= al1;
-                acc[i][3] *= al1;
-            }
-            // P V with P carried as hi + lo BF16 parts (about 16 bits): two MMAs per V fragment
-#pragma unroll
-            for (int kk = 0; kk < BN / 16; ++kk) {
-                uint32_t ph[4], pl[4];
-                split_bf16x2(s[2 * kk][0], s[2 * kk][1], ph[0], pl[0]);
-                split_bf16x2(s[2 * kk][2], s[2 * kk][3], ph[1], pl[1]);
-                split_bf16x2(s[2 * kk + 1][0], s[2 * kk + 1][1], ph[2], pl[2]);
-                split_bf16x2(s[2 * kk + 1][2], s[2 * kk + 1][3], ph[3], pl[3]);
-#pragma unroll
-                for (int dp = 0; dp < D / 16; ++dp) {
-                    uint32_t bfr[4];
-                    const int r = kk * 16 + (lane & 7) + (((lane >> 3) & 1) << 3);
-                    const int c = dp * 2 + (lane >> 4);
-                    ldmatrix_x4_trans(bfr, vb + swz<D>(r, c));
-                    mma_bf16_16816(acc[2 * dp], ph, bfr[0], bfr[1]);
-                    mma_bf16_16816(acc[2 * dp + 1], ph, bfr[2], bfr[3]);
-                    mma_bf16_16816(acc[2 * dp], pl, bfr[0], bfr[1]);
-                    mma_bf16_16816(acc[2 * dp + 1], pl, bfr[2], bfr[3]);
-                }
-            }
-        }
-        __syncthreads();
-    }
-    cp_async_wait<0>();
-
-    // row sums across the quad
-#pragma unroll
-    for (int o = 1; o <= 2; o <<= 1) {
-        l0 += __shfl_xor_sync(0xffffffffu, l0, o);
-        l1 += __shfl_xor_sync(0xffffffffu, l1, o);
-    }
-    const float inv0 = l0 > 0.f ? 1.f / l0 : 0.f;
-    const float inv1 = l1 > 0.f ? 1.f / l1 : 0.f;
-    if (row0 + qr0 < a.seq_len) {
-        __nv_bfloat16* o = a.out + ((tok0 + row0 + qr0) * a.n_heads + h) * D;
-#pragma unroll
-        for (int i = 0; i < D / 8; ++i)
-            *reinterpret_cast<uint32_t*>(o + i * 8 + 2 * cq) = pack_bf16x2(acc[i][0] * inv0, acc[i][1] * inv0);
-    }
-    if (row0 + qr1 < a.seq_len) {
-        __nv_bfloat16* o = a.out + ((tok0 + row0 + qr1) * a.n_heads + h) * D;
-#pragma unroll
-        for (int i = 0; i < D / 8; ++i)
-            *reinterpret_cast<uint32_t*>(o + i * 8 + 2 * cq) = pack_bf16x2(acc[i][2] * inv1, acc[i][3] * inv1);
-    }
 }
 
 // ---------------------------------------------------------------- decode
@@ -601,23 +353,6 @@ __global__ void attn_decode_combine_kernel(const AttnDecodeArgs a, int max_split
 }
 
 template <int D>
-cudaError_t prefill_for(const AttnPrefillArgs& a, cudaStream_t stream) {
-    const size_t smem = (size_t)(128 * D * 2) + 4 * (64 * D * 2) + 128;
-    static bool configured = false;
-    if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(attn_prefill_kernel<D>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return record(e, "cudaFuncSetAttribute(attn_prefill_kernel)");
-        configured = true;
-    }
-    dim3 grid((a.seq_len + 127) / 128, a.n_heads, a.batch);
-    trace_before("attn_prefill", stream);
-    attn_prefill_kernel<D><<<grid, 256, smem, stream>>>(a);
-    trace_after(stream);
-    return record(cudaGetLastError(), "attn_prefill_kernel launch");
-}
-
-template <int D>
 cudaError_t decode_for(const AttnDecodeArgs& a, cudaStream_t stream) {
     const int max_splits = attn_decode_max_splits(a.max_blocks, a.block_size);
     const size_t smem = (size_t)2 * 3 * (64 * D * 2) + 16 * D * 2 + 1024;
@@ -657,13 +392,6 @@ size_t attn_decode_scratch_bytes(int batch, int n_heads, int head_dim, int max_b
                                  int block_size) {
     const size_t rows = (size_t)batch * n_heads * attn_decode_max_splits(max_blocks, block_size);
     return rows * head_dim * sizeof(float) + rows * 2 * sizeof(float);
-}
-
-cudaError_t launch_attn_prefill(const AttnPrefillArgs& a, cudaStream_t stream) {
-    if (a.batch <= 0 || a.seq_len <= 0) return cudaSuccess;
-    if (a.head_dim == 128) return prefill_for<128>(a, stream);
-    if (a.head_dim == 64) return prefill_for<64>(a, stream);
-    return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_attn_decode(const AttnDecodeArgs& a, cudaStream_t stream) {

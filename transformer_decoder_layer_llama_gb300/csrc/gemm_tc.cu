@@ -62,8 +62,6 @@ struct GemmArgs {
     uint32_t tmem_cols;
 };
 
-LL_DEVINL void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
-
 LL_DEVINL float silu_f(float z) { return z / (1.0f + expf(-z)); }
 
 struct TokenSlot {

@@ -104,7 +104,7 @@ struct AttnPrefillArgs {
     __nv_bfloat16* out;            // [tokens, n_heads, d]
     int32_t* status;
 };
-cudaError_t launch_attn_prefill(const AttnPrefillArgs& a, cudaStream_t stream);
+cudaError_t launch_attn_prefill_tc(const AttnPrefillArgs& a, cudaStream_t stream);
 
 struct AttnDecodeArgs {
     const __nv_bfloat16* q;        // [batch, n_heads, d]

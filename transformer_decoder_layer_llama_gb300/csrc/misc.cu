@@ -20,7 +20,6 @@ template <typename In>
 struct RowIO;
 template <>
 struct RowIO<__nv_bfloat16> {
-    static constexpr int kVec = 8;   // elements per 16-byte load
     LL_DEVINL static void load(const __nv_bfloat16* row, int i, float (&f)[8]) {
         uint4 u = reinterpret_cast<const uint4*>(row)[i];
         uint32_t w[4] = {u.x, u.y, u.z, u.w};
@@ -33,7 +32,6 @@ struct RowIO<__nv_bfloat16> {
 };
 template <>
 struct RowIO<float> {
-    static constexpr int kVec = 8;
     LL_DEVINL static void load(const float* row, int i, float (&f)[8]) {
         float4 a = reinterpret_cast<const float4*>(row)[2 * i];
         float4 b = reinterpret_cast<const float4*>(row)[2 * i + 1];
