@@ -299,35 +299,42 @@ def traced_breakdown(api, work, steps, stream, flush):
 
 # ---------------------------------------------------------------- oracle (CPU) throughput
 
-def oracle_prefill_sample(wl, budget_s, chunk, seed=7, max_steps=None):
-    """Times the CPU oracle on chunks of `chunk` tokens of the 7B prefill workload, centred on
-    position S/2 (so the attention share matches the whole sequence's average), over a
-    pre-filled cache prefix; repeats until budget_s has passed.  Returns (TFLOP/s, steps,
-    description)."""
-    from oracle import llama_layer as O
-    d = wl.dims
-    S = wl.prefill_len
-    W = synth.make_weights(d, wl.w_std, seed)
-    Wn = {k: v.float().numpy().astype(np.float64) for k, v in W.items()}
-    start = S // 2 - chunk // 2
-    table, nb = synth.make_block_table([S], d.block_size, seed + 1)
-    kp, vp = synth.make_pool(nb, d, seed + 2)
-    kpo = kp.view(torch.int16).numpy().view(np.uint16)
-    vpo = vp.view(torch.int16).numpy().view(np.uint16)
-    x = synth.make_x(chunk, d.hidden, seed + 3).float().numpy().astype(np.float64)
-    pos = np.arange(start, start + chunk)
-    flops = gemm_flops(d, chunk) + attn_flops(d, pos + 1)
-    t_total, n = 0.0, 0
-    while True:
-        t0 = time.perf_counter()
-        O.layer_prefill(d, Wn, x, pos, 1, chunk, kpo, vpo, table.numpy())
-        t_total += time.perf_counter() - t0
-        n += 1
-        if (max_steps is not None and n >= max_steps) or (max_steps is None and t_total >= budget_s):
-            break
-    desc = (f"oracle (numpy float64) on {n} x {chunk}-token chunks of the 2048-token 7B prefill "
-            f"at positions {start}..{start + chunk - 1} over a pre-filled cache prefix")
-    return flops * n / t_total / 1e12, n, desc
+class OracleSample:
+    """The CPU oracle on chunks of the 2048-token 7B prefill workload.  A chunk of `chunk`
+    tokens sits at positions centred on S/2 (so the attention share matches the whole
+    sequence's average) over a pre-filled cache prefix.  Weights are drawn once."""
+
+    def __init__(self, wl, seed=7):
+        d = wl.dims
+        self.d, self.S = d, wl.prefill_len
+        W = synth.make_weights(d, wl.w_std, seed)
+        self.W = {k: v.float().numpy().astype(np.float64) for k, v in W.items()}
+        self.table, nb = synth.make_block_table([self.S], d.block_size, seed + 1)
+        kp, vp = synth.make_pool(nb, d, seed + 2)
+        self.kp = kp.view(torch.int16).numpy().view(np.uint16)
+        self.vp = vp.view(torch.int16).numpy().view(np.uint16)
+        self.seed = seed
+
+    def run(self, chunk, budget_s=0.0, max_steps=None):
+        """Times steps of `chunk` tokens until budget_s has passed (or max_steps steps).
+        Returns (TFLOP/s, steps, description)."""
+        from oracle import llama_layer as O
+        d = self.d
+        start = self.S // 2 - chunk // 2
+        x = synth.make_x(chunk, d.hidden, self.seed + 3).float().numpy().astype(np.float64)
+        pos = np.arange(start, start + chunk)
+        flops = gemm_flops(d, chunk) + attn_flops(d, pos + 1)
+        t_total, n = 0.0, 0
+        while True:
+            t0 = time.perf_counter()
+            O.layer_prefill(d, self.W, x, pos, 1, chunk, self.kp, self.vp, self.table.numpy())
+            t_total += time.perf_counter() - t0
+            n += 1
+            if (max_steps is not None and n >= max_steps) or (max_steps is None and t_total >= budget_s):
+                break
+        desc = (f"oracle (numpy float64) on {n} x {chunk}-token chunks of the 2048-token 7B prefill "
+                f"at positions {start}..{start + chunk - 1} over a pre-filled cache prefix")
+        return flops * n / t_total / 1e12, n, desc
 
 
 def host_cores():
@@ -379,15 +386,16 @@ def main():
         if rank != 0:
             return
         # bounded oracle sample per step: size the chunk so K + W steps end in ~3 minutes
-        probe, _, _ = oracle_prefill_sample(wl, 0.0, 16, max_steps=1)
+        sampler = OracleSample(wl)
+        probe, _, _ = sampler.run(16, max_steps=1)
         per_tok_s = gemm_flops(wl.dims, 1) / (probe * 1e12)
         chunk = int(max(4, min(256, 150.0 / max(args.steps + args.warmup, 1) / max(per_tok_s, 1e-6))))
-        oracle_prefill_sample(wl, 0.0, chunk, max_steps=args.warmup)
+        sampler.run(chunk, max_steps=args.warmup)
         t0 = time.perf_counter()
-        v, n, desc = oracle_prefill_sample(wl, 0.0, chunk, max_steps=args.steps)
+        v, n, desc = sampler.run(chunk, max_steps=args.steps)
         wall = time.perf_counter() - t0
         line = {"metric": METRIC, "impl": "reference", "value": v, "unit": "TFLOP/s",
-                "n_gpus": 0, "steps": args.steps, "warmup": args.warmup,
+                "n_gpus": max(world, args.gpus), "steps": args.steps, "warmup": args.warmup,
                 "ms_per_step": wall / max(n, 1) * 1e3, "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
                 "config": cfg_json,
@@ -523,7 +531,7 @@ def main():
         line["decode"] = extras
 
     if rank == 0 and world == 1 and not args.no_cpu:
-        v, n, desc = oracle_prefill_sample(wl, 12.0, 64)
+        v, n, desc = OracleSample(wl).run(64, budget_s=12.0)
         line["cpu_baseline"] = {"value": v, "unit": "TFLOP/s", "cores": host_cores(),
                                 "kind": "oracle", "sample": desc}
     if rank == 0:
