@@ -256,6 +256,114 @@ class Decode:
         return max(self.flops / (peaks["bf16_tflops"] * 1e12), self.min_bytes / (peaks["hbm_gbs"] * 1e9))
 
 
+def continuous_batching(api, wl, steps, warmup, stream, peaks, seed=4321):
+    """The 32-layer stack under continuous batching: 64 slots with resident contexts
+    ~U[ctx_lo, ctx_hi] (pre-filled cache), per-request decode budgets ~U[1, 256]; a finished
+    request's blocks go back to the free list and a new request is admitted with a 256-token
+    prefill.  Each step: retire/admit (+ batched prefill of the admitted, all layers), grow
+    the block tables, one decode step for all slots through all layers (a CUDA graph).
+    Timed over `steps` steps with CUDA events around the whole loop (host scheduling
+    included)."""
+    from transformer_decoder_layer_llama_gb300.serving import BlockAllocator, Scheduler, StackEngine
+    d = wl.dims
+    L, n_slots, prompt = wl.layers, wl.batch, wl.new_prefill
+    ctx0 = synth.make_context_lens(n_slots, wl.ctx_lo, wl.ctx_hi, seed).tolist()
+    max_ctx = max(max(ctx0), prompt) + steps + warmup + 1
+    max_blocks = -(-max_ctx // d.block_size) + 1
+    nb = sum(-(-(max(c, prompt) + steps + warmup + 1) // d.block_size) + 1 for c in ctx0) + 2 * n_slots
+    cfgs, packed, pools = [], [], []
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(seed)
+    for l in range(L):
+        cfg, pk, _ = device_layer(api, d, wl.w_std, max_blocks * d.block_size, seed + 17 * l)
+        cfgs.append(cfg)
+        packed.append(pk)
+        shape = (nb, d.n_kv_heads, d.block_size, d.head_dim)
+        pools.append((dev_normal(shape, 1.0, gen), dev_normal(shape, 1.0, gen)))
+    alloc = BlockAllocator(nb, seed)
+    sch = Scheduler(n_slots, d.block_size, max_blocks, alloc, seed + 1, budget_max=256, prompt_len=prompt)
+    for sl, c in enumerate(ctx0):
+        sch.start_resident(sl, c)
+    eng = StackEngine(api, cfgs, packed, pools, n_slots, max_blocks, n_slots * prompt)
+    n_total = steps + warmup
+    x_steps = dev_normal((n_total, n_slots, d.hidden), 1.0, gen)
+    x_prompt = dev_normal((n_slots * prompt, d.hidden), 1.0, gen)
+    pos_prompt = synth.prefill_positions(n_slots, prompt).cuda()
+    eng.pf_pos.copy_(pos_prompt)
+    pinned = [(torch.empty(n_slots, max_blocks, dtype=torch.int32).pin_memory(),
+               torch.empty(n_slots, dtype=torch.int32).pin_memory(),
+               torch.empty(n_slots, max_blocks, dtype=torch.int32).pin_memory()) for _ in range(2)]
+    copied = [None, None]
+    stats = {"decode_tokens": 0, "prefill_tokens": 0, "admitted": 0, "kv_tokens_read": 0,
+             "prefill_flops": 0.0}
+
+    def one_step(i, record):
+        k = i & 1
+        if copied[k] is not None:
+            copied[k].synchronize()           # pinned buffer k free again
+        tab_h, ctx_h, sub_h = pinned[k]
+        admitted = sch.retire_and_admit()
+        with torch.cuda.stream(stream):
+            if admitted:
+                n = len(admitted)
+                sub_h[:n].copy_(torch.from_numpy(sch.table[admitted]))
+                eng.pf_table[:n].copy_(sub_h[:n], non_blocking=True)
+                eng.pf_x[:n * prompt].copy_(x_prompt[:n * prompt], non_blocking=True)
+                eng.prefill(n, prompt, stream)
+            ctx = sch.grow_for_decode()
+            tab_h.copy_(torch.from_numpy(sch.table))
+            ctx_h.copy_(torch.from_numpy(ctx))
+            eng.table.copy_(tab_h, non_blocking=True)
+            eng.ctx.copy_(ctx_h, non_blocking=True)
+            eng.x.copy_(x_steps[i], non_blocking=True)
+            ev = torch.cuda.Event()
+            ev.record(stream)
+            copied[k] = ev
+            eng.decode(stream)
+        if record:
+            stats["decode_tokens"] += n_slots
+            stats["prefill_tokens"] += len(admitted) * prompt
+            stats["admitted"] += len(admitted)
+            stats["kv_tokens_read"] += int(ctx.sum())
+            if admitted:
+                stats["prefill_flops"] += L * (gemm_flops(d, len(admitted) * prompt)
+                                               + attn_flops(d, np.tile(np.arange(1, prompt + 1), len(admitted))))
+
+    one_step(0, False)
+    stream.synchronize()
+    eng.capture_decode(stream)                 # replays the decode of every later step
+    for i in range(1, warmup):
+        one_step(i, False)
+    stream.synchronize()
+    t_ev = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+    t0 = time.perf_counter()
+    t_ev[0].record(stream)
+    for i in range(warmup, n_total):
+        one_step(i, True)
+    t_ev[1].record(stream)
+    stream.synchronize()
+    wall = time.perf_counter() - t0
+    ms = t_ev[0].elapsed_time(t_ev[1])
+    status = int(eng.status.item())
+    # minimum bytes of the decode steps: every layer's weights + the KV each step reads
+    decode_bytes = steps * L * weight_bytes(d) + L * kv_bytes_read(d, [stats["kv_tokens_read"]])
+    roof_s = decode_bytes / (peaks["hbm_gbs"] * 1e9) + stats["prefill_flops"] / (peaks["bf16_tflops"] * 1e12)
+    out = {
+        "layers": L, "slots": n_slots, "steps": steps, "ms_total": ms, "wall_s": wall,
+        "decode_tok_per_s": stats["decode_tokens"] / (ms * 1e-3),
+        "total_tok_per_s": (stats["decode_tokens"] + stats["prefill_tokens"]) / (ms * 1e-3),
+        "admitted_requests": stats["admitted"],
+        "hbm_gbs_decode_min_bytes": decode_bytes / (ms * 1e-3) / 1e9,
+        "roofline_frac": roof_s / (ms * 1e-3),
+        "kv_pool_gb": 2 * L * nb * d.n_kv_heads * d.block_size * d.head_dim * 2 / 1e9,
+        "device_status": status,
+        "cuda_graph_decode": True,
+    }
+    del eng, pools, packed
+    torch.cuda.empty_cache()
+    return out
+
+
 def timed_steps(work, steps, stream, flush):
     """Device time of `steps` steps, each bracketed by its own events, L2 flushed between."""
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
@@ -354,6 +462,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-extras", action="store_true", help="skip the decode workloads")
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle CPU baseline")
+    ap.add_argument("--no-stack", action="store_true", help="skip the 32-layer continuous batching")
     ap.add_argument("--ncu-target", choices=["llama2_7b_prefill", "llama2_7b_decode",
                                              "llama70b_gqa_decode"],
                     help="set up one workload, run --calls untimed layer calls and exit (for ncu)")
@@ -529,6 +638,10 @@ def main():
             del dw
             torch.cuda.empty_cache()
         line["decode"] = extras
+        if not args.no_stack:
+            line["continuous_batching"] = continuous_batching(
+                api, synth.WORKLOADS["llama2_7b_stack_cb"], synth.WORKLOADS["llama2_7b_stack_cb"].steps,
+                3, stream, peaks)
 
     if rank == 0 and world == 1 and not args.no_cpu:
         v, n, desc = OracleSample(wl).run(64, budget_s=12.0)
