@@ -75,6 +75,8 @@ def test_scheduler_matches_independent_replay_and_invariants():
 
 @pytest.mark.gpu
 def test_tiny_stack_continuous_batching_matches_oracle():
+    """Steps 0-1 decode eagerly, steps 2-5 replay a captured CUDA graph; requests retire
+    (budgets <= 3) and new ones are prefilled on the way."""
     from transformer_decoder_layer_llama_gb300 import api
     from transformer_decoder_layer_llama_gb300.serving import StackEngine
     d = synth.DIMS_TINY
@@ -94,7 +96,8 @@ def test_tiny_stack_continuous_batching_matches_oracle():
     for s, c in enumerate(ctx0):
         sch.start_resident(s, c)
     eng = StackEngine(api, [cfg] * L, packed, pools, n_slots, max_blocks, n_slots * prompt)
-    stream = torch.cuda.current_stream()
+    stream = torch.cuda.Stream()            # graph capture needs a non-default stream
+    torch.cuda.set_stream(stream)
     for step in range(steps):
         admitted = sch.retire_and_admit()
         if admitted:
@@ -116,6 +119,8 @@ def test_tiny_stack_continuous_batching_matches_oracle():
         eng.table.copy_(torch.from_numpy(sch.table))
         eng.ctx.copy_(torch.from_numpy(ctx))
         eng.x.copy_(xd)
+        if step == 2:
+            eng.capture_decode(stream)   # later steps replay the all-layer decode as a CUDA graph
         yd = eng.decode(stream)
         xo = f64(xd)
         for l in range(L):
@@ -124,3 +129,4 @@ def test_tiny_stack_continuous_batching_matches_oracle():
         torch.cuda.synchronize()
         assert int(eng.status.item()) == 0
         assert_close(f64(yd), xo, f"step {step} decode")
+    torch.cuda.set_stream(torch.cuda.default_stream())
