@@ -39,6 +39,7 @@ namespace {
 constexpr int kTcThreads = 320;   // TMA warp, MMA warp, 8 softmax warps
 constexpr int kKT = 128;          // keys per tile
 constexpr int kQT = 128;          // queries per CTA
+constexpr int kMaxKeyTiles = 512; // key positions up to 65535 per call
 constexpr float kLog2eTc = 1.4426950408889634f;
 
 template <int D>
@@ -103,6 +104,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     __shared__ int max_pos_s;
     __shared__ float red_max[2][2][kQT];      // [tile parity][key half][row]
     __shared__ float red_sum[2][kQT];         // [key half][row], at the end
+    __shared__ uint32_t tile_ok_s[kMaxKeyTiles];   // per key tile: bit c = 16-key chunk c has a valid block
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int b = blockIdx.z, h = blockIdx.y;
@@ -146,12 +148,23 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         atomicMax(&max_pos_s, p);
     }
+    for (int i = threadIdx.x; i < kMaxKeyTiles; i += blockDim.x) tile_ok_s[i] = 0;
+    __syncthreads();
+    {
+        // which 16-key chunks of the tile's key range are backed by a valid block (bs >= 16)
+        const int mp = max_pos_s;
+        if (threadIdx.x == 0 && mp >= kMaxKeyTiles * kKT) flag_status(status, LL_DEV_BAD_POSITION);
+        for (int i = threadIdx.x; i <= mp / 16 && i < kMaxKeyTiles * (kKT / 16); i += blockDim.x) {
+            const int blk = table_row[(i * 16) / a.block_size];
+            if (blk >= 0 && blk < a.num_blocks) atomicOr(&tile_ok_s[i / (kKT / 16)], 1u << (i % (kKT / 16)));
+        }
+    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = tmem_base_s;
     const int max_pos = max_pos_s;
-    const int n_kt = max_pos < 0 ? 0 : (max_pos + kKT) / kKT;
+    const int n_kt = max_pos < 0 ? 0 : min((max_pos + kKT) / kKT, kMaxKeyTiles);
 
     if (warp == 0) {
         if (lane == 0 && n_kt > 0) {
@@ -291,33 +304,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             tc_fence_after();
             const uint32_t tbuf = tmem + lane_base + (st ? L::TMEM_S1 : L::TMEM_S0);
             const int kbase = j * kKT + half * HK;    // first key of this thread's half
-            // 16-key chunks of this half backed by a valid block (block_size >= 16)
-            uint32_t chunk_ok = 0;
-#pragma unroll
-            for (int c = 0; c < HK / 16; ++c) {
-                const int p = kbase + c * 16;
-                if (p <= max_pos) {
-                    const int blk = table_row[p / a.block_size];
-                    if (blk >= 0 && blk < a.num_blocks) chunk_ok |= 1u << c;
-                }
-            }
+            const uint32_t tile_ok = tile_ok_s[j];
+            const uint32_t chunk_ok = (tile_ok >> (half * (HK / 16))) & ((1u << (HK / 16)) - 1u);
             // V rows of this tile that hold no key (past the tile's last position, or in an
             // invalid block) may be stale or uninitialised: zero them so 0 * V stays 0.  Thread
             // (row r, half) owns V row r's half of the head dims.
             {
                 const int jb = j * kKT;
-                bool need = jb + kKT - 1 > max_pos;
-                for (int c = 0; c < kKT / 16 && !need; ++c) {
-                    const int blk = table_row[(jb + c * 16) / a.block_size];
-                    need = blk < 0 || blk >= a.num_blocks;
-                }
+                const bool need = jb + kKT - 1 > max_pos || tile_ok != (1u << (kKT / 16)) - 1u;
                 if (need && mbar_wait_bounded(&v_full[st], ph, &abort_s, status)) {
                     const int kr = jb + r;
-                    bool row_ok = kr <= max_pos;
-                    if (row_ok) {
-                        const int blk = table_row[kr / a.block_size];
-                        row_ok = blk >= 0 && blk < a.num_blocks;
-                    }
+                    const bool row_ok = kr <= max_pos && ((tile_ok >> (r >> 4)) & 1u);
                     if (!row_ok) {
                         uint8_t* vrow = smem + L::OFF_V + st * L::KV_BYTES;
 #pragma unroll
@@ -327,7 +324,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     }
                 }
             }
-            // one pass over the half row of S: scaled, masked scores in registers
+            // one pass over the half row of S: raw scores in registers, masked (-inf) only
+            // where this half touches the diagonal or an invalid block
+            const bool full = chunk_ok == (1u << (HK / 16)) - 1u && kbase + HK - 1 <= my_pos;
             float sv[HK];
 #pragma unroll
             for (int c = 0; c < HK; c += 16) {
@@ -338,10 +337,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
                     for (int i = 0; i < 16; ++i) v[i] = 0.f;
                 }
-                const bool cok = (chunk_ok >> (c >> 4)) & 1u;
+                if (full) {
 #pragma unroll
-                for (int i = 0; i < 16; ++i)
-                    sv[c + i] = (cok && kbase + c + i <= my_pos) ? v[i] * sl2 : -INFINITY;
+                    for (int i = 0; i < 16; ++i) sv[c + i] = v[i];
+                } else {
+                    const bool cok = (chunk_ok >> (c >> 4)) & 1u;
+#pragma unroll
+                    for (int i = 0; i < 16; ++i)
+                        sv[c + i] = (cok && kbase + c + i <= my_pos) ? v[i] : -INFINITY;
+                }
             }
             float mx = -INFINITY;
 #pragma unroll
@@ -349,7 +353,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             red_max[j & 1][half][r] = mx;
             asm volatile("bar.sync 2, 256;" ::: "memory");   // both halves have read S_j
             if (abort_s) { ok = false; break; }
-            mx = fmaxf(mx, red_max[j & 1][half ^ 1][r]);
+            mx = fmaxf(mx, red_max[j & 1][half ^ 1][r]) * sl2;  // scale > 0: max commutes
             const float m_new = fmaxf(m_used, mx);
             const bool move = m_new > m_used + kRescaleLog2;  // false while the row has no key
             if (__any_sync(0xffffffffu, move)) {
@@ -384,8 +388,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 uint32_t hi[16], lo[16];
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
-                    const float p0 = exp2f(sv[c + 2 * i] - base);
-                    const float p1 = exp2f(sv[c + 2 * i + 1] - base);
+                    const float p0 = ex2_approx(fmaf(sv[c + 2 * i], sl2, -base));
+                    const float p1 = ex2_approx(fmaf(sv[c + 2 * i + 1], sl2, -base));
                     rs += p0 + p1;
                     split_bf16x2(p0, p1, hi[i], lo[i]);
                 }

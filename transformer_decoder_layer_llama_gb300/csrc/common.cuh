@@ -31,6 +31,13 @@ LL_DEVINL void split_bf16x2(float a, float b, uint32_t& hi, uint32_t& lo) {
     lo = pack_bf16x2(a - bf16_lo(hi), b - bf16_hi(hi));
 }
 
+// 2^x by the SFU instruction (approximate, flush-to-zero; ex2(-inf) = +0).
+LL_DEVINL float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 LL_DEVINL void flag_status(int32_t* status, int32_t bits) {
     if (status) atomicOr(status, bits);
 }
