@@ -221,6 +221,13 @@ int32_t ll_trace_end(void);
 float ll_trace_elapsed_ms(int32_t i);
 const char* ll_trace_name(int32_t i);
 
+/* Self-test of the in-kernel failure detection (not a layer operation): one
+ * block of 64 threads waits on an mbarrier that nothing completes, with a
+ * limit of limit_us microseconds (1 .. 2,000,000).  Each wait gives up, sets
+ * LL_DEV_TIMEOUT in *status and adds 1 to *out (device int32, caller-zeroed),
+ * and the kernel finishes normally: the context stays usable. */
+int ll_selftest_bounded_wait(int32_t limit_us, int32_t* status, int32_t* out, void* stream);
+
 /* Number of streaming multiprocessors the library sizes its grids for
  * (queried once per device), or -1 without a device. */
 int ll_device_sm_count(void);

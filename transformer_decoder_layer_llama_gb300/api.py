@@ -30,7 +30,7 @@ EXPORTED = [
     "ll_layer_prefill", "ll_layer_decode_step", "ll_reshape_and_cache",
     "ll_attention_workspace_size", "ll_paged_attention_decode", "ll_linear_workspace_size",
     "ll_linear", "ll_device_sm_count", "ll_trace_begin", "ll_trace_end", "ll_trace_elapsed_ms",
-    "ll_trace_name", "ll_paged_attention_decode_noalloc",
+    "ll_trace_name", "ll_paged_attention_decode_noalloc", "ll_selftest_bounded_wait",
 ]
 
 
@@ -81,6 +81,7 @@ def _load():
         "ll_trace_end": (I32, []),
         "ll_trace_elapsed_ms": (ctypes.c_float, [I32]),
         "ll_trace_name": (ctypes.c_char_p, [I32]),
+        "ll_selftest_bounded_wait": (ctypes.c_int, [I32, P, P, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)

@@ -385,6 +385,13 @@ const char* ll_strerror(int code) {
 
 int ll_device_sm_count(void) { return ll::device_sm_count(); }
 
+int ll_selftest_bounded_wait(int32_t limit_us, int32_t* status, int32_t* out, void* stream) {
+    ll::clear_last_error();
+    if (!status || !out || limit_us <= 0 || limit_us > 2000000) return LL_ERR_INVALID_ARG;
+    return cuda_rc(ll::launch_bounded_wait_selftest(status, out, (uint64_t)limit_us * 1000ull,
+                                                    static_cast<cudaStream_t>(stream)));
+}
+
 size_t ll_packed_weights_size(const ll_config* cfg) {
     if (config_supported(cfg) != LL_OK) return 0;
     return packed_layout(cfg).total;

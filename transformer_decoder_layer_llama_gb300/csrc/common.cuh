@@ -93,14 +93,14 @@ LL_DEVINL bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 // kWaitLimitNs (or at once if *abort is already set), sets *abort and the
 // LL_DEV_TIMEOUT status bit, and returns false.
 LL_DEVINL bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, volatile int* abort,
-                                 int32_t* status) {
+                                 int32_t* status, uint64_t limit_ns = kWaitLimitNs) {
     if (mbar_try_wait(bar, parity)) return true;
     uint64_t t0 = global_timer_ns();
     for (uint32_t it = 1;; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
         if ((it & 255u) == 0) {
             if (*abort) return false;
-            if (global_timer_ns() - t0 > kWaitLimitNs) {
+            if (global_timer_ns() - t0 > limit_ns) {
                 *abort = 1;
                 flag_status(status, LL_DEV_TIMEOUT);
                 return false;

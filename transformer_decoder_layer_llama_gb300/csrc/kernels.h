@@ -132,5 +132,7 @@ cudaError_t launch_interleave_rows(const __nv_bfloat16* a, const __nv_bfloat16* 
                                    __nv_bfloat16* dst, int rows, int cols, cudaStream_t stream);
 cudaError_t launch_rope_table(float2* cs, int max_position, int head_dim, double theta,
                               cudaStream_t stream);
+cudaError_t launch_bounded_wait_selftest(int32_t* status, int32_t* out, uint64_t limit_ns,
+                                         cudaStream_t stream);
 
 }  // namespace ll

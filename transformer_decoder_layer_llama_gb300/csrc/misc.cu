@@ -157,6 +157,23 @@ __global__ void rope_table_kernel(float2* cs, int max_position, int head_dim, do
     cs[idx] = make_float2((float)c, (float)s);
 }
 
+// Failure-detection self-test: every thread of the block waits on an mbarrier
+// whose phase nothing ever completes, with a limit of limit_ns.  The bounded
+// wait must give up, set LL_DEV_TIMEOUT and let the kernel finish; out[0]
+// receives the number of threads that returned from the wait.
+__global__ void bounded_wait_selftest_kernel(int32_t* status, int32_t* out, uint64_t limit_ns) {
+    __shared__ uint64_t bar;
+    __shared__ int abort_s;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);      // one arrival needed; none will come
+        abort_s = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+    const bool done = mbar_wait_bounded(&bar, 0, &abort_s, status, limit_ns);
+    if (!done) atomicAdd(out, 1);
+}
+
 unsigned blocks_for(long long n, int threads) { return (unsigned)((n + threads - 1) / threads); }
 
 }  // namespace
@@ -217,6 +234,14 @@ cudaError_t launch_interleave_rows(const __nv_bfloat16* a, const __nv_bfloat16* 
         reinterpret_cast<const uint4*>(a), reinterpret_cast<const uint4*>(b),
         reinterpret_cast<uint4*>(dst), rows, vpr);
     return record(cudaGetLastError(), "interleave_rows launch");
+}
+
+cudaError_t launch_bounded_wait_selftest(int32_t* status, int32_t* out, uint64_t limit_ns,
+                                         cudaStream_t stream) {
+    trace_before("bounded_wait_selftest", stream);
+    bounded_wait_selftest_kernel<<<1, 64, 0, stream>>>(status, out, limit_ns);
+    trace_after(stream);
+    return record(cudaGetLastError(), "bounded_wait_selftest launch");
 }
 
 cudaError_t launch_rope_table(float2* cs, int max_position, int head_dim, double theta,
