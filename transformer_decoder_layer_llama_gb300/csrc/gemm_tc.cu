@@ -456,6 +456,174 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 1) tmem_dealloc(tmem, a.tmem_cols);
 }
 
+// ---------------------------------------------------------------- token form, CTA pairs
+// A cluster of two CTAs computes 256 x 256 output tiles with tcgen05.mma.cta_group::2:
+// CTA r stages rows [128 r, 128 r + 128) of the tile's A block and rows
+// [128 r, 128 r + 128) of its B block (256 output columns), the even CTA issues the
+// pair's MMAs, and each CTA's TMEM receives its 128 output rows.  Per k-block each
+// CTA moves 32 KB (not 48 KB) for the same MMA work, which relieves shared memory.
+// Both CTAs' TMA loads complete the even CTA's full barrier; the MMA commits
+// arrive on both CTAs' barriers (multicast); both CTAs' epilogue threads release
+// the even CTA's accumulator barrier.
+constexpr int kPairBN = 256;
+
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_token2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                       const GemmArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                               ~uintptr_t(1023));
+    __shared__ uint64_t full_bar[MAX_STAGES], empty_bar[MAX_STAGES];
+    __shared__ uint64_t tfull_bar[2], tempty_bar[2], drain_bar;
+    __shared__ uint32_t tmem_base_s;
+    __shared__ int abort_s;
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_rank();
+    const bool leader = rank == 0;
+    const int pair = blockIdx.x >> 1, num_pairs = gridDim.x >> 1;
+    int32_t* status = a.ep.status;
+    // a.tiles_m counts 256-row tiles here, a.bn = 256
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < a.stages; ++s) {
+            mbar_init(&full_bar[s], 1);
+            mbar_init(&empty_bar[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&tfull_bar[b], 1);
+            mbar_init(&tempty_bar[b], 256);
+        }
+        mbar_init(&drain_bar, 1);
+        abort_s = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tmA);
+        tma_prefetch_desc(&tmB);
+    }
+    if (warp == 1) {
+        tmem_alloc_pair(&tmem_base_s, a.tmem_cols);
+        tmem_relinquish_pair();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    cluster_sync();                              // both CTAs' barriers exist before remote use
+    const uint32_t tmem = tmem_base_s;
+    const uint32_t half_bytes = (uint32_t)BM * BK * 2;     // 16 KB: A rows or B rows of one CTA
+
+    if (warp == 0) {
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            uint32_t issued[MAX_STAGES];
+            for (int s = 0; s < MAX_STAGES; ++s) issued[s] = 0;
+            bool ok = true;
+            for (int u = pair; u < a.units && ok; u += num_pairs) {
+                const int m2 = u % a.tiles_m, nb = u / a.tiles_m;
+                for (int kb = 0; kb < a.num_kb; ++kb) {
+                    if (!mbar_wait_bounded(&empty_bar[stage], phase ^ 1, &abort_s, status)) {
+                        ok = false;
+                        break;
+                    }
+                    uint8_t* sa = smem + (size_t)stage * a.stage_bytes;
+                    uint8_t* sb = sa + half_bytes;
+                    // both CTAs' loads of this stage complete the even CTA's full barrier
+                    if (leader) mbar_arrive_expect_tx(&full_bar[stage], 2u * a.stage_bytes);
+                    const uint32_t fb = cluster_map(smem_u32(&full_bar[stage]), 0);
+                    tma_load_2d_pair(sa, &tmA, kb * BK, m2 * 256 + (int)rank * BM, fb);
+                    tma_load_2d_pair(sb, &tmB, kb * BK, nb * kPairBN + (int)rank * BM, fb);
+                    for (int s = 0; s < MAX_STAGES; ++s) issued[s] += (s == stage);
+                    if (++stage == a.stages) {
+                        stage = 0;
+                        phase ^= 1;
+                    }
+                }
+            }
+            if (abort_s && leader) {
+                volatile int never = 0;
+                for (int s = 0; s < a.stages; ++s)
+                    if (issued[s]) mbar_wait_bounded(&full_bar[s], (issued[s] - 1) & 1, &never, nullptr);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        if (lane == 0 && leader) {
+            const uint32_t idesc = umma_idesc_bf16(2 * BM, kPairBN);
+            int stage = 0;
+            uint32_t phase = 0;
+            int local = 0;
+            bool ok = true;
+            const int nbuf = (int)(a.tmem_cols / kPairBN);
+            for (int u = pair; u < a.units && ok; u += num_pairs, ++local) {
+                const int buf = local % nbuf;
+                const uint32_t accp = (uint32_t)(local / nbuf) & 1;
+                if (!mbar_wait_bounded(&tempty_bar[buf], accp ^ 1, &abort_s, status)) break;
+                tc_fence_after();
+                const uint32_t d_tmem = tmem + (uint32_t)(buf * kPairBN);
+                for (int kb = 0; kb < a.num_kb; ++kb) {
+                    if (!mbar_wait_bounded(&full_bar[stage], phase, &abort_s, status)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t sa = smem_u32(smem + (size_t)stage * a.stage_bytes);
+                    const uint64_t da = umma_desc_sw128(sa);
+                    const uint64_t db = umma_desc_sw128(sa + half_bytes);
+#pragma unroll
+                    for (int kk = 0; kk < BK / UK; ++kk)
+                        tc_mma_bf16_pair(d_tmem, da + (uint64_t)(kk * 2), db + (uint64_t)(kk * 2), idesc,
+                                         (kb > 0 || kk > 0) ? 1u : 0u);
+                    tc_commit_pair_mc(&empty_bar[stage], 0x3);
+                    if (++stage == a.stages) {
+                        stage = 0;
+                        phase ^= 1;
+                    }
+                }
+                if (ok) tc_commit_pair_mc(&tfull_bar[buf], 0x3);
+            }
+            tc_commit_pair_mc(&drain_bar, 0x1);
+            volatile int never = 0;
+            mbar_wait_bounded(&drain_bar, 0, &never, status);
+        }
+        __syncwarp();
+    } else {
+        const int q = warp & 3;
+        const int r = q * 32 + lane;             // TMEM lane = token row within this CTA's 128
+        const uint32_t lane_base = (uint32_t)(q * 32) << 16;
+        int local = 0;
+        const int nbuf = (int)(a.tmem_cols / kPairBN);
+        for (int u = pair; u < a.units; u += num_pairs, ++local) {
+            const int m2 = u % a.tiles_m, nb = u / a.tiles_m;
+            const int buf = local % nbuf;
+            const uint32_t accp = (uint32_t)(local / nbuf) & 1;
+            if (!mbar_wait_bounded(&tfull_bar[buf], accp, &abort_s, status)) break;
+            tc_fence_after();
+            const uint32_t taddr = tmem + lane_base + (uint32_t)(buf * kPairBN);
+            const int t = m2 * 256 + (int)rank * BM + r;
+            const bool row_ok = t < a.tokens;
+            TokenSlot ts{-1, -1};
+            if (a.ep.kind == EPI_QKV && row_ok) ts = token_slot(a.ep, t);
+            for (int c = 0; c < kPairBN; c += 16) {
+                const int n0 = nb * kPairBN + c;
+                if (n0 >= a.n) break;
+                float v[16];
+                tmem_ld16(taddr + (uint32_t)c, v);
+                epi_token_chunk(a.ep, t, row_ok, n0, a.n, ts, v);
+            }
+            tc_fence_before();
+            mbar_arrive_cluster(cluster_map(smem_u32(&tempty_bar[buf]), 0));
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();                              // no remote arrival or load outstanding
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc_pair(tmem, a.tmem_cols);
+}
+
 // ---------------------------------------------------------------- weight form
 // One CTA = one (128-feature tile, K split); the splits of a tile form one
 // thread-block cluster (cluster rank = split).  Each CTA accumulates its K
@@ -809,6 +977,48 @@ cudaError_t launch_gemm(const GemmProblem& pr, cudaStream_t stream) {
         ok = make_tmap(&tmA, pr.w, pr.k, pr.n, BM) && make_tmap(&tmB, pr.act, pr.k, pr.tokens, p.bn);
     }
     if (!ok) return cudaErrorInvalidValue;
+    if (!p.swap && pr.tokens > BM) {
+        // CTA pairs: 256 x 256 tiles, each CTA stages 128 rows of A and of B per stage
+        a.tiles_m = ceil_div(pr.tokens, 2 * BM);
+        a.tiles_n = ceil_div(pr.n, kPairBN);
+        a.bn = kPairBN;
+        a.units = a.tiles_m * a.tiles_n;
+        a.stage_bytes = 2u * BM * BK * 2;
+        a.stages = std::min(MAX_STAGES, (int)((227 * 1024 - 2048) / a.stage_bytes));
+        // two 256-column accumulators per CTA (the epilogue of one tile overlaps the main
+        // loop of the next); tcgen05.alloc.cta_group::2 is one allocation made jointly by
+        // the pair, at the same TMEM address in both CTAs
+        a.tmem_cols = 512;
+        CUtensorMap tA2, tB2;
+        if (!make_tmap(&tA2, pr.act, pr.k, pr.tokens, BM) || !make_tmap(&tB2, pr.w, pr.k, pr.n, BM))
+            return cudaErrorInvalidValue;
+        const size_t smem = (size_t)a.stages * a.stage_bytes + 1024;
+        static int configured_smem2 = 0;
+        if ((int)smem > configured_smem2) {
+            cudaError_t e = cudaFuncSetAttribute(gemm_token2_kernel,
+                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+            if (e != cudaSuccess) return record(e, "cudaFuncSetAttribute(gemm_token2_kernel)");
+            configured_smem2 = (int)smem;
+        }
+        const int pairs = std::min(a.units, sms / 2);
+        cudaLaunchConfig_t lc = {};
+        lc.gridDim = dim3((unsigned)(2 * pairs), 1, 1);
+        lc.blockDim = dim3(kThreads, 1, 1);
+        lc.dynamicSmemBytes = smem;
+        lc.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        lc.attrs = attr;
+        lc.numAttrs = 1;
+        trace_before("gemm_tc", stream);
+        cudaError_t e = cudaLaunchKernelEx(&lc, gemm_token2_kernel, tA2, tB2, a);
+        trace_after(stream);
+        if (e != cudaSuccess) return record(e, "gemm_token2_kernel launch");
+        return record(cudaGetLastError(), "gemm_token2_kernel launch");
+    }
     if (!p.swap) {
         static int configured_smem = 0;
         if ((int)p.smem_bytes > configured_smem) {
