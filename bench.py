@@ -47,15 +47,15 @@ L2_FLUSH_BYTES = 256 << 20
 # file the kernel was built from at capture time.  A changed source makes the figure stale
 # and the bench reports traffic as null.
 NCU_TRAFFIC = {
-    # gemm_token_kernel, 7B prefill layer: mean over its 4 launches (QKV, O, gate/up, down)
+    # gemm_token2_kernel (CTA pairs), 7B prefill layer: mean over its 4 launches (QKV, O, gate/up, down)
     "prefill_gemm": {"file": "transformer_decoder_layer_llama_gb300/csrc/gemm_tc.cu",
-                     "sha256": "3471b371352cecf0c9876ccf137179dbc494e25bcecedcf780c3dffb35124269", "bytes_per_launch": 166.96e6},
+                     "sha256": "02ba661f13b8b3b313e90d65ca970d7a54ea306515e776b1182c4b0bb8ad5da9", "bytes_per_launch": 168.74e6},
     # attn_decode_split_kernel, 7B decode (batch 64)
     "llama2_7b_decode_attn": {"file": "transformer_decoder_layer_llama_gb300/csrc/attn.cu",
-                              "sha256": "1fe45d5f7900fc5aa93b3e50982462b484b3bdbf3faf77d4dde5ff4e6891b1ea", "bytes_per_launch": 2245.9e6},
+                              "sha256": "d6df5b316556de7966cdfa479055e63d410d30d157f4291db69131c87f95cff8", "bytes_per_launch": 2246.0e6},
     # gemm_weight_kernel, 70B decode: mean over its 4 launches
     "llama70b_gqa_decode_gemm": {"file": "transformer_decoder_layer_llama_gb300/csrc/gemm_tc.cu",
-                                 "sha256": "3471b371352cecf0c9876ccf137179dbc494e25bcecedcf780c3dffb35124269", "bytes_per_launch": 429.7e6},
+                                 "sha256": "02ba661f13b8b3b313e90d65ca970d7a54ea306515e776b1182c4b0bb8ad5da9", "bytes_per_launch": 429.7e6},
 }
 
 
