@@ -80,6 +80,8 @@ __global__ void __launch_bounds__(160, 2)
     const int split = blockIdx.x, hk = blockIdx.y, b = blockIdx.z;
     const int G = a.n_heads / a.n_kv_heads;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    pdl_wait();
+    pdl_trigger();
     int ctx = a.context_lens[b];
     if (ctx > a.max_blocks * a.block_size || ctx < 0) {
         if (threadIdx.x == 0 && split == 0 && hk == 0) flag_status(a.status, LL_DEV_BAD_POSITION);
@@ -332,6 +334,8 @@ __global__ void __launch_bounds__(160, 2)
 
 // out[b][h] = sum_s 2^(m_s - M) l_s o_s / sum_s 2^(m_s - M) l_s over the splits of (b, h)
 __global__ void attn_decode_combine_kernel(const AttnDecodeArgs a, int max_splits) {
+    pdl_wait();
+    pdl_trigger();
     const int h = blockIdx.x, b = blockIdx.y;
     const int D = a.head_dim;
     int ctx = min(max(a.context_lens[b], 0), a.max_blocks * a.block_size);
@@ -371,13 +375,16 @@ cudaError_t decode_for(const AttnDecodeArgs& a, cudaStream_t stream) {
         return cudaErrorInvalidValue;
     dim3 grid(max_splits, a.n_kv_heads, a.batch);
     trace_before("attn_decode_split", stream);
-    attn_decode_split_kernel<D><<<grid, 160, smem, stream>>>(tmK, tmV, a, max_splits);
+    cudaError_t e = launch_pdl(attn_decode_split_kernel<D>, grid, dim3(160), smem, stream, 1, tmK, tmV, a,
+                               max_splits);
     trace_after(stream);
-    cudaError_t e = cudaGetLastError();
+    if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) return record(e, "attn_decode_split_kernel launch");
     trace_before("attn_decode_combine", stream);
-    attn_decode_combine_kernel<<<dim3(a.n_heads, a.batch), D, 0, stream>>>(a, max_splits);
+    e = launch_pdl(attn_decode_combine_kernel, dim3(a.n_heads, a.batch), dim3(D), 0, stream, 1, a,
+                   max_splits);
     trace_after(stream);
+    if (e != cudaSuccess) return record(e, "attn_decode_combine_kernel launch");
     return record(cudaGetLastError(), "attn_decode_combine_kernel launch");
 }
 

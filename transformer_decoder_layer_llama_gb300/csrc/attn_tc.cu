@@ -137,6 +137,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         tmem_alloc(&tmem_base_s, L::TMEM_COLS);
         tmem_relinquish();
     }
+    pdl_wait();
+    pdl_trigger();
     __syncthreads();
     // the tile's last query position (rows beyond the sequence or out of range count as -1)
     if (threadIdx.x < kQT) {
@@ -466,8 +468,10 @@ cudaError_t prefill_tc_for(const AttnPrefillArgs& a, cudaStream_t stream) {
         return cudaErrorInvalidValue;
     dim3 grid((a.seq_len + kQT - 1) / kQT, a.n_heads, a.batch);
     trace_before("attn_prefill", stream);
-    attn_prefill_tc_kernel<D><<<grid, kTcThreads, smem, stream>>>(tmQ, tmK, tmV, args);
+    cudaError_t e = launch_pdl(attn_prefill_tc_kernel<D>, grid, dim3(kTcThreads), smem, stream, 1, tmQ, tmK,
+                               tmV, args);
     trace_after(stream);
+    if (e != cudaSuccess) return record(e, "attn_prefill_tc_kernel launch");
     return record(cudaGetLastError(), "attn_prefill_tc_kernel launch");
 }
 

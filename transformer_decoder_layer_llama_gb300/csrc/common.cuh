@@ -48,6 +48,15 @@ LL_DEVINL uint64_t global_timer_ns() {
     return t;
 }
 
+// Programmatic dependent launch: a kernel launched with the programmatic-stream-
+// serialization attribute may start while its predecessor in the stream is still
+// finishing.  pdl_wait() blocks until the predecessor grid has completed and its
+// writes are visible; every layer kernel calls it before touching global memory.
+// pdl_trigger() lets the successor be scheduled (only once every CTA of this grid
+// is resident or done, so it can never take slots this grid still needs).
+LL_DEVINL void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+LL_DEVINL void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // A wait that has not finished after this long is treated as a hang.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 

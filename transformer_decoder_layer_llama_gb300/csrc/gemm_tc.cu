@@ -336,6 +336,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    pdl_wait();
+    pdl_trigger();
     const uint32_t tmem = tmem_base_s;
 
     if (warp == 0) {
@@ -510,6 +512,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     cluster_sync();                              // both CTAs' barriers exist before remote use
+    pdl_wait();
+    pdl_trigger();
     const uint32_t tmem = tmem_base_s;
     const uint32_t half_bytes = (uint32_t)BM * BK * 2;     // 16 KB: A rows or B rows of one CTA
 
@@ -688,6 +692,8 @@ __global__ void __launch_bounds__(kThreads, 2)
         tmem_alloc(&tmem_base_s, a.tmem_cols);
         tmem_relinquish();
     }
+    pdl_wait();
+    pdl_trigger();
     if (warp >= 2 && a.ep.kind == EPI_QKV) {
         // each token's position and cache row, once per CTA (the tokens are few)
         const int et = threadIdx.x - 64;
@@ -1001,20 +1007,9 @@ cudaError_t launch_gemm(const GemmProblem& pr, cudaStream_t stream) {
             configured_smem2 = (int)smem;
         }
         const int pairs = std::min(a.units, sms / 2);
-        cudaLaunchConfig_t lc = {};
-        lc.gridDim = dim3((unsigned)(2 * pairs), 1, 1);
-        lc.blockDim = dim3(kThreads, 1, 1);
-        lc.dynamicSmemBytes = smem;
-        lc.stream = stream;
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = 2;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        lc.attrs = attr;
-        lc.numAttrs = 1;
         trace_before("gemm_tc", stream);
-        cudaError_t e = cudaLaunchKernelEx(&lc, gemm_token2_kernel, tA2, tB2, a);
+        cudaError_t e = launch_pdl(gemm_token2_kernel, dim3((unsigned)(2 * pairs)), dim3(kThreads), smem,
+                                   stream, 2, tA2, tB2, a);
         trace_after(stream);
         if (e != cudaSuccess) return record(e, "gemm_token2_kernel launch");
         return record(cudaGetLastError(), "gemm_token2_kernel launch");
@@ -1031,8 +1026,10 @@ cudaError_t launch_gemm(const GemmProblem& pr, cudaStream_t stream) {
         }
         const int grid = std::min(p.units, sms * p.ctas_per_sm);
         trace_before("gemm_tc", stream);
-        gemm_token_kernel<<<grid, kThreads, p.smem_bytes, stream>>>(tmA, tmB, a);
+        cudaError_t e = launch_pdl(gemm_token_kernel, dim3(grid), dim3(kThreads), p.smem_bytes, stream, 1,
+                                   tmA, tmB, a);
         trace_after(stream);
+        if (e != cudaSuccess) return record(e, "gemm_token_kernel launch");
         return record(cudaGetLastError(), "gemm_token_kernel launch");
     }
     static int configured_smem_w = 0;
@@ -1043,20 +1040,9 @@ cudaError_t launch_gemm(const GemmProblem& pr, cudaStream_t stream) {
         if (e != cudaSuccess) return record(e, "cudaFuncSetAttribute(gemm_weight_kernel)");
         configured_smem_w = (int)p.smem_bytes;
     }
-    cudaLaunchConfig_t lc = {};
-    lc.gridDim = dim3((unsigned)p.splits, (unsigned)p.tiles_m, 1);
-    lc.blockDim = dim3(kThreads, 1, 1);
-    lc.dynamicSmemBytes = p.smem_bytes;
-    lc.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = (unsigned)p.splits;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    lc.attrs = attr;
-    lc.numAttrs = 1;
     trace_before("gemm_tc", stream);
-    cudaError_t e = cudaLaunchKernelEx(&lc, gemm_weight_kernel, tmA, tmB, a);
+    cudaError_t e = launch_pdl(gemm_weight_kernel, dim3((unsigned)p.splits, (unsigned)p.tiles_m),
+                               dim3(kThreads), p.smem_bytes, stream, (unsigned)p.splits, tmA, tmB, a);
     trace_after(stream);
     if (e != cudaSuccess) return record(e, "gemm_weight_kernel launch");
     return record(cudaGetLastError(), "gemm_weight_kernel launch");

@@ -9,6 +9,35 @@
 
 namespace ll {
 
+// Launches `kernel` with programmatic dependent launch (it may be scheduled while
+// the previous kernel in the stream finishes; the kernel itself waits for that
+// kernel with griddepcontrol.wait) and, when cluster_x > 1, as clusters of
+// cluster_x CTAs along x.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t stream, unsigned cluster_x, Args&&... args) {
+    cudaLaunchConfig_t lc = {};
+    lc.gridDim = grid;
+    lc.blockDim = block;
+    lc.dynamicSmemBytes = smem;
+    lc.stream = stream;
+    cudaLaunchAttribute at[2];
+    unsigned n = 0;
+    at[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+    if (cluster_x > 1) {
+        at[n].id = cudaLaunchAttributeClusterDimension;
+        at[n].val.clusterDim.x = cluster_x;
+        at[n].val.clusterDim.y = 1;
+        at[n].val.clusterDim.z = 1;
+        ++n;
+    }
+    lc.attrs = at;
+    lc.numAttrs = n;
+    return cudaLaunchKernelEx(&lc, kernel, static_cast<Args&&>(args)...);
+}
+
 enum EpiKind : int {
     EPI_STORE = 0,   // out = acc
     EPI_RESID = 1,   // out = resid + acc (O projection, down projection); resid and out may be fp32

@@ -46,6 +46,8 @@ __global__ void __launch_bounds__(kNormThreads) rmsnorm_kernel(const In* __restr
                                                                __nv_bfloat16* __restrict__ out,
                                                                int hidden, float eps,
                                                                int32_t* zero_ptr, int zero_words) {
+    pdl_wait();
+    pdl_trigger();
     const int t = blockIdx.x;
     if (zero_ptr && t == 0)
         for (int i = threadIdx.x; i < zero_words; i += blockDim.x) zero_ptr[i] = 0;
@@ -184,9 +186,10 @@ cudaError_t launch_rmsnorm(const __nv_bfloat16* x, const float* g, __nv_bfloat16
     if (tokens <= 0) return cudaSuccess;
     const int threads = std::min(kNormThreads, std::max(32, ((hidden / 8 + 31) / 32) * 32));
     trace_before("rmsnorm", stream);
-    rmsnorm_kernel<__nv_bfloat16><<<tokens, threads, 0, stream>>>(x, g, out, hidden, eps, zero_ptr,
-                                                                   zero_words);
+    cudaError_t e = launch_pdl(rmsnorm_kernel<__nv_bfloat16>, dim3(tokens), dim3(threads), 0, stream, 1, x,
+                               g, out, hidden, eps, zero_ptr, zero_words);
     trace_after(stream);
+    if (e != cudaSuccess) return record(e, "rmsnorm launch");
     return record(cudaGetLastError(), "rmsnorm launch");
 }
 
@@ -195,8 +198,10 @@ cudaError_t launch_rmsnorm_f32(const float* x, const float* g, __nv_bfloat16* ou
     if (tokens <= 0) return cudaSuccess;
     const int threads = std::min(kNormThreads, std::max(32, ((hidden / 8 + 31) / 32) * 32));
     trace_before("rmsnorm", stream);
-    rmsnorm_kernel<float><<<tokens, threads, 0, stream>>>(x, g, out, hidden, eps, nullptr, 0);
+    cudaError_t e = launch_pdl(rmsnorm_kernel<float>, dim3(tokens), dim3(threads), 0, stream, 1, x, g, out,
+                               hidden, eps, (int32_t*)nullptr, 0);
     trace_after(stream);
+    if (e != cudaSuccess) return record(e, "rmsnorm_f32 launch");
     return record(cudaGetLastError(), "rmsnorm_f32 launch");
 }
 
