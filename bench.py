@@ -392,11 +392,13 @@ def traced_breakdown(api, work, steps, stream, flush):
         e = per.setdefault(name, {"launches": 0, "ms": 0.0})
         e["launches"] += 1
         e["ms"] += ms
-        # the k-th GEMM of a step (QKV, O, gate/up, down), averaged over steps
-        if name == "gemm_tc" and per_step:
+        # the k-th GEMM of a step (QKV, O, gate/up, down), averaged over steps; a
+        # weight-form GEMM is its stream-K launch plus the fix-up launch behind it
+        if name in ("gemm_tc", "gemm_fixup") and per_step:
             k = sum(1 for n, _ in launches[(i // per_step) * per_step:i] if n == "gemm_tc")
+            k -= name == "gemm_fixup"
             g = per.setdefault("gemm_by_position_ms", [0.0] * 4)
-            if k < 4:
+            if 0 <= k < 4:
                 g[k] += ms / steps
     total = sum(v["ms"] for k, v in per.items() if isinstance(v, dict))
     for v in per.values():
@@ -614,7 +616,7 @@ def main():
             n2 = min(k2, 30)
             att_ms = (per2.get("attn_decode_split", {"ms": 0})["ms"]
                       + per2.get("attn_decode_combine", {"ms": 0})["ms"]) / n2
-            gem_ms = per2.get("gemm_tc", {"ms": 0})["ms"] / n2
+            gem_ms = (per2.get("gemm_tc", {"ms": 0})["ms"] + per2.get("gemm_fixup", {"ms": 0})["ms"]) / n2
             dom = "attn_decode" if att_ms >= gem_ms else "gemm_tc"
             dom_bytes = dw.kv_read if dom == "attn_decode" else weight_bytes(dw.d)
             dom_ms = att_ms if dom == "attn_decode" else gem_ms

@@ -22,6 +22,7 @@ DEV = "cuda"
 @pytest.mark.parametrize("m,n,k", [
     (1, 128, 64), (2, 512, 256), (16, 1376, 688), (64, 4096, 4096), (33, 11008, 4096),
     (64, 4096, 11008),                                   # weight form, split K
+    (64, 128, 4096), (48, 256, 8192),                    # 16-32 CTAs share one tile
     (65, 256, 128), (128, 512, 256), (300, 1376, 688), (2048, 4096, 4096), (257, 12288, 4096),
 ])
 def test_linear_matches_float64_matmul(m, n, k):
@@ -183,3 +184,32 @@ def test_bad_block_table_sets_status_without_fault():
     torch.cuda.synchronize()
     assert int(status.item()) & api.LL_DEV_BAD_BLOCK
     assert torch.isfinite(y.float()).all()
+
+
+def test_decode_step_is_bitwise_repeatable():
+    """The weight-form GEMMs split K over CTAs and add the float32 partials in a fixed
+    order whichever CTA finishes last, so repeating a step reproduces every bit (the
+    K/V rows it appends are rewritten with the same values)."""
+    wl, d, B, S, W, Wn, table, kp, vp, cfg, packed = _tiny_setup(seed=11, S=40, B=2, steps=2)
+    kpd, vpd, td = kp.to(DEV), vp.to(DEV), table.to(DEV)
+    ctx = torch.full((B,), S + 1, dtype=torch.int32, device=DEV)
+    xd = synth.make_x(B, d.hidden, seed=61).to(DEV)
+    status = api.new_status()
+    y1 = api.layer_decode_step(cfg, packed, xd, kpd, vpd, td, ctx, status=status).clone()
+    y2 = api.layer_decode_step(cfg, packed, xd, kpd, vpd, td, ctx, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    assert torch.equal(y1, y2)
+
+
+@pytest.mark.parametrize("m,n,k", [(64, 12288, 4096), (7, 22016, 4096), (64, 4096, 11008)])
+def test_weight_form_linear_repeatable(m, n, k):
+    x = synth.normal_bf16((m, k), 1.0, seed=k + m, tag="x").to(DEV)
+    w = synth.normal_bf16((n, k), 0.02, seed=n, tag="w").to(DEV)
+    y1 = api.linear(x, w)
+    y2 = api.linear(x, w)
+    torch.cuda.synchronize()
+    assert torch.equal(y1, y2)
+    idx = torch.arange(0, n, 997)
+    ref = f64(x.cpu()) @ f64(w.cpu()[idx]).T
+    assert_close(f64(y1.cpu()[:, idx]), ref, f"linear {m}x{n}x{k} sampled", atol=2e-3, rtol=8e-3)

@@ -164,6 +164,7 @@ int run_layer(const ll_config* cfg, const void* packed, const void* x, const int
     if (e != cudaSuccess) return LL_ERR_CUDA;
 
     GemmProblem g{};
+    g.w_static = true;                           // the packed weights
     g.partials = partials;
     g.partial_bytes = L.partial_bytes;
     g.counter_cap = L.counter_words;

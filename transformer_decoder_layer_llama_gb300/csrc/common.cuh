@@ -135,6 +135,25 @@ LL_DEVINL void tma_load_2d(void* smem_dst, const void* tmap, int32_t c0, int32_t
         : "memory");
 }
 
+// Plain bulk copy of `bytes` (a multiple of 16, both addresses 16-byte aligned)
+// from global to shared memory, completing `bar`'s transaction count.
+LL_DEVINL void bulk_load(void* smem_dst, const void* gmem_src, uint32_t bytes, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_u32(smem_dst)),
+        "l"(reinterpret_cast<uint64_t>(gmem_src)), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+
+// Hint: bring the 128-byte line holding `p` into L2.
+LL_DEVINL void prefetch_l2(const void* p) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<uint64_t>(p)));
+}
+
+// Orders this thread's generic-proxy global accesses with its async-proxy ones
+// (bulk copies) in both directions.
+LL_DEVINL void fence_proxy_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
+
 LL_DEVINL void tma_load_2d_hint(void* smem_dst, const void* tmap, int32_t c0, int32_t c1,
                                 uint64_t* bar, uint64_t policy) {
     asm volatile(

@@ -14,10 +14,10 @@
 //    the output tiles token-block-fastest so that CTAs running together share
 //    the weight tile in L2.
 //  * weight form (<= 64 tokens, decode): A = weights in 128-row blocks, B = the
-//    few token rows (MMA N = tokens rounded up to 16).  The K range is split
-//    across CTAs so that enough of them stream weights; float32 partial tiles
-//    go to a scratch buffer and the last CTA to finish a tile (an atomic
-//    ticket, no spinning) adds them up and runs the epilogue.
+//    few token rows (MMA N = tokens rounded up to 16).  Persistent stream-K
+//    CTAs (one per SM) split the tiles x K blocks evenly; tiles split between
+//    CTAs leave float32 partials in scratch, which a small fix-up kernel,
+//    launched right behind, adds up before running the epilogue.
 //
 // Warp roles (192 threads): warp 0 issues TMA loads, warp 1 allocates TMEM
 // and issues the MMAs, warps 2-5 drain TMEM (warp w reads TMEM lanes
@@ -53,13 +53,14 @@ struct GemmArgs {
     int bn;                  // MMA N
     int tiles_m;             // number of A blocks
     int tiles_n;             // number of B blocks
-    int splits;
     int num_kb;
     int units;
     int stages;
     uint32_t stage_bytes;
     uint32_t a_bytes;
     uint32_t tmem_cols;
+    int w_prefetch;          // weight form: weights may be loaded before the grid dependency wait
+    float* partials;         // weight form: [CTAs][2][tokens][128] float32 partial tiles
 };
 
 LL_DEVINL float silu_f(float z) { return z / (1.0f + expf(-z)); }
@@ -210,10 +211,14 @@ LL_DEVINL void epi_token_chunk(const EpiParams& ep, int t, bool row_ok, int n0, 
 // ---------------------------------------------------------------- weight-form epilogue
 // One thread owns one output feature n (its TMEM lane) and up to 16
 // consecutive tokens t0..t0+tcount-1.  All 32 lanes of the warp call this
-// together (shuffles).
+// together (shuffles).  The shared-memory tables hold tokens tb, tb+1, ...:
+// s_pos / s_row the tokens' positions and cache rows (EPI_QKV), cs_s their
+// RoPE (cos, sin) rows, [token][head_dim / 2] (EPI_QKV); rs the residual rows
+// of n's 128-feature tile, [token][128] (EPI_RESID), or null to read them from
+// global memory.
 LL_DEVINL void epi_weight_chunk(const EpiParams& ep, int n, int N, int t0, int T,
                                 const float (&v)[16], const int* s_pos, const long long* s_row,
-                                int tcount = 16) {
+                                const float2* cs_s, const uint8_t* rs, int tb, int tcount = 16) {
     const bool n_ok = n < N;
     T = min(T, t0 + tcount);   // this call covers tokens t0 .. min(T, t0 + tcount) - 1
     switch (ep.kind) {
@@ -224,17 +229,45 @@ LL_DEVINL void epi_weight_chunk(const EpiParams& ep, int n, int N, int t0, int T
                     if (t0 + j < T) ep.out[(size_t)(t0 + j) * ep.ld_out + n] = __float2bfloat16_rn(v[j]);
             break;
         case EPI_RESID:
-            if (n_ok)
+            if (n_ok) {
+                // All 16 residuals are at hand before the first store: from shared memory, or
+                // requested together from global memory (raw predicated loads, converted after,
+                // so that no load waits for the one before it).
+                float rv[16];
+                const int col = n % 128;
+                if (rs) {
+                    if (ep.resid_f32) {
+#pragma unroll
+                        for (int j = 0; j < 16; ++j)
+                            rv[j] = reinterpret_cast<const float*>(rs)[(t0 + j - tb) * 128 + col];
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 16; ++j)
+                            rv[j] = __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(rs)[(t0 + j - tb) * 128 + col]);
+                    }
+                } else if (ep.resid_f32) {
+#pragma unroll
+                    for (int j = 0; j < 16; ++j)
+                        rv[j] = t0 + j < T ? __ldcg(ep.resid_f32 + (size_t)(t0 + j) * N + n) : 0.f;
+                } else {
+                    const unsigned short* rb = reinterpret_cast<const unsigned short*>(ep.resid);
+                    unsigned short raw[16];
+#pragma unroll
+                    for (int j = 0; j < 16; ++j)
+                        raw[j] = t0 + j < T ? __ldcg(rb + (size_t)(t0 + j) * N + n) : (unsigned short)0;
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) rv[j] = __uint_as_float((uint32_t)raw[j] << 16);
+                }
 #pragma unroll
                 for (int j = 0; j < 16; ++j)
                     if (t0 + j < T) {
                         const size_t at = (size_t)(t0 + j) * N + n;
-                        const float r = ep.resid_f32 ? ep.resid_f32[at] : __bfloat162float(ep.resid[at]);
                         if (ep.out_f32)
-                            ep.out_f32[at] = r + v[j];
+                            ep.out_f32[at] = rv[j] + v[j];
                         else
-                            ep.out[(size_t)(t0 + j) * ep.ld_out + n] = __float2bfloat16_rn(r + v[j]);
+                            ep.out[(size_t)(t0 + j) * ep.ld_out + n] = __float2bfloat16_rn(rv[j] + v[j]);
                     }
+            }
             break;
         case EPI_SWIGLU:
 #pragma unroll
@@ -259,27 +292,26 @@ LL_DEVINL void epi_weight_chunk(const EpiParams& ep, int n, int N, int t0, int T
 #pragma unroll
             for (int j = 0; j < 16; ++j) other[j] = __shfl_xor_sync(0xffffffffu, v[j], 1);
             if (!n_ok) break;
-            float2 cs[16];
-            if (sec != 2) {
+            int pj[16];
+            long long rj[16];
 #pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    const int p = (t0 + j < T) ? s_pos[t0 + j] : -1;
-                    cs[j] = p >= 0 ? ep.rope_cs[(size_t)p * (d >> 1) + pair] : make_float2(0.f, 0.f);
-                }
+            for (int j = 0; j < 16; ++j) {
+                pj[j] = t0 + j < T ? s_pos[t0 + j - tb] : -1;
+                rj[j] = t0 + j < T ? s_row[t0 + j - tb] : -1;
             }
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
-                const int t = t0 + j;
-                if (t >= T || s_pos[t] < 0) continue;
+                if (pj[j] < 0) continue;
                 float val = v[j];
-                if (sec != 2)
-                    val = (e & 1) ? (v[j] * cs[j].x + other[j] * cs[j].y)
-                                  : (v[j] * cs[j].x - other[j] * cs[j].y);
+                if (sec != 2) {
+                    const float2 cs = cs_s[(t0 + j - tb) * (d >> 1) + pair];
+                    val = (e & 1) ? (v[j] * cs.x + other[j] * cs.y) : (v[j] * cs.x - other[j] * cs.y);
+                }
                 const __nv_bfloat16 bv = __float2bfloat16_rn(val);
                 if (sec == 0) {
-                    ep.q_out[(size_t)t * nq + (size_t)head * d + orig] = bv;
-                } else if (s_row[t] >= 0) {
-                    const size_t row = (size_t)s_row[t] + (size_t)head * ep.block_size;
+                    ep.q_out[(size_t)(t0 + j) * nq + (size_t)head * d + orig] = bv;
+                } else if (rj[j] >= 0) {
+                    const size_t row = (size_t)rj[j] + (size_t)head * ep.block_size;
                     (sec == 1 ? ep.k_pool : ep.v_pool)[row * d + orig] = bv;
                 }
             }
@@ -629,38 +661,51 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ---------------------------------------------------------------- weight form
-// One CTA = one (128-feature tile, K split); the splits of a tile form one
-// thread-block cluster (cluster rank = split).  Each CTA accumulates its K
-// range in TMEM, drains the float32 partial [tokens][128] into its own
-// shared memory, and after a cluster barrier reduces its share of the tokens
-// over all the cluster's partials through distributed shared memory, then
-// runs the fused epilogue on them.  Deterministic; no global scratch.
+// Persistent stream-K over the weights.  The tiles_m x num_kb (128-feature
+// tile, 64-wide K block) iterations are cut into one contiguous, equal share
+// per CTA, so every SM streams the same number of weight bytes whatever the
+// tile count.  A share crosses tile boundaries; the part of a tile that one
+// CTA covers (a segment) accumulates in one of two TMEM buffers, so the
+// epilogue of one segment overlaps the main loop of the next.  A segment that
+// covers its whole tile runs the fused epilogue straight from TMEM; any other
+// segment stores its float32 partial to scratch (slot 0 for the CTA's first
+// segment, slot 1 for its last) and the fix-up kernel finishes the tile.  No
+// CTA ever waits for another.  The RoPE rows of the step's tokens sit in
+// shared memory from the start, so a whole-tile QKV epilogue reads nothing
+// from global memory but the token table.
 
-LL_DEVINL void cluster_sync_all() {
-    asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
-}
+// First iteration of CTA c's share, and the CTA whose share holds iteration w.
+LL_DEVINL int sk_begin(int c, int W, int P) { return (int)((long long)c * W / P); }
+LL_DEVINL int sk_owner(int w, int W, int P) { return (int)(((long long)(w + 1) * P - 1) / W); }
 
-// shared::cluster address of `local_smem_addr` in the CTA of cluster rank `rank`
-LL_DEVINL uint32_t dsmem_map(uint32_t local_smem_addr, uint32_t rank) {
+constexpr int kPartialFloats = kSwapMaxTokens * BM;   // one partial tile: [tokens][128] float32
+constexpr int kAuxBytes = kSwapMaxTokens * 64 * 8;    // RoPE (cos, sin) rows of the tokens, head_dim <= 128
+constexpr int kMaxWeightCtas = 160;                   // scratch bound: CTAs of one launch
+constexpr int kMinItersPerCta = 4;
+
+// bar.red.and over the 128 epilogue threads (named barrier 1): every one of them
+// learns whether all of them hold `v`.
+LL_DEVINL bool epi_all(bool v) {
     uint32_t r;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local_smem_addr), "r"(rank));
-    return r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\tbar.red.and.pred q, 1, 128, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)v)
+        : "memory");
+    return r != 0;
 }
 
-LL_DEVINL float dsmem_ld(uint32_t cluster_addr) {
-    float v;
-    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(cluster_addr) : "memory");
-    return v;
-}
+LL_DEVINL void epi_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
-__global__ void __launch_bounds__(kThreads, 2)
+__global__ void __launch_bounds__(kThreads, 1)
     gemm_weight_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                        const GemmArgs a) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~uintptr_t(1023));
     __shared__ uint64_t full_bar[MAX_STAGES], empty_bar[MAX_STAGES];
-    __shared__ uint64_t tfull_bar, drain_bar;
+    __shared__ uint64_t tfull_bar[2], tempty_bar[2], drain_bar;
     __shared__ uint32_t tmem_base_s;
     __shared__ int abort_s;
     __shared__ int tok_pos_s[kSwapMaxTokens];        // EPI_QKV: per-token position
@@ -669,17 +714,21 @@ __global__ void __launch_bounds__(kThreads, 2)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     int32_t* status = a.ep.status;
-    const int split = blockIdx.x;                    // == cluster rank (cluster = the tile's splits)
-    const int tile = blockIdx.y;
-    const int kb0 = (int)((long long)split * a.num_kb / a.splits);
-    const int kb1 = (int)((long long)(split + 1) * a.num_kb / a.splits);
+    const int P = (int)gridDim.x;
+    const int cta = (int)blockIdx.x;
+    const int nkb = a.num_kb;
+    const int W = a.tiles_m * nkb;
+    const int w0 = sk_begin(cta, W, P), w1 = sk_begin(cta + 1, W, P);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < a.stages; ++s) {
             mbar_init(&full_bar[s], 1);
             mbar_init(&empty_bar[s], 1);
         }
-        mbar_init(&tfull_bar, 1);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&tfull_bar[b], 1);
+            mbar_init(&tempty_bar[b], 128);
+        }
         mbar_init(&drain_bar, 1);
         abort_s = 0;
         fence_mbar_init();
@@ -691,6 +740,20 @@ __global__ void __launch_bounds__(kThreads, 2)
     if (warp == 1) {
         tmem_alloc(&tmem_base_s, a.tmem_cols);
         tmem_relinquish();
+    }
+    // weights stream once: keep them from pushing the activations out of L2
+    const uint64_t pol_w = l2_policy_evict_first();
+    // Weights that no kernel still in flight can be writing (the layer's packed
+    // weights) fill the first ring of stages before the wait for the previous
+    // kernel, so their latency overlaps its tail; the activations come after it.
+    const int n_pre = a.w_prefetch ? min(a.stages, w1 - w0) : 0;
+    __syncthreads();                             // barriers initialised before the first load
+    if (warp == 0 && lane == 0) {
+        for (int i = 0; i < n_pre; ++i) {
+            const int w = w0 + i, tile = w / nkb, kb = w - tile * nkb;
+            mbar_arrive_expect_tx(&full_bar[i], a.stage_bytes);
+            tma_load_2d_hint(smem + (size_t)i * a.stage_bytes, &tmW, kb * BK, tile * BM, &full_bar[i], pol_w);
+        }
     }
     pdl_wait();
     pdl_trigger();
@@ -710,19 +773,23 @@ __global__ void __launch_bounds__(kThreads, 2)
 
     if (warp == 0) {
         if (lane == 0) {
-            // weights stream once: keep them from pushing the activations out of L2
-            const uint64_t pol_w = l2_policy_evict_first();
             int stage = 0;
             uint32_t phase = 0;
             uint32_t issued[MAX_STAGES];
             for (int s = 0; s < MAX_STAGES; ++s) issued[s] = 0;
-            for (int kb = kb0; kb < kb1; ++kb) {
-                if (!mbar_wait_bounded(&empty_bar[stage], phase ^ 1, &abort_s, status)) break;
+            for (int w = w0; w < w1; ++w) {
+                const int tile = w / nkb, kb = w - tile * nkb;
                 uint8_t* sa = smem + (size_t)stage * a.stage_bytes;
                 uint8_t* sb = sa + a.a_bytes;
-                mbar_arrive_expect_tx(&full_bar[stage], a.stage_bytes);
-                tma_load_2d_hint(sa, &tmW, kb * BK, tile * BM, &full_bar[stage], pol_w);
-                tma_load_2d(sb, &tmX, kb * BK, 0, &full_bar[stage]);
+                if (w - w0 < n_pre) {
+                    // the weight half of this stage is already on its way
+                    tma_load_2d(sb, &tmX, kb * BK, 0, &full_bar[stage]);
+                } else {
+                    if (!mbar_wait_bounded(&empty_bar[stage], phase ^ 1, &abort_s, status)) break;
+                    mbar_arrive_expect_tx(&full_bar[stage], a.stage_bytes);
+                    tma_load_2d_hint(sa, &tmW, kb * BK, tile * BM, &full_bar[stage], pol_w);
+                    tma_load_2d(sb, &tmX, kb * BK, 0, &full_bar[stage]);
+                }
                 for (int s = 0; s < MAX_STAGES; ++s) issued[s] += (s == stage);
                 if (++stage == a.stages) {
                     stage = 0;
@@ -742,88 +809,170 @@ __global__ void __launch_bounds__(kThreads, 2)
             int stage = 0;
             uint32_t phase = 0;
             bool ok = true;
-            for (int kb = kb0; kb < kb1; ++kb) {
-                if (!mbar_wait_bounded(&full_bar[stage], phase, &abort_s, status)) {
-                    ok = false;
-                    break;
-                }
+            for (int w = w0, seg = 0; w < w1 && ok; ++seg) {
+                const int tile = w / nkb;
+                const int ws = w, we = min(w1, (tile + 1) * nkb);
+                const int buf = seg & 1;
+                const uint32_t accp = (uint32_t)(seg >> 1) & 1;
+                if (!mbar_wait_bounded(&tempty_bar[buf], accp ^ 1, &abort_s, status)) break;
                 tc_fence_after();
-                const uint32_t sa = smem_u32(smem + (size_t)stage * a.stage_bytes);
-                const uint32_t sb = sa + a.a_bytes;
-                const uint64_t da = umma_desc_sw128(sa);
-                const uint64_t db = umma_desc_sw128(sb);
+                const uint32_t d_tmem = tmem + (uint32_t)(buf * a.bn);
+                for (; w < we; ++w) {
+                    if (!mbar_wait_bounded(&full_bar[stage], phase, &abort_s, status)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t sa = smem_u32(smem + (size_t)stage * a.stage_bytes);
+                    const uint32_t sb = sa + a.a_bytes;
+                    const uint64_t da = umma_desc_sw128(sa);
+                    const uint64_t db = umma_desc_sw128(sb);
 #pragma unroll
-                for (int kk = 0; kk < BK / UK; ++kk)
-                    tc_mma_bf16(tmem, da + (uint64_t)(kk * 2), db + (uint64_t)(kk * 2), idesc,
-                                (kb > kb0 || kk > 0) ? 1u : 0u);
-                tc_commit(&empty_bar[stage]);
-                if (++stage == a.stages) {
-                    stage = 0;
-                    phase ^= 1;
+                    for (int kk = 0; kk < BK / UK; ++kk)
+                        tc_mma_bf16(d_tmem, da + (uint64_t)(kk * 2), db + (uint64_t)(kk * 2), idesc,
+                                    (w > ws || kk > 0) ? 1u : 0u);
+                    tc_commit(&empty_bar[stage]);
+                    if (++stage == a.stages) {
+                        stage = 0;
+                        phase ^= 1;
+                    }
                 }
+                if (ok) tc_commit(&tfull_bar[buf]);
             }
-            if (ok) tc_commit(&tfull_bar);
             tc_commit(&drain_bar);
             volatile int never = 0;
             mbar_wait_bounded(&drain_bar, 0, &never, status);
         }
         __syncwarp();
-    }
-
-    // ---------------------------------------------------- epilogue warps: drain TMEM
-    const int q = warp & 3;
-    const int r = q * 32 + lane;                 // TMEM lane = feature row of the tile
-    const int n = tile * BM + r;
-    const int T = a.tokens;
-    float* part = reinterpret_cast<float*>(smem);   // [bn][128] float32, over the idle ring
-    bool have = false;
-    if (warp >= 2) {
-        have = mbar_wait_bounded(&tfull_bar, 0, &abort_s, status);
-        if (have) {
-            tc_fence_after();
-            const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16);
-            for (int c = 0; c < a.bn; c += 16) {
-                float v[16];
-                tmem_ld16(taddr + (uint32_t)c, v);
-                if (a.splits == 1) {
-                    epi_weight_chunk(a.ep, n, a.n, c, T, v, tok_pos_s, tok_row_s);
-                } else {
-#pragma unroll
-                    for (int j = 0; j < 16; ++j) part[(c + j) * BM + r] = v[j];
-                }
+    } else {
+        // ------------------------------------------------ epilogue warps 2-5
+        const int q = warp & 3;
+        const int r = q * 32 + lane;             // TMEM lane = feature row of the tile
+        const int T = a.tokens;
+        const int et = threadIdx.x - 64;         // 0..127
+        const uint32_t lane_base = (uint32_t)(q * 32) << 16;
+        uint8_t* aux = smem + (size_t)a.stages * a.stage_bytes;   // kAuxBytes: RoPE rows (QKV)
+        const float2* cs_s = reinterpret_cast<const float2*>(aux);
+        const int resid_esz = a.ep.resid_f32 ? 4 : 2;
+        if (a.ep.kind == EPI_QKV) {
+            // the (cos, sin) rows of the tokens' positions, once per CTA, while the weights stream
+            const int half = a.ep.head_dim / 2;
+            float2* dst = reinterpret_cast<float2*>(aux);
+            for (int i = et; i < T * half; i += 128) {
+                const int p = tok_pos_s[i / half];
+                dst[i] = p >= 0 ? __ldg(a.ep.rope_cs + (size_t)p * half + (i % half)) : make_float2(0.f, 0.f);
             }
+        } else if (a.ep.kind == EPI_RESID) {
+            // warm L2 with the residual rows of the tiles this CTA touches
+            const int lines = BM * resid_esz / 128;
+            const uint8_t* base = a.ep.resid_f32 ? reinterpret_cast<const uint8_t*>(a.ep.resid_f32)
+                                                 : reinterpret_cast<const uint8_t*>(a.ep.resid);
+            for (int tile = w0 / nkb; tile <= (w1 - 1) / nkb; ++tile)
+                for (int i = et; i < T * lines; i += 128) {
+                    const int n0 = tile * BM + (i % lines) * (128 / resid_esz);
+                    if (n0 < a.n) prefetch_l2(base + ((size_t)(i / lines) * a.n + n0) * resid_esz);
+                }
         }
-    }
-    if (a.splits > 1) {
-        cluster_sync_all();                      // every partial of the tile is in shared memory
-        if (warp >= 2 && !abort_s) {
-            // this CTA's tokens: [t_lo, t_hi), summed over the cluster's partials
-            const int t_lo = split * T / a.splits, t_hi = (split + 1) * T / a.splits;
-            const uint32_t my_part = smem_u32(part);
-            for (int t0 = t_lo; t0 < t_hi; t0 += 16) {
-                const int cnt = min(16, t_hi - t0);
-                float v[16];
-#pragma unroll
-                for (int j = 0; j < 16; ++j) v[j] = 0.f;
-                for (int sp = 0; sp < a.splits; ++sp) {
-                    const uint32_t base = dsmem_map(my_part, (uint32_t)sp);
-                    float t16[16];
+        epi_sync();                              // the RoPE rows are in shared memory
+
+        for (int w = w0, seg = 0; w < w1; ++seg) {
+            const int tile = w / nkb;
+            const int ws = w, we = min(w1, (tile + 1) * nkb);
+            w = we;
+            const int buf = seg & 1;
+            const uint32_t accp = (uint32_t)(seg >> 1) & 1;
+            const bool have = mbar_wait_bounded(&tfull_bar[buf], accp, &abort_s, status);
+            if (!epi_all(have)) break;           // all 128 threads leave together
+            tc_fence_after();
+            const uint32_t taddr = tmem + lane_base + (uint32_t)(buf * a.bn);
+            if (ws == tile * nkb && we == (tile + 1) * nkb) {
+                const int n = tile * BM + r;
+                for (int c = 0; c < a.bn; c += 16) {
+                    float v[16];
+                    tmem_ld16(taddr + (uint32_t)c, v);
+                    epi_weight_chunk(a.ep, n, a.n, c, T, v, tok_pos_s, tok_row_s, cs_s, nullptr, 0);
+                }
+            } else {
+                // a piece of the tile: the CTA's first segment goes to slot 0, its last to slot 1
+                float* mine = a.partials + ((size_t)cta * 2 + (ws == w0 ? 0 : 1)) * kPartialFloats;
+                for (int c = 0; c < a.bn; c += 16) {
+                    float v[16];
+                    tmem_ld16(taddr + (uint32_t)c, v);
 #pragma unroll
                     for (int j = 0; j < 16; ++j)
-                        t16[j] = j < cnt ? dsmem_ld(base + (uint32_t)(((t0 + j) * BM + r) * 4)) : 0.f;
-#pragma unroll
-                    for (int j = 0; j < 16; ++j) v[j] += t16[j];
+                        if (c + j < T) __stcg(mine + (size_t)(c + j) * BM + r, v[j]);
                 }
-                epi_weight_chunk(a.ep, n, a.n, t0, T, v, tok_pos_s, tok_row_s, cnt);
             }
+            tc_fence_before();
+            mbar_arrive(&tempty_bar[buf]);
         }
-        cluster_sync_all();                      // nobody leaves while others read its partial
     }
 
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     if (warp == 1) tmem_dealloc(tmem, a.tmem_cols);
+}
+
+// ---------------------------------------------------------------- weight form: fix-up
+// One CTA per (128-feature tile, 16 tokens) of a tile that the stream-K kernel
+// split over several CTAs: adds their float32 partials in CTA order (the same
+// sum whichever of them finished first: deterministic) and runs the fused
+// epilogue.  Launched right behind the stream-K kernel (programmatic dependent
+// launch): its CTAs take the SMs as the stream-K CTAs drain and start the
+// moment the last one finishes.  Thread r owns feature r of the tile.
+constexpr int kFixTokens = 16;
+
+__global__ void __launch_bounds__(BM)
+    gemm_weight_fixup_kernel(const GemmArgs a, int P) {
+    __shared__ int tok_pos_s[kFixTokens];
+    __shared__ long long tok_row_s[kFixTokens];
+    __shared__ float2 cs_s[kFixTokens * 64];     // head_dim <= 128
+    const int tile = blockIdx.x, t0 = blockIdx.y * kFixTokens;
+    const int nkb = a.num_kb, W = a.tiles_m * nkb;
+    const int c_first = sk_owner(tile * nkb, W, P), c_last = sk_owner((tile + 1) * nkb - 1, W, P);
+    pdl_wait();
+    pdl_trigger();
+    if (c_first == c_last) return;               // the stream-K kernel finished this tile itself
+    const int r = threadIdx.x;
+    const int T = a.tokens;
+    const int cnt = min(kFixTokens, T - t0);
+    if (a.ep.kind == EPI_QKV) {
+        if (r < cnt) {
+            TokenSlot ts = token_slot(a.ep, t0 + r);
+            tok_pos_s[r] = ts.pos;
+            tok_row_s[r] = ts.kv_row;
+        }
+        __syncthreads();
+        const int half = a.ep.head_dim / 2;
+        for (int i = r; i < cnt * half; i += BM) {
+            const int p = tok_pos_s[i / half];
+            cs_s[i] = p >= 0 ? __ldg(a.ep.rope_cs + (size_t)p * half + i % half) : make_float2(0.f, 0.f);
+        }
+        __syncthreads();
+    }
+    float v[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) v[j] = 0.f;
+    // the contributors in CTA order, up to four partials in flight at once
+    for (int c0 = c_first; c0 <= c_last; c0 += 4) {
+        float part[4][16];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int cc = c0 + u;
+            const int slot = (sk_begin(min(cc, c_last), W, P) / nkb == tile) ? 0 : 1;
+            const float* pp = a.partials + ((size_t)min(cc, c_last) * 2 + slot) * kPartialFloats +
+                              (size_t)t0 * BM + r;
+#pragma unroll
+            for (int j = 0; j < 16; ++j) part[u][j] = (cc <= c_last && j < cnt) ? __ldcg(pp + (size_t)j * BM) : 0.f;
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+            if (c0 + u <= c_last)
+#pragma unroll
+                for (int j = 0; j < 16; ++j) v[j] += part[u][j];
+    }
+    epi_weight_chunk(a.ep, tile * BM + r, a.n, t0, T, v, tok_pos_s, tok_row_s, cs_s, nullptr, t0, cnt);
 }
 
 // ---------------------------------------------------------------- host side
@@ -857,27 +1006,16 @@ uint32_t pow2_at_least(uint32_t x) {
 
 struct Plan {
     bool swap;
-    int bn, tiles_m, tiles_n, splits, num_kb, units, stages, ctas_per_sm;
+    int bn, tiles_m, tiles_n, num_kb, units, stages, ctas_per_sm;
     uint32_t stage_bytes, a_bytes, tmem_cols;
     size_t smem_bytes;
 };
 
-// Weight form: split count s in [1, 8] (one cluster per tile) minimising
-// waves(s) / s, the time of a pass over the weights when every CTA streams
-// 1/s of a tile; ties go to fewer splits.  Each split keeps >= 4 K blocks.
-int choose_splits(int tiles, int num_kb, int slots) {
-    const int s_max = std::max(1, std::min(8, num_kb / 4));
-    int best = 1;
-    double best_cost = 1e30;
-    for (int sp = 1; sp <= s_max; ++sp) {
-        const double waves = (double)((tiles * sp + slots - 1) / slots);
-        const double cost = waves / sp;
-        if (cost < best_cost - 1e-9) {
-            best_cost = cost;
-            best = sp;
-        }
-    }
-    return best;
+// Weight form: one persistent CTA per SM, but never fewer than kMinItersPerCta
+// K blocks per CTA (tiny problems use fewer CTAs and fewer partial tiles).
+int weight_ctas(int tiles, int num_kb, int sms) {
+    const int W = tiles * num_kb;
+    return std::max(1, std::min({sms, kMaxWeightCtas, (W + kMinItersPerCta - 1) / kMinItersPerCta}));
 }
 
 Plan make_plan(int tokens, int n, int k, int sms) {
@@ -889,7 +1027,6 @@ Plan make_plan(int tokens, int n, int k, int sms) {
         p.bn = kTokenFormBN;
         p.tiles_m = ceil_div(tokens, BM);
         p.tiles_n = ceil_div(n, p.bn);
-        p.splits = 1;
         p.stage_bytes = p.a_bytes + p.bn * BK * 2;
         p.stages = 4;
         p.ctas_per_sm = 1;
@@ -900,14 +1037,14 @@ Plan make_plan(int tokens, int n, int k, int sms) {
         p.tiles_m = ceil_div(n, BM);
         p.tiles_n = 1;
         p.stage_bytes = p.a_bytes + p.bn * BK * 2;
-        p.ctas_per_sm = 2;
-        const int budget = (227 * 1024) / p.ctas_per_sm - 2048;
-        p.stages = std::min(MAX_STAGES, budget / (int)p.stage_bytes);
-        p.splits = choose_splits(p.tiles_m, p.num_kb, sms * p.ctas_per_sm);
-        p.units = p.tiles_m * p.splits;
-        p.tmem_cols = pow2_at_least((uint32_t)p.bn);
+        p.ctas_per_sm = 1;
+        // the ring plus the auxiliary region must fit 227 KB with the static shared
+        // memory (< 2 KB) and the 1 KB alignment slack
+        p.stages = std::min(MAX_STAGES, (227 * 1024 - 3072 - kAuxBytes) / (int)p.stage_bytes);
+        p.units = weight_ctas(p.tiles_m, p.num_kb, sms);
+        p.tmem_cols = pow2_at_least(2u * (uint32_t)p.bn);   // two accumulators
     }
-    p.smem_bytes = (size_t)p.stages * p.stage_bytes + 1024;
+    p.smem_bytes = (size_t)p.stages * p.stage_bytes + (p.swap ? kAuxBytes : 0) + 1024;
     return p;
 }
 
@@ -945,15 +1082,19 @@ int device_sm_count() {
 }
 
 void gemm_scratch_need(int tokens, int n, int k, size_t* partial_bytes, int* counters) {
-    (void)tokens; (void)n; (void)k;
-    // split-K partials stay in the cluster's shared memory: no global scratch
-    *partial_bytes = 0;
+    (void)n;
+    (void)k;
+    *partial_bytes = tokens > kSwapMaxTokens ? 0 : gemm_partial_bound_bytes();   // token form: no split K
     *counters = 0;
 }
 
-size_t gemm_partial_bound_bytes() { return 0; }
+// two partial tiles per CTA (its first and its last segment)
+size_t gemm_partial_bound_bytes() { return (size_t)kMaxWeightCtas * 2 * kPartialFloats * sizeof(float); }
 
-int gemm_counter_bound(int n) { (void)n; return 0; }
+int gemm_counter_bound(int n) {
+    (void)n;
+    return 0;
+}
 
 cudaError_t launch_gemm(const GemmProblem& pr, cudaStream_t stream) {
     int sms = device_sm_count();
@@ -968,7 +1109,6 @@ cudaError_t launch_gemm(const GemmProblem& pr, cudaStream_t stream) {
     a.bn = p.bn;
     a.tiles_m = p.tiles_m;
     a.tiles_n = p.tiles_n;
-    a.splits = p.splits;
     a.num_kb = p.num_kb;
     a.units = p.units;
     a.stages = p.stages;
@@ -1040,12 +1180,24 @@ cudaError_t launch_gemm(const GemmProblem& pr, cudaStream_t stream) {
         if (e != cudaSuccess) return record(e, "cudaFuncSetAttribute(gemm_weight_kernel)");
         configured_smem_w = (int)p.smem_bytes;
     }
+    if (!pr.partials || pr.partial_bytes < gemm_partial_bound_bytes()) {
+        set_last_error("launch_gemm", "weight form needs split-K scratch");
+        return cudaErrorInvalidValue;
+    }
+    a.partials = pr.partials;
+    a.w_prefetch = pr.w_static ? 1 : 0;
     trace_before("gemm_tc", stream);
-    cudaError_t e = launch_pdl(gemm_weight_kernel, dim3((unsigned)p.splits, (unsigned)p.tiles_m),
-                               dim3(kThreads), p.smem_bytes, stream, (unsigned)p.splits, tmA, tmB, a);
+    cudaError_t e = launch_pdl(gemm_weight_kernel, dim3((unsigned)p.units), dim3(kThreads), p.smem_bytes,
+                               stream, 1, tmA, tmB, a);
     trace_after(stream);
+    if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) return record(e, "gemm_weight_kernel launch");
-    return record(cudaGetLastError(), "gemm_weight_kernel launch");
+    trace_before("gemm_fixup", stream);
+    e = launch_pdl(gemm_weight_fixup_kernel, dim3((unsigned)p.tiles_m, (unsigned)ceil_div(pr.tokens, kFixTokens)),
+                   dim3(BM), 0, stream, 1, a, p.units);
+    trace_after(stream);
+    if (e != cudaSuccess) return record(e, "gemm_weight_fixup_kernel launch");
+    return record(cudaGetLastError(), "gemm_weight_fixup_kernel launch");
 }
 
 }  // namespace ll

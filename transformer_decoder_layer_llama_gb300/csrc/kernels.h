@@ -80,6 +80,8 @@ struct GemmProblem {
     size_t partial_bytes;
     int32_t* counters;             // one per output tile, zero on entry, left zero on exit
     int counter_cap;
+    bool w_static;                 // w is not written by any kernel that may still be running
+                                   // (it may be read before the wait on the previous kernel)
 };
 
 // Scratch the GEMM may need for a problem of this shape (bytes of float
