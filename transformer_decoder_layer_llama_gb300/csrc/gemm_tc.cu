@@ -212,10 +212,10 @@ LL_DEVINL void epi_token_chunk(const EpiParams& ep, int t, bool row_ok, int n0, 
 // One thread owns one output feature n (its TMEM lane) and up to 16
 // consecutive tokens t0..t0+tcount-1.  All 32 lanes of the warp call this
 // together (shuffles).  The shared-memory tables hold tokens tb, tb+1, ...:
-// s_pos / s_row the tokens' positions and cache rows (EPI_QKV), cs_s their
-// RoPE (cos, sin) rows, [token][head_dim / 2] (EPI_QKV); rs the residual rows
-// of n's 128-feature tile, [token][128] (EPI_RESID), or null to read them from
-// global memory.
+// s_pos / s_row the tokens' positions and cache rows (EPI_QKV); cs_s their
+// RoPE (cos, sin) rows, [token][head_dim / 2] (EPI_QKV), and rs the residual
+// rows of n's 128-feature tile, [token][128] (EPI_RESID), each null to read
+// them from global memory instead.
 LL_DEVINL void epi_weight_chunk(const EpiParams& ep, int n, int N, int t0, int T,
                                 const float (&v)[16], const int* s_pos, const long long* s_row,
                                 const float2* cs_s, const uint8_t* rs, int tb, int tcount = 16) {
@@ -299,12 +299,23 @@ LL_DEVINL void epi_weight_chunk(const EpiParams& ep, int n, int N, int t0, int T
                 pj[j] = t0 + j < T ? s_pos[t0 + j - tb] : -1;
                 rj[j] = t0 + j < T ? s_row[t0 + j - tb] : -1;
             }
+            float2 csj[16];
+            if (sec != 2) {
+                if (cs_s) {
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) csj[j] = cs_s[(t0 + j - tb) * (d >> 1) + pair];
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 16; ++j)
+                        csj[j] = __ldg(ep.rope_cs + (size_t)max(pj[j], 0) * (d >> 1) + pair);
+                }
+            }
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
                 if (pj[j] < 0) continue;
                 float val = v[j];
                 if (sec != 2) {
-                    const float2 cs = cs_s[(t0 + j - tb) * (d >> 1) + pair];
+                    const float2 cs = csj[j];
                     val = (e & 1) ? (v[j] * cs.x + other[j] * cs.y) : (v[j] * cs.x - other[j] * cs.y);
                 }
                 const __nv_bfloat16 bv = __float2bfloat16_rn(val);
@@ -670,16 +681,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 // covers its whole tile runs the fused epilogue straight from TMEM; any other
 // segment stores its float32 partial to scratch (slot 0 for the CTA's first
 // segment, slot 1 for its last) and the fix-up kernel finishes the tile.  No
-// CTA ever waits for another.  The RoPE rows of the step's tokens sit in
-// shared memory from the start, so a whole-tile QKV epilogue reads nothing
-// from global memory but the token table.
+// CTA ever waits for another.  The CTA leaves room in its SM's shared memory
+// for fix-up CTAs, which are placed beside it and wait for it to finish.
 
 // First iteration of CTA c's share, and the CTA whose share holds iteration w.
 LL_DEVINL int sk_begin(int c, int W, int P) { return (int)((long long)c * W / P); }
 LL_DEVINL int sk_owner(int w, int W, int P) { return (int)(((long long)(w + 1) * P - 1) / W); }
 
 constexpr int kPartialFloats = kSwapMaxTokens * BM;   // one partial tile: [tokens][128] float32
-constexpr int kAuxBytes = kSwapMaxTokens * 64 * 8;    // RoPE (cos, sin) rows of the tokens, head_dim <= 128
 constexpr int kMaxWeightCtas = 160;                   // scratch bound: CTAs of one launch
 constexpr int kMinItersPerCta = 4;
 
@@ -851,16 +860,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int T = a.tokens;
         const int et = threadIdx.x - 64;         // 0..127
         const uint32_t lane_base = (uint32_t)(q * 32) << 16;
-        uint8_t* aux = smem + (size_t)a.stages * a.stage_bytes;   // kAuxBytes: RoPE rows (QKV)
-        const float2* cs_s = reinterpret_cast<const float2*>(aux);
         const int resid_esz = a.ep.resid_f32 ? 4 : 2;
         if (a.ep.kind == EPI_QKV) {
-            // the (cos, sin) rows of the tokens' positions, once per CTA, while the weights stream
+            // warm L2 with the RoPE rows of the tokens' positions
             const int half = a.ep.head_dim / 2;
-            float2* dst = reinterpret_cast<float2*>(aux);
-            for (int i = et; i < T * half; i += 128) {
-                const int p = tok_pos_s[i / half];
-                dst[i] = p >= 0 ? __ldg(a.ep.rope_cs + (size_t)p * half + (i % half)) : make_float2(0.f, 0.f);
+            const int lines = half * 8 / 128;
+            for (int i = et; i < T * lines; i += 128) {
+                const int p = tok_pos_s[i / lines];
+                if (p >= 0)
+                    prefetch_l2(reinterpret_cast<const uint8_t*>(a.ep.rope_cs + (size_t)p * half) + (i % lines) * 128);
             }
         } else if (a.ep.kind == EPI_RESID) {
             // warm L2 with the residual rows of the tiles this CTA touches
@@ -873,7 +881,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (n0 < a.n) prefetch_l2(base + ((size_t)(i / lines) * a.n + n0) * resid_esz);
                 }
         }
-        epi_sync();                              // the RoPE rows are in shared memory
 
         for (int w = w0, seg = 0; w < w1; ++seg) {
             const int tile = w / nkb;
@@ -890,7 +897,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int c = 0; c < a.bn; c += 16) {
                     float v[16];
                     tmem_ld16(taddr + (uint32_t)c, v);
-                    epi_weight_chunk(a.ep, n, a.n, c, T, v, tok_pos_s, tok_row_s, cs_s, nullptr, 0);
+                    epi_weight_chunk(a.ep, n, a.n, c, T, v, tok_pos_s, tok_row_s, nullptr, nullptr, 0);
                 }
             } else {
                 // a piece of the tile: the CTA's first segment goes to slot 0, its last to slot 1
@@ -927,17 +934,21 @@ __global__ void __launch_bounds__(BM)
     gemm_weight_fixup_kernel(const GemmArgs a, int P) {
     __shared__ int tok_pos_s[kFixTokens];
     __shared__ long long tok_row_s[kFixTokens];
-    __shared__ float2 cs_s[kFixTokens * 64];     // head_dim <= 128
+    __shared__ __align__(16) uint8_t side_s[kFixTokens * 64 * 8];   // RoPE rows or residual rows
     const int tile = blockIdx.x, t0 = blockIdx.y * kFixTokens;
     const int nkb = a.num_kb, W = a.tiles_m * nkb;
     const int c_first = sk_owner(tile * nkb, W, P), c_last = sk_owner((tile + 1) * nkb - 1, W, P);
-    pdl_wait();
-    pdl_trigger();
-    if (c_first == c_last) return;               // the stream-K kernel finished this tile itself
     const int r = threadIdx.x;
     const int T = a.tokens;
     const int cnt = min(kFixTokens, T - t0);
-    if (a.ep.kind == EPI_QKV) {
+    const bool split = c_first != c_last;        // else the stream-K kernel finished the tile
+    // Before the wait on the stream-K kernel: everything that does not come from it (the
+    // token table, RoPE rows and residual rows are inputs of the layer call, complete
+    // before the kernel that launched the stream-K kernel finished waiting on its own
+    // predecessor).
+    const float2* cs_s = reinterpret_cast<const float2*>(side_s);
+    const uint8_t* rs = nullptr;
+    if (split && a.ep.kind == EPI_QKV) {
         if (r < cnt) {
             TokenSlot ts = token_slot(a.ep, t0 + r);
             tok_pos_s[r] = ts.pos;
@@ -945,12 +956,27 @@ __global__ void __launch_bounds__(BM)
         }
         __syncthreads();
         const int half = a.ep.head_dim / 2;
+        float2* dst = reinterpret_cast<float2*>(side_s);
         for (int i = r; i < cnt * half; i += BM) {
             const int p = tok_pos_s[i / half];
-            cs_s[i] = p >= 0 ? __ldg(a.ep.rope_cs + (size_t)p * half + i % half) : make_float2(0.f, 0.f);
+            dst[i] = p >= 0 ? __ldg(a.ep.rope_cs + (size_t)p * half + i % half) : make_float2(0.f, 0.f);
         }
-        __syncthreads();
+    } else if (split && a.ep.kind == EPI_RESID && tile * BM + r < a.n) {
+        // residual rows t0.., features of this tile: [token][128], float32 or BF16
+        const int n = tile * BM + r;
+        for (int j = 0; j < cnt; ++j) {
+            const size_t at = (size_t)(t0 + j) * a.n + n;
+            if (a.ep.resid_f32)
+                reinterpret_cast<float*>(side_s)[j * BM + r] = __ldg(a.ep.resid_f32 + at);
+            else
+                reinterpret_cast<__nv_bfloat16*>(side_s)[j * BM + r] = a.ep.resid[at];
+        }
     }
+    if (a.ep.kind == EPI_RESID) rs = side_s;
+    pdl_wait();
+    pdl_trigger();
+    if (!split) return;
+    __syncthreads();
     float v[16];
 #pragma unroll
     for (int j = 0; j < 16; ++j) v[j] = 0.f;
@@ -959,12 +985,12 @@ __global__ void __launch_bounds__(BM)
         float part[4][16];
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
-            const int cc = c0 + u;
-            const int slot = (sk_begin(min(cc, c_last), W, P) / nkb == tile) ? 0 : 1;
-            const float* pp = a.partials + ((size_t)min(cc, c_last) * 2 + slot) * kPartialFloats +
-                              (size_t)t0 * BM + r;
+            const int cc = min(c0 + u, c_last);
+            const int slot = (sk_begin(cc, W, P) / nkb == tile) ? 0 : 1;
+            const float* pp = a.partials + ((size_t)cc * 2 + slot) * kPartialFloats + (size_t)t0 * BM + r;
 #pragma unroll
-            for (int j = 0; j < 16; ++j) part[u][j] = (cc <= c_last && j < cnt) ? __ldcg(pp + (size_t)j * BM) : 0.f;
+            for (int j = 0; j < 16; ++j)
+                part[u][j] = (c0 + u <= c_last && j < cnt) ? __ldcg(pp + (size_t)j * BM) : 0.f;
         }
 #pragma unroll
         for (int u = 0; u < 4; ++u)
@@ -972,7 +998,7 @@ __global__ void __launch_bounds__(BM)
 #pragma unroll
                 for (int j = 0; j < 16; ++j) v[j] += part[u][j];
     }
-    epi_weight_chunk(a.ep, tile * BM + r, a.n, t0, T, v, tok_pos_s, tok_row_s, cs_s, nullptr, t0, cnt);
+    epi_weight_chunk(a.ep, tile * BM + r, a.n, t0, T, v, tok_pos_s, tok_row_s, cs_s, rs, t0, cnt);
 }
 
 // ---------------------------------------------------------------- host side
@@ -1038,13 +1064,12 @@ Plan make_plan(int tokens, int n, int k, int sms) {
         p.tiles_n = 1;
         p.stage_bytes = p.a_bytes + p.bn * BK * 2;
         p.ctas_per_sm = 1;
-        // the ring plus the auxiliary region must fit 227 KB with the static shared
-        // memory (< 2 KB) and the 1 KB alignment slack
-        p.stages = std::min(MAX_STAGES, (227 * 1024 - 3072 - kAuxBytes) / (int)p.stage_bytes);
+        // at most ~200 KB, so that fix-up CTAs (< 10 KB) can wait beside the stream-K CTA
+        p.stages = std::min(MAX_STAGES, (200 * 1024) / (int)p.stage_bytes);
         p.units = weight_ctas(p.tiles_m, p.num_kb, sms);
         p.tmem_cols = pow2_at_least(2u * (uint32_t)p.bn);   // two accumulators
     }
-    p.smem_bytes = (size_t)p.stages * p.stage_bytes + (p.swap ? kAuxBytes : 0) + 1024;
+    p.smem_bytes = (size_t)p.stages * p.stage_bytes + 1024;
     return p;
 }
 
