@@ -296,6 +296,7 @@ def continuous_batching(api, wl, steps, warmup, stream, peaks, seed=4321):
     copied = [None, None]
     stats = {"decode_tokens": 0, "prefill_tokens": 0, "admitted": 0, "kv_tokens_read": 0,
              "prefill_flops": 0.0}
+    phase_events = {"prefill": [], "decode": []}
 
     def one_step(i, record):
         k = i & 1
@@ -309,7 +310,13 @@ def continuous_batching(api, wl, steps, warmup, stream, peaks, seed=4321):
                 sub_h[:n].copy_(torch.from_numpy(sch.table[admitted]))
                 eng.pf_table[:n].copy_(sub_h[:n], non_blocking=True)
                 eng.pf_x[:n * prompt].copy_(x_prompt[:n * prompt], non_blocking=True)
+                if record:
+                    e_pf = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                    e_pf[0].record(stream)
                 eng.prefill(n, prompt, stream)
+                if record:
+                    e_pf[1].record(stream)
+                    phase_events["prefill"].append(e_pf)
             ctx = sch.grow_for_decode()
             tab_h.copy_(torch.from_numpy(sch.table))
             ctx_h.copy_(torch.from_numpy(ctx))
@@ -319,7 +326,13 @@ def continuous_batching(api, wl, steps, warmup, stream, peaks, seed=4321):
             ev = torch.cuda.Event()
             ev.record(stream)
             copied[k] = ev
+            if record:
+                e_dc = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                e_dc[0].record(stream)
             eng.decode(stream)
+            if record:
+                e_dc[1].record(stream)
+                phase_events["decode"].append(e_dc)
         if record:
             stats["decode_tokens"] += n_slots
             stats["prefill_tokens"] += len(admitted) * prompt
@@ -348,6 +361,8 @@ def continuous_batching(api, wl, steps, warmup, stream, peaks, seed=4321):
     # minimum bytes of the decode steps: every layer's weights + the KV each step reads
     decode_bytes = steps * L * weight_bytes(d) + L * kv_bytes_read(d, [stats["kv_tokens_read"]])
     roof_s = decode_bytes / (peaks["hbm_gbs"] * 1e9) + stats["prefill_flops"] / (peaks["bf16_tflops"] * 1e12)
+    phase_ms = {k: sum(a.elapsed_time(b) for a, b in v) for k, v in phase_events.items()}
+    decode_roof_s = decode_bytes / (peaks["hbm_gbs"] * 1e9)
     out = {
         "layers": L, "slots": n_slots, "steps": steps, "ms_total": ms, "wall_s": wall,
         "decode_tok_per_s": stats["decode_tokens"] / (ms * 1e-3),
@@ -355,6 +370,13 @@ def continuous_batching(api, wl, steps, warmup, stream, peaks, seed=4321):
         "admitted_requests": stats["admitted"],
         "hbm_gbs_decode_min_bytes": decode_bytes / (ms * 1e-3) / 1e9,
         "roofline_frac": roof_s / (ms * 1e-3),
+        # the same run split by phase: the decode CUDA graphs alone against the decode
+        # bytes, the batched prefills alone, and what is left (host scheduling, copies)
+        "decode_graph_ms": phase_ms["decode"],
+        "decode_graph_roofline_frac": decode_roof_s / (phase_ms["decode"] * 1e-3) if phase_ms["decode"] else 0.0,
+        "prefill_ms": phase_ms["prefill"],
+        "prefill_tflops": stats["prefill_flops"] / (phase_ms["prefill"] * 1e-3) / 1e12 if phase_ms["prefill"] else 0.0,
+        "other_ms": ms - phase_ms["decode"] - phase_ms["prefill"],
         "kv_pool_gb": 2 * L * nb * d.n_kv_heads * d.block_size * d.head_dim * 2 / 1e9,
         "device_status": status,
         "cuda_graph_decode": True,

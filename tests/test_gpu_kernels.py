@@ -23,6 +23,8 @@ DEV = "cuda"
     (1, 128, 64), (2, 512, 256), (16, 1376, 688), (64, 4096, 4096), (33, 11008, 4096),
     (64, 4096, 11008),                                   # weight form, split K
     (64, 128, 4096), (48, 256, 8192),                    # 16-32 CTAs share one tile
+    (200, 1376, 688), (256, 4096, 4096),                 # weight form up to 256 tokens
+    (129, 12288, 512),                                   # few tokens, wide output: CTA pairs
     (65, 256, 128), (128, 512, 256), (300, 1376, 688), (2048, 4096, 4096), (257, 12288, 4096),
 ])
 def test_linear_matches_float64_matmul(m, n, k):
@@ -202,7 +204,7 @@ def test_decode_step_is_bitwise_repeatable():
     assert torch.equal(y1, y2)
 
 
-@pytest.mark.parametrize("m,n,k", [(64, 12288, 4096), (7, 22016, 4096), (64, 4096, 11008)])
+@pytest.mark.parametrize("m,n,k", [(64, 12288, 4096), (7, 22016, 4096), (64, 4096, 11008), (200, 4096, 4096)])
 def test_weight_form_linear_repeatable(m, n, k):
     x = synth.normal_bf16((m, k), 1.0, seed=k + m, tag="x").to(DEV)
     w = synth.normal_bf16((n, k), 0.02, seed=n, tag="w").to(DEV)

@@ -117,7 +117,7 @@ WsLayout ws_layout(const ll_config* c, int T, int max_blocks) {
     L.h = at;  at = align_up(at + (size_t)T * H * 4);   // float32 residual stream
     L.hh = at; at = align_up(at + (size_t)T * H * 2);
     L.a = at;  at = align_up(at + (size_t)T * I * 2);
-    L.partial_bytes = ll::gemm_partial_bound_bytes();
+    L.partial_bytes = ll::gemm_partial_bound_bytes(T);
     L.partials = at; at = align_up(at + L.partial_bytes);
     L.counter_words = std::max({ll::gemm_counter_bound(nqkv), ll::gemm_counter_bound((int)H),
                                 ll::gemm_counter_bound(2 * (int)I)});

@@ -8,13 +8,14 @@
 // after the output and down projections, and SiLU(gate) * up after the merged
 // gate/up projection.
 //
-// Two forms share the kernel:
-//  * token form (many tokens, prefill): A = activations [tokens, K] in
-//    128-row blocks, B = weights [N, K] in 256-row blocks; persistent CTAs walk
-//    the output tiles token-block-fastest so that CTAs running together share
-//    the weight tile in L2.
-//  * weight form (<= 64 tokens, decode): A = weights in 128-row blocks, B = the
-//    few token rows (MMA N = tokens rounded up to 16).  Persistent stream-K
+// Two forms:
+//  * token form (more than 256 tokens, prefill): 256 x 256 output tiles of
+//    tokens x features on CTA pairs (tcgen05.mma.cta_group::2); persistent
+//    pairs walk the tiles token-block-fastest so that pairs running together
+//    share the weight tile in L2.
+//  * weight form (<= 256 tokens: decode and short prefill chunks): A = weights
+//    in 128-row blocks, B = the token rows (MMA N = tokens rounded up to 16,
+//    so the weights are streamed exactly once).  Persistent stream-K
 //    CTAs (one per SM) split the tiles x K blocks evenly; tiles split between
 //    CTAs leave float32 partials in scratch, which a small fix-up kernel,
 //    launched right behind, adds up before running the epilogue.
@@ -43,8 +44,7 @@ constexpr int BK = 64;           // K per pipeline stage: one 128-byte swizzle r
 constexpr int UK = 16;           // K of one tcgen05.mma kind::f16
 constexpr int MAX_STAGES = 8;
 constexpr int kThreads = 192;
-constexpr int kTokenFormBN = 256;
-constexpr int kSwapMaxTokens = 64;
+constexpr int kSwapMaxTokens = 256;
 
 struct GemmArgs {
     EpiParams ep;
@@ -331,177 +331,7 @@ LL_DEVINL void epi_weight_chunk(const EpiParams& ep, int n, int N, int t0, int T
     }
 }
 
-LL_DEVINL void unit_coords(const GemmArgs& a, int u, int& a_blk, int& b_blk, int& kb0, int& kb1) {
-    a_blk = u % a.tiles_m;
-    b_blk = u / a.tiles_m;
-    kb0 = 0;
-    kb1 = a.num_kb;
-}
-
 // ---------------------------------------------------------------- token form
-// Persistent CTAs over output tiles of tokens x features.
-__global__ void __launch_bounds__(kThreads, 1)
-    gemm_token_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                      const GemmArgs a) {
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                               ~uintptr_t(1023));
-    __shared__ uint64_t full_bar[MAX_STAGES], empty_bar[MAX_STAGES];
-    __shared__ uint64_t tfull_bar[2], tempty_bar[2], drain_bar;
-    __shared__ uint32_t tmem_base_s;
-    __shared__ int abort_s;
-
-    const int warp = threadIdx.x >> 5;
-    const int lane = threadIdx.x & 31;
-    int32_t* status = a.ep.status;
-
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < a.stages; ++s) {
-            mbar_init(&full_bar[s], 1);
-            mbar_init(&empty_bar[s], 1);
-        }
-        for (int b = 0; b < 2; ++b) {
-            mbar_init(&tfull_bar[b], 1);
-            mbar_init(&tempty_bar[b], 128);
-        }
-        mbar_init(&drain_bar, 1);
-        abort_s = 0;
-        fence_mbar_init();
-    }
-    if (warp == 0 && lane == 0) {
-        tma_prefetch_desc(&tmA);
-        tma_prefetch_desc(&tmB);
-    }
-    if (warp == 1) {
-        tmem_alloc(&tmem_base_s, a.tmem_cols);
-        tmem_relinquish();
-    }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    pdl_wait();
-    pdl_trigger();
-    const uint32_t tmem = tmem_base_s;
-
-    if (warp == 0) {
-        if (lane == 0) {
-            // ------------------------------------------------ TMA producer
-            int stage = 0;
-            uint32_t phase = 0;
-            uint32_t issued[MAX_STAGES];
-            for (int s = 0; s < MAX_STAGES; ++s) issued[s] = 0;
-            bool ok = true;
-            for (int u = blockIdx.x; u < a.units && ok; u += gridDim.x) {
-                int a_blk, b_blk, kb0, kb1;
-                unit_coords(a, u, a_blk, b_blk, kb0, kb1);
-                for (int kb = kb0; kb < kb1; ++kb) {
-                    if (!mbar_wait_bounded(&empty_bar[stage], phase ^ 1, &abort_s, status)) {
-                        ok = false;
-                        break;
-                    }
-                    uint8_t* sa = smem + (size_t)stage * a.stage_bytes;
-                    uint8_t* sb = sa + a.a_bytes;
-                    mbar_arrive_expect_tx(&full_bar[stage], a.stage_bytes);
-                    tma_load_2d(sa, &tmA, kb * BK, a_blk * BM, &full_bar[stage]);
-                    tma_load_2d(sb, &tmB, kb * BK, b_blk * a.bn, &full_bar[stage]);
-                    for (int s = 0; s < MAX_STAGES; ++s) issued[s] += (s == stage);
-                    if (++stage == a.stages) {
-                        stage = 0;
-                        phase ^= 1;
-                    }
-                }
-            }
-            if (abort_s) {
-                // let loads already in flight land before the CTA's shared memory goes away
-                volatile int never = 0;
-                for (int s = 0; s < a.stages; ++s)
-                    if (issued[s]) mbar_wait_bounded(&full_bar[s], (issued[s] - 1) & 1, &never, nullptr);
-            }
-        }
-        __syncwarp();
-    } else if (warp == 1) {
-        if (lane == 0) {
-            // ------------------------------------------------ MMA issuer
-            const uint32_t idesc = umma_idesc_bf16(BM, a.bn);
-            int stage = 0;
-            uint32_t phase = 0;
-            int local = 0;
-            bool ok = true;
-            for (int u = blockIdx.x; u < a.units && ok; u += gridDim.x, ++local) {
-                int a_blk, b_blk, kb0, kb1;
-                unit_coords(a, u, a_blk, b_blk, kb0, kb1);
-                const int buf = local & 1;
-                const uint32_t accp = (local >> 1) & 1;
-                if (!mbar_wait_bounded(&tempty_bar[buf], accp ^ 1, &abort_s, status)) break;
-                tc_fence_after();
-                const uint32_t d_tmem = tmem + (uint32_t)(buf * a.bn);
-                for (int kb = kb0; kb < kb1; ++kb) {
-                    if (!mbar_wait_bounded(&full_bar[stage], phase, &abort_s, status)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    const uint32_t sa = smem_u32(smem + (size_t)stage * a.stage_bytes);
-                    const uint32_t sb = sa + a.a_bytes;
-                    const uint64_t da = umma_desc_sw128(sa);
-                    const uint64_t db = umma_desc_sw128(sb);
-#pragma unroll
-                    for (int kk = 0; kk < BK / UK; ++kk) {
-                        // advance the start address by kk * 32 bytes inside the swizzled row
-                        tc_mma_bf16(d_tmem, da + (uint64_t)(kk * 2), db + (uint64_t)(kk * 2), idesc,
-                                    (kb > kb0 || kk > 0) ? 1u : 0u);
-                    }
-                    tc_commit(&empty_bar[stage]);
-                    if (++stage == a.stages) {
-                        stage = 0;
-                        phase ^= 1;
-                    }
-                }
-                if (ok) tc_commit(&tfull_bar[buf]);
-            }
-            // all MMAs issued by this thread must be complete before TMEM is freed
-            tc_commit(&drain_bar);
-            volatile int never = 0;
-            mbar_wait_bounded(&drain_bar, 0, &never, status);
-        }
-        __syncwarp();
-    } else {
-        // ---------------------------------------------------- epilogue warps
-        const int q = warp & 3;
-        const int r = q * 32 + lane;             // TMEM lane = token row of the tile
-        const uint32_t lane_base = (uint32_t)(q * 32) << 16;
-        int local = 0;
-        for (int u = blockIdx.x; u < a.units; u += gridDim.x, ++local) {
-            int a_blk, b_blk, kb0, kb1;
-            unit_coords(a, u, a_blk, b_blk, kb0, kb1);
-            const int buf = local & 1;
-            const uint32_t accp = (local >> 1) & 1;
-            if (!mbar_wait_bounded(&tfull_bar[buf], accp, &abort_s, status)) break;
-            tc_fence_after();
-            const uint32_t taddr = tmem + lane_base + (uint32_t)(buf * a.bn);
-            const int t = a_blk * BM + r;
-            const bool row_ok = t < a.tokens;
-            TokenSlot ts{-1, -1};
-            if (a.ep.kind == EPI_QKV && row_ok) ts = token_slot(a.ep, t);
-            for (int c = 0; c < a.bn; c += 16) {
-                const int n0 = b_blk * a.bn + c;
-                if (n0 >= a.n) break;
-                float v[16];
-                tmem_ld16(taddr + (uint32_t)c, v);
-                epi_token_chunk(a.ep, t, row_ok, n0, a.n, ts, v);
-            }
-            tc_fence_before();
-            mbar_arrive(&tempty_bar[buf]);
-        }
-    }
-
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    if (warp == 1) tmem_dealloc(tmem, a.tmem_cols);
-}
-
-// ---------------------------------------------------------------- token form, CTA pairs
 // A cluster of two CTAs computes 256 x 256 output tiles with tcgen05.mma.cta_group::2:
 // CTA r stages rows [128 r, 128 r + 128) of the tile's A block and rows
 // [128 r, 128 r + 128) of its B block (256 output columns), the even CTA issues the
@@ -688,7 +518,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 LL_DEVINL int sk_begin(int c, int W, int P) { return (int)((long long)c * W / P); }
 LL_DEVINL int sk_owner(int w, int W, int P) { return (int)(((long long)(w + 1) * P - 1) / W); }
 
-constexpr int kPartialFloats = kSwapMaxTokens * BM;   // one partial tile: [tokens][128] float32
 constexpr int kMaxWeightCtas = 160;                   // scratch bound: CTAs of one launch
 constexpr int kMinItersPerCta = 4;
 
@@ -767,12 +596,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     pdl_wait();
     pdl_trigger();
     if (warp >= 2 && a.ep.kind == EPI_QKV) {
-        // each token's position and cache row, once per CTA (the tokens are few)
-        const int et = threadIdx.x - 64;
-        if (et < a.tokens) {
-            TokenSlot ts = token_slot(a.ep, et);
-            tok_pos_s[et] = ts.pos;
-            tok_row_s[et] = ts.kv_row;
+        // each token's position and cache row, once per CTA
+        for (int t = threadIdx.x - 64; t < a.tokens; t += 128) {
+            TokenSlot ts = token_slot(a.ep, t);
+            tok_pos_s[t] = ts.pos;
+            tok_row_s[t] = ts.kv_row;
         }
     }
     tc_fence_before();
@@ -901,7 +729,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             } else {
                 // a piece of the tile: the CTA's first segment goes to slot 0, its last to slot 1
-                float* mine = a.partials + ((size_t)cta * 2 + (ws == w0 ? 0 : 1)) * kPartialFloats;
+                float* mine = a.partials + ((size_t)cta * 2 + (ws == w0 ? 0 : 1)) * T * BM;
                 for (int c = 0; c < a.bn; c += 16) {
                     float v[16];
                     tmem_ld16(taddr + (uint32_t)c, v);
@@ -987,7 +815,7 @@ __global__ void __launch_bounds__(BM)
         for (int u = 0; u < 4; ++u) {
             const int cc = min(c0 + u, c_last);
             const int slot = (sk_begin(cc, W, P) / nkb == tile) ? 0 : 1;
-            const float* pp = a.partials + ((size_t)cc * 2 + slot) * kPartialFloats + (size_t)t0 * BM + r;
+            const float* pp = a.partials + ((size_t)cc * 2 + slot) * T * BM + (size_t)t0 * BM + r;
 #pragma unroll
             for (int j = 0; j < 16; ++j)
                 part[u][j] = (c0 + u <= c_last && j < cnt) ? __ldcg(pp + (size_t)j * BM) : 0.f;
@@ -1044,13 +872,23 @@ int weight_ctas(int tiles, int num_kb, int sms) {
     return std::max(1, std::min({sms, kMaxWeightCtas, (W + kMinItersPerCta - 1) / kMinItersPerCta}));
 }
 
+// Weight form for decode-sized calls (<= 64 tokens), and for up to 256 tokens when
+// the 256 x 256 pair tiles would leave most SMs idle (fewer than one tile per four
+// SMs: short prefill chunks through narrow projections); else pair tiles, which
+// reuse both operands.
+bool use_weight_form(int tokens, int n, int sms) {
+    if (tokens <= 64) return true;
+    if (tokens > kSwapMaxTokens) return false;
+    return ceil_div(tokens, 2 * BM) * ceil_div(n, kPairBN) * 4 < sms;
+}
+
 Plan make_plan(int tokens, int n, int k, int sms) {
     Plan p{};
-    p.swap = tokens <= kSwapMaxTokens;
+    p.swap = use_weight_form(tokens, n, sms);
     p.num_kb = ceil_div(k, BK);
     p.a_bytes = BM * BK * 2;
     if (!p.swap) {
-        p.bn = kTokenFormBN;
+        p.bn = kPairBN;
         p.tiles_m = ceil_div(tokens, BM);
         p.tiles_n = ceil_div(n, p.bn);
         p.stage_bytes = p.a_bytes + p.bn * BK * 2;
@@ -1109,12 +947,15 @@ int device_sm_count() {
 void gemm_scratch_need(int tokens, int n, int k, size_t* partial_bytes, int* counters) {
     (void)n;
     (void)k;
-    *partial_bytes = tokens > kSwapMaxTokens ? 0 : gemm_partial_bound_bytes();   // token form: no split K
+    *partial_bytes = tokens > kSwapMaxTokens ? 0 : gemm_partial_bound_bytes(tokens);  // token form: none
     *counters = 0;
 }
 
-// two partial tiles per CTA (its first and its last segment)
-size_t gemm_partial_bound_bytes() { return (size_t)kMaxWeightCtas * 2 * kPartialFloats * sizeof(float); }
+// Two partial tiles [tokens][128] float32 per CTA (its first and its last
+// segment), for any call of at most max_tokens tokens.
+size_t gemm_partial_bound_bytes(int max_tokens) {
+    return (size_t)kMaxWeightCtas * 2 * (size_t)std::min(max_tokens, kSwapMaxTokens) * BM * sizeof(float);
+}
 
 int gemm_counter_bound(int n) {
     (void)n;
@@ -1148,7 +989,7 @@ cudaError_t launch_gemm(const GemmProblem& pr, cudaStream_t stream) {
         ok = make_tmap(&tmA, pr.w, pr.k, pr.n, BM) && make_tmap(&tmB, pr.act, pr.k, pr.tokens, p.bn);
     }
     if (!ok) return cudaErrorInvalidValue;
-    if (!p.swap && pr.tokens > BM) {
+    if (!p.swap) {
         // CTA pairs: 256 x 256 tiles, each CTA stages 128 rows of A and of B per stage
         a.tiles_m = ceil_div(pr.tokens, 2 * BM);
         a.tiles_n = ceil_div(pr.n, kPairBN);
@@ -1179,24 +1020,6 @@ cudaError_t launch_gemm(const GemmProblem& pr, cudaStream_t stream) {
         if (e != cudaSuccess) return record(e, "gemm_token2_kernel launch");
         return record(cudaGetLastError(), "gemm_token2_kernel launch");
     }
-    if (!p.swap) {
-        static int configured_smem = 0;
-        if ((int)p.smem_bytes > configured_smem) {
-            // dynamic + static shared memory must fit the per-block opt-in limit
-            cudaError_t e = cudaFuncSetAttribute(gemm_token_kernel,
-                                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                 (int)p.smem_bytes);
-            if (e != cudaSuccess) return record(e, "cudaFuncSetAttribute(gemm_token_kernel)");
-            configured_smem = (int)p.smem_bytes;
-        }
-        const int grid = std::min(p.units, sms * p.ctas_per_sm);
-        trace_before("gemm_tc", stream);
-        cudaError_t e = launch_pdl(gemm_token_kernel, dim3(grid), dim3(kThreads), p.smem_bytes, stream, 1,
-                                   tmA, tmB, a);
-        trace_after(stream);
-        if (e != cudaSuccess) return record(e, "gemm_token_kernel launch");
-        return record(cudaGetLastError(), "gemm_token_kernel launch");
-    }
     static int configured_smem_w = 0;
     if ((int)p.smem_bytes > configured_smem_w) {
         cudaError_t e = cudaFuncSetAttribute(gemm_weight_kernel,
@@ -1205,7 +1028,7 @@ cudaError_t launch_gemm(const GemmProblem& pr, cudaStream_t stream) {
         if (e != cudaSuccess) return record(e, "cudaFuncSetAttribute(gemm_weight_kernel)");
         configured_smem_w = (int)p.smem_bytes;
     }
-    if (!pr.partials || pr.partial_bytes < gemm_partial_bound_bytes()) {
+    if (!pr.partials || pr.partial_bytes < (size_t)p.units * 2 * pr.tokens * BM * sizeof(float)) {
         set_last_error("launch_gemm", "weight form needs split-K scratch");
         return cudaErrorInvalidValue;
     }

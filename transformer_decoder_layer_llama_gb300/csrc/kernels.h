@@ -87,7 +87,7 @@ struct GemmProblem {
 // Scratch the GEMM may need for a problem of this shape (bytes of float
 // partials, number of tile counters).
 void gemm_scratch_need(int tokens, int n, int k, size_t* partial_bytes, int* counters);
-size_t gemm_partial_bound_bytes();      // upper bound over all shapes with tokens <= 64
+size_t gemm_partial_bound_bytes(int max_tokens);   // bound over all calls of <= max_tokens tokens
 int gemm_counter_bound(int n);          // counters needed for an output of n features
 
 cudaError_t launch_gemm(const GemmProblem& p, cudaStream_t stream);
