@@ -49,13 +49,14 @@ L2_FLUSH_BYTES = 256 << 20
 NCU_TRAFFIC = {
     # gemm_token2_kernel (CTA pairs), 7B prefill layer: mean over its 4 launches (QKV, O, gate/up, down)
     "prefill_gemm": {"file": "transformer_decoder_layer_llama_gb300/csrc/gemm_tc.cu",
-                     "sha256": "02ba661f13b8b3b313e90d65ca970d7a54ea306515e776b1182c4b0bb8ad5da9", "bytes_per_launch": 168.74e6},
+                     "sha256": "1e5795240cc47683a8522595ef79f5adbf32b913e647d23a1419c924284416a1", "bytes_per_launch": 168.4e6},
     # attn_decode_split_kernel, 7B decode (batch 64)
     "llama2_7b_decode_attn": {"file": "transformer_decoder_layer_llama_gb300/csrc/attn.cu",
-                              "sha256": "d6df5b316556de7966cdfa479055e63d410d30d157f4291db69131c87f95cff8", "bytes_per_launch": 2246.0e6},
-    # gemm_weight_kernel, 70B decode: mean over its 4 launches
+                              "sha256": "ecb69701119c45ebbecdab0be178b44a481fd38acaff8f983f50249f90f93051", "bytes_per_launch": 2246.1e6},
+    # one weight-form GEMM (gemm_weight_kernel + gemm_weight_fixup_kernel), 70B decode:
+    # mean over the layer's 4 GEMMs
     "llama70b_gqa_decode_gemm": {"file": "transformer_decoder_layer_llama_gb300/csrc/gemm_tc.cu",
-                                 "sha256": "02ba661f13b8b3b313e90d65ca970d7a54ea306515e776b1182c4b0bb8ad5da9", "bytes_per_launch": 429.7e6},
+                                 "sha256": "1e5795240cc47683a8522595ef79f5adbf32b913e647d23a1419c924284416a1", "bytes_per_launch": 433.1e6},
 }
 
 
