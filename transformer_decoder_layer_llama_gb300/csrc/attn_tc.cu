@@ -107,8 +107,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     __shared__ uint32_t tile_ok_s[kMaxKeyTiles];   // per key tile: bit c = 16-key chunk c has a valid block
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int b = blockIdx.z, h = blockIdx.y;
-    const int mt = gridDim.x - 1 - blockIdx.x;       // heavy (late) query tiles first
+    // CTAs are dispatched x-fastest: every head's heaviest (latest) query tile first,
+    // then the next heaviest, ... (longest-first keeps the SMs evenly loaded)
+    const int b = blockIdx.z, h = blockIdx.x;
+    const int mt = gridDim.y - 1 - blockIdx.y;
     const int G = a.n_heads / a.n_kv_heads;
     const int hk = h / G;
     const int row0 = mt * kQT;
@@ -466,7 +468,7 @@ cudaError_t prefill_tc_for(const AttnPrefillArgs& a, cudaStream_t stream) {
         !make_tmap_bf16_sw128(&tmK, a.k_pool, D, rows, (uint32_t)args.box_rows) ||
         !make_tmap_bf16_sw128(&tmV, a.v_pool, D, rows, (uint32_t)args.box_rows))
         return cudaErrorInvalidValue;
-    dim3 grid((a.seq_len + kQT - 1) / kQT, a.n_heads, a.batch);
+    dim3 grid(a.n_heads, (a.seq_len + kQT - 1) / kQT, a.batch);
     trace_before("attn_prefill", stream);
     cudaError_t e = launch_pdl(attn_prefill_tc_kernel<D>, grid, dim3(kTcThreads), smem, stream, 1, tmQ, tmK,
                                tmV, args);
