@@ -331,25 +331,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             // one pass over the half row of S: raw scores in registers, masked (-inf) only
             // where this half touches the diagonal or an invalid block
             const bool full = chunk_ok == (1u << (HK / 16)) - 1u && kbase + HK - 1 <= my_pos;
+            static_assert(HK == 64, "one 64-column TMEM load per half row");
             float sv[HK];
+            if (got_s) {
+                tmem_ld64(tbuf + (uint32_t)(half * HK), sv);   // the half row, one wait
+            } else {
 #pragma unroll
-            for (int c = 0; c < HK; c += 16) {
-                float v[16];
-                if (got_s) {
-                    tmem_ld16(tbuf + (uint32_t)(half * HK + c), v);
-                } else {
+                for (int i = 0; i < HK; ++i) sv[i] = 0.f;
+            }
+            if (!full) {
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) v[i] = 0.f;
-                }
-                if (full) {
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) sv[c + i] = v[i];
-                } else {
-                    const bool cok = (chunk_ok >> (c >> 4)) & 1u;
-#pragma unroll
-                    for (int i = 0; i < 16; ++i)
-                        sv[c + i] = (cok && kbase + c + i <= my_pos) ? v[i] : -INFINITY;
-                }
+                for (int i = 0; i < HK; ++i)
+                    if (!(((chunk_ok >> (i >> 4)) & 1u) && kbase + i <= my_pos)) sv[i] = -INFINITY;
             }
             float mx = -INFINITY;
 #pragma unroll
@@ -387,19 +380,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             // P = exp2(s - base) as hi + lo BF16 parts, written over S in TMEM:
             // hi in columns [0, 64) and lo in [64, 128) of the buffer, two keys per column
             float rs = 0.f;
+            {
+                uint32_t hi[HK / 2], lo[HK / 2];
 #pragma unroll
-            for (int c = 0; c < HK; c += 32) {
-                uint32_t hi[16], lo[16];
-#pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const float p0 = ex2_approx(fmaf(sv[c + 2 * i], sl2, -base));
-                    const float p1 = ex2_approx(fmaf(sv[c + 2 * i + 1], sl2, -base));
+                for (int i = 0; i < HK / 2; ++i) {
+                    const float p0 = ex2_approx(fmaf(sv[2 * i], sl2, -base));
+                    const float p1 = ex2_approx(fmaf(sv[2 * i + 1], sl2, -base));
                     rs += p0 + p1;
                     split_bf16x2(p0, p1, hi[i], lo[i]);
                 }
-                const uint32_t col = (uint32_t)((half * HK + c) >> 1);
-                tmem_st16(tbuf + col, hi);
-                tmem_st16(tbuf + 64u + col, lo);
+                // the half row's 32 hi and 32 lo columns, one wait
+                const uint32_t col = (uint32_t)((half * HK) >> 1);
+                tmem_st32x2(tbuf + col, hi, tbuf + 64u + col, lo);
             }
             l += rs;
             tc_fence_before();
