@@ -50,6 +50,8 @@ def assert_close_fullsize(got, ref, name=""):
     assert np.isfinite(got).all(), name
     err = np.abs(got - ref)
     frac = float((err > ATOL + RTOL * np.abs(ref)).mean())
+    print(f"{name}: {frac:.2e} outside {ATOL}+{RTOL}|ref|, rms error {float(np.sqrt((err ** 2).mean())):.2e}, "
+          f"worst {float((err / (FULL_HARD_ATOL + RTOL * np.abs(ref))).max()):.2f} of the hard bound")
     assert frac <= FULL_MAX_FRAC_OUTSIDE, (
         f"{name}: {frac:.2e} of elements outside {ATOL}+{RTOL}|ref| (allowed {FULL_MAX_FRAC_OUTSIDE})")
     assert_close(got, ref, name + " [hard bound]", atol=FULL_HARD_ATOL, rtol=RTOL)
