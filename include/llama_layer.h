@@ -120,6 +120,30 @@ int ll_pack_weights(const ll_config* cfg, const ll_weights* w, void* packed, siz
  * seq_len; decode: batch) and block tables up to max_blocks wide. */
 size_t ll_workspace_size(const ll_config* cfg, int32_t max_tokens, int32_t max_blocks);
 
+/* Checkpoints of the fused layer (page "ATB fused-operator matrix and KV-cache
+ * management", section on the engineering limits of fusion granularity: besides
+ * the step-by-step and fully fused execution modes it names a fused mode with
+ * verification checkpoints at key nodes, so that a wrong result can be traced to
+ * one step).  A layer call leaves the output of every kernel of its chain in the
+ * workspace; these are their byte offsets from the workspace start, for a
+ * workspace sized by ll_workspace_size(cfg, max_tokens, max_blocks).  After a call
+ * over T tokens (and until the next call on the same workspace), row t < T of:
+ *   x_hat  BF16    [T][hidden]           RMSNorm(x) * g_attn
+ *   q      BF16    [T][n_heads*head_dim] q after RoPE, heads in order, element i of a
+ *                                        head at i (RoPE pairs i, i + head_dim/2)
+ *   o      BF16    [T][n_heads*head_dim] attention output
+ *   h      float32 [T][hidden]           x + o W_o^T
+ *   h_hat  BF16    [T][hidden]           RMSNorm(h) * g_ffn
+ *   a      BF16    [T][intermediate]     SiLU(x_hat2 W_gate^T) * (x_hat2 W_up^T)
+ * The new tokens' K and V are in the KV pool at their slots.  Host-only; no GPU
+ * work.  Returns LL_ERR_INVALID_ARG for an invalid cfg or sizes. */
+typedef struct {
+    size_t x_hat, q, o, h, h_hat, a;
+} ll_checkpoints;
+
+int ll_workspace_checkpoints(const ll_config* cfg, int32_t max_tokens, int32_t max_blocks,
+                             ll_checkpoints* out);
+
 /* Prefill: x BF16 [batch*seq_len, hidden], token-major; token t belongs to
  * sequence t / seq_len and sits at positions[t] (int32 [batch*seq_len]).
  * Writes every token's K and V (after RoPE on K) into the pool at

@@ -63,3 +63,24 @@ def test_python_binding_refuses_cpu_tensors():
     x = torch.zeros(4, 256, dtype=torch.bfloat16)
     with pytest.raises(ValueError):
         api.linear(x, torch.zeros(16, 256, dtype=torch.bfloat16))
+
+
+def test_workspace_checkpoints_lie_inside_the_workspace():
+    """The fused layer's checkpoints (one region per kernel output) are disjoint,
+    16-byte aligned, hold max_tokens rows each, and fit the workspace size."""
+    for name in ("tiny_gqa", "llama2_7b_decode", "llama70b_gqa_decode"):
+        d = synth.WORKLOADS[name].dims
+        cfg = api.make_config(d, max_position=4096)
+        T, mb = 96, 40
+        total = api.workspace_size(cfg, T, mb)
+        out = api.ll_checkpoints()
+        assert api.lib.ll_workspace_checkpoints(ctypes.byref(cfg), T, mb, ctypes.byref(out)) == 0
+        nq = d.n_heads * d.head_dim
+        widths = {"x_hat": d.hidden * 2, "q": nq * 2, "o": nq * 2, "h": d.hidden * 4,
+                  "h_hat": d.hidden * 2, "a": d.intermediate * 2}
+        spans = sorted((getattr(out, k), getattr(out, k) + T * w) for k, w in widths.items())
+        for (a0, a1), (b0, _) in zip(spans, spans[1:]):
+            assert a1 <= b0
+        assert all(a0 % 16 == 0 for a0, _ in spans)
+        assert spans[-1][1] <= total
+        assert api.lib.ll_workspace_checkpoints(ctypes.byref(cfg), 0, mb, ctypes.byref(out)) == api.LL_ERR_INVALID_ARG

@@ -215,3 +215,66 @@ def test_weight_form_linear_repeatable(m, n, k):
     idx = torch.arange(0, n, 997)
     ref = f64(x.cpu()) @ f64(w.cpu()[idx]).T
     assert_close(f64(y1.cpu()[:, idx]), ref, f"linear {m}x{n}x{k} sampled", atol=2e-3, rtol=8e-3)
+
+
+@pytest.mark.parametrize("ctx0,q_len", [((17, 130, 64), 4), ((1, 255, 40), 3), ((300, 5), 16)])
+def test_multi_token_decode_over_ragged_cached_contexts(ctx0, q_len):
+    """Several new tokens per request appended after cached contexts of different lengths
+    (a prefill chunk per request at its own position offset): each token attends to its
+    request's cached prefix plus the new tokens up to itself."""
+    B = len(ctx0)
+    wl = synth.WORKLOADS["tiny_gqa"]
+    d = wl.dims
+    W = synth.make_weights(d, wl.w_std, seed=71)
+    lens = [c + q_len for c in ctx0]
+    table, nb = synth.make_block_table(lens, d.block_size, seed=72, extra_blocks=3)
+    kp, vp = synth.make_pool(nb, d, seed=73)            # the cached prefix: N(0, 1) K/V
+    cfg = api.make_config(d, max_position=max(lens) + 1)
+    packed = api.pack_weights(cfg, {k: v.to(DEV) for k, v in W.items()})
+    x = synth.make_x(B * q_len, d.hidden, seed=74)
+    pos = torch.cat([torch.arange(c, c + q_len, dtype=torch.int32) for c in ctx0])
+    kpd, vpd = kp.to(DEV), vp.to(DEV)
+    status = api.new_status()
+    y = api.layer_prefill(cfg, packed, x.to(DEV), pos.to(DEV), B, q_len, kpd, vpd, table.to(DEV), status=status)
+    torch.cuda.synchronize()
+    ko, vo = bits(kp), bits(vp)
+    y_ref = O.layer_prefill(d, {k: f64(v) for k, v in W.items()}, f64(x), pos.numpy(), B, q_len, ko, vo,
+                            table.numpy())
+    assert int(status.item()) == 0
+    assert_close(f64(y), y_ref, f"multi-token decode {ctx0} + {q_len}")
+    np.testing.assert_array_equal(bits(kpd) == bits(kp), ko == bits(kp))   # only the new slots changed
+
+
+@pytest.mark.parametrize("mode", ["prefill", "decode"])
+def test_checkpoints_match_oracle_stage_by_stage(mode):
+    """Each kernel output the fused layer leaves in its workspace (x_hat, q after RoPE,
+    attention o, residual h, h_hat, SwiGLU a) against the oracle's value of that stage,
+    so that a wrong layer output can be traced to one kernel."""
+    wl, d, B, S, W, Wn, table, kp, vp, cfg, packed = _tiny_setup(seed=81, S=40, B=2, steps=1)
+    kpd, vpd, td = kp.to(DEV), vp.to(DEV), table.to(DEV)
+    ko, vo = bits(kp), bits(vp)
+    want = {}
+    if mode == "prefill":
+        T = B * S
+        x = synth.make_x(T, d.hidden, seed=82)
+        pos = synth.prefill_positions(B, S)
+        ws = api.new_workspace(cfg, T, table.shape[1])
+        api.layer_prefill(cfg, packed, x.to(DEV), pos.to(DEV), B, S, kpd, vpd, td, workspace=ws)
+        O.layer_prefill(d, Wn, f64(x), pos.numpy(), B, S, ko, vo, table.numpy(), want=want)
+    else:
+        # a prefill fills the cache, then one decode step is checked stage by stage
+        x = synth.make_x(B * S, d.hidden, seed=83)
+        pos = synth.prefill_positions(B, S)
+        api.layer_prefill(cfg, packed, x.to(DEV), pos.to(DEV), B, S, kpd, vpd, td)
+        O.layer_prefill(d, Wn, f64(x), pos.numpy(), B, S, ko, vo, table.numpy())
+        T = B
+        xd = synth.make_x(B, d.hidden, seed=84)
+        ctx = torch.full((B,), S + 1, dtype=torch.int32)
+        ws = api.new_workspace(cfg, T, table.shape[1])
+        api.layer_decode_step(cfg, packed, xd.to(DEV), kpd, vpd, td, ctx.to(DEV), workspace=ws)
+        O.layer_decode_step(d, Wn, f64(xd), ko, vo, table.numpy(), ctx.numpy(), want=want)
+    torch.cuda.synchronize()
+    cp = api.checkpoints(cfg, ws, T, table.shape[1], T)
+    for name, ref in (("x_hat", want["xh"]), ("q", want["q"].reshape(T, -1)), ("o", want["o"].reshape(T, -1)),
+                      ("h", want["h"]), ("h_hat", want["hh"]), ("a", want["a"])):
+        assert_close(f64(cp[name]), ref, f"{mode} checkpoint {name}")

@@ -31,6 +31,7 @@ EXPORTED = [
     "ll_attention_workspace_size", "ll_paged_attention_decode", "ll_linear_workspace_size",
     "ll_linear", "ll_device_sm_count", "ll_trace_begin", "ll_trace_end", "ll_trace_elapsed_ms",
     "ll_trace_name", "ll_paged_attention_decode_noalloc", "ll_selftest_bounded_wait",
+    "ll_workspace_checkpoints",
 ]
 
 
@@ -50,6 +51,11 @@ class ll_weights(ctypes.Structure):
 
 class ll_kv_pool(ctypes.Structure):
     _fields_ = [("k", ctypes.c_void_p), ("v", ctypes.c_void_p), ("num_blocks", ctypes.c_int32)]
+
+
+class ll_checkpoints(ctypes.Structure):
+    _fields_ = [("x_hat", ctypes.c_size_t), ("q", ctypes.c_size_t), ("o", ctypes.c_size_t),
+                ("h", ctypes.c_size_t), ("h_hat", ctypes.c_size_t), ("a", ctypes.c_size_t)]
 
 
 def _load():
@@ -82,6 +88,7 @@ def _load():
         "ll_trace_elapsed_ms": (ctypes.c_float, [I32]),
         "ll_trace_name": (ctypes.c_char_p, [I32]),
         "ll_selftest_bounded_wait": (ctypes.c_int, [I32, P, P, P]),
+        "ll_workspace_checkpoints": (ctypes.c_int, [cfgp, I32, I32, ctypes.POINTER(ll_checkpoints)]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -174,6 +181,29 @@ def new_workspace(cfg, max_tokens, max_blocks, device=None):
     if n == 0:
         raise LayerError("ll_workspace_size", LL_ERR_INVALID_ARG)
     return torch.empty(n, dtype=torch.uint8, device=device or "cuda")
+
+
+def checkpoints(cfg: ll_config, workspace: torch.Tensor, max_tokens: int, max_blocks: int, tokens: int) -> dict:
+    """Views into `workspace` (allocated by new_workspace(cfg, max_tokens, max_blocks)) of the
+    intermediates the last layer call over `tokens` tokens left there: x_hat, q, o, h_hat, a
+    (BF16) and h (float32), each [tokens, features].  Read them after the call has finished
+    on its stream; the next call on the workspace overwrites them."""
+    out = ll_checkpoints()
+    rc = lib.ll_workspace_checkpoints(ctypes.byref(cfg), int(max_tokens), int(max_blocks), ctypes.byref(out))
+    if rc != 0:
+        raise LayerError("ll_workspace_checkpoints", rc)
+    if not 0 < tokens <= max_tokens:
+        raise ValueError("tokens must be in 1..max_tokens")
+    nq = cfg.n_heads * cfg.head_dim
+    shapes = {"x_hat": (cfg.hidden, torch.bfloat16), "q": (nq, torch.bfloat16), "o": (nq, torch.bfloat16),
+              "h": (cfg.hidden, torch.float32), "h_hat": (cfg.hidden, torch.bfloat16),
+              "a": (cfg.intermediate, torch.bfloat16)}
+    views = {}
+    for name, (width, dt) in shapes.items():
+        off = getattr(out, name)
+        nbytes = tokens * width * torch.finfo(dt).bits // 8
+        views[name] = workspace[off:off + nbytes].view(dt).view(tokens, width)
+    return views
 
 
 def _pool(k_pool, v_pool):

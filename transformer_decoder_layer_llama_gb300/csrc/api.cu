@@ -545,6 +545,22 @@ int ll_paged_attention_decode(const void* q, const ll_kv_pool* pool, const int32
     return cuda_rc(ll::launch_attn_decode(at, static_cast<cudaStream_t>(stream)));
 }
 
+int ll_workspace_checkpoints(const ll_config* cfg, int32_t max_tokens, int32_t max_blocks,
+                             ll_checkpoints* out) {
+    ll::clear_last_error();
+    if (!out || max_tokens <= 0 || max_blocks <= 0) return LL_ERR_INVALID_ARG;
+    const int rc = config_supported(cfg);
+    if (rc != LL_OK) return rc;
+    const WsLayout L = ws_layout(cfg, max_tokens, max_blocks);
+    out->x_hat = L.xh;
+    out->q = L.q;
+    out->o = L.o;
+    out->h = L.h;
+    out->h_hat = L.hh;
+    out->a = L.a;
+    return LL_OK;
+}
+
 size_t ll_linear_workspace_size(int32_t m, int32_t n, int32_t k) {
     if (m <= 0 || n <= 0 || k <= 0) return 0;
     size_t pb = 0;
