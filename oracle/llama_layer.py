@@ -58,7 +58,8 @@ rounding (pinned in tests).
 Pools: a K pool and a V pool, each [num_blocks, n_kv_heads, block_size,
 head_dim].  A uint16 pool holds BF16 bit patterns; a float64 pool holds exact
 values.  block_table[b, j] is the physical block of logical block j of
-sequence b (-1 = unused); slot = block * block_size + offset.
+sequence b (-1 = unused); slot = block * block_size + offset.  A QuantPool holds
+INT8 codes with one float32 scale per token and head (see quantize_int8_rows).
 
 Every function here is pinned in tests/test_oracle.py against closed forms, invariants,
 library routines or the figures the pages print.
@@ -236,8 +237,41 @@ def slot_of(block_table, b, pos, block_size):
     return blk * block_size + pos % block_size
 
 
+def quantize_int8_rows(x):
+    """INT8 codes and float32 scales of the rows of x (last axis) [paging] section
+    "KV Cache quantisation": per-token granularity, each token's K (or V) vector
+    with its own float32 scale.  Reading (symmetric, absmax): scale = max|x| / 127,
+    code = round-half-even(x / scale) clipped to [-127, 127]; a row of zeros has
+    scale 0 and codes 0.  The codes are integers decided by floating point, so they
+    are computed in float32, the kernel's precision, with IEEE division."""
+    xf = np.asarray(x, np.float32)
+    amax = np.abs(xf).max(axis=-1)
+    scale = (amax / np.float32(127.0)).astype(np.float32)
+    safe = np.where(scale > 0, scale, np.float32(1.0)).astype(np.float32)
+    codes = np.rint(xf / safe[..., None]).astype(np.float32)
+    codes = np.clip(codes, -127, 127)
+    codes[scale == 0] = 0
+    return codes.astype(np.int8), scale
+
+
+class QuantPool:
+    """An INT8 KV pool: codes int8 [num_blocks, heads, block_size, d] and float32
+    scales [num_blocks, heads, block_size] (one per token and head); a row reads
+    back as codes * scale."""
+
+    def __init__(self, codes, scales):
+        self.codes = codes
+        self.scales = scales
+        self.shape = codes.shape
+        self.dtype = np.int8
+
+
 def _pool_store(pool, blk, off, vals):
-    if pool.dtype == np.uint16:
+    if isinstance(pool, QuantPool):
+        codes, scale = quantize_int8_rows(vals)        # vals [heads, d]: one scale per head
+        pool.codes[blk, :, off, :] = codes
+        pool.scales[blk, :, off] = scale
+    elif pool.dtype == np.uint16:
         pool[blk, :, off, :] = bf16_bits(bf16_round(vals))
     else:
         pool[blk, :, off, :] = vals
@@ -246,8 +280,12 @@ def _pool_store(pool, blk, off, vals):
 def _pool_load(pool, blks, n):
     """Contiguous [heads, n, d] float64 view of the first n positions held in blocks `blks`."""
     bs = pool.shape[2]
-    parts = [pool[int(bk)] for bk in blks[: -(-n // bs)]]
-    raw = np.concatenate(parts, axis=1)[:, :n, :]
+    used = [int(bk) for bk in blks[: -(-n // bs)]]
+    if isinstance(pool, QuantPool):
+        codes = np.concatenate([pool.codes[bk] for bk in used], axis=1)[:, :n, :]
+        scales = np.concatenate([pool.scales[bk] for bk in used], axis=1)[:, :n]
+        return codes.astype(np.float64) * scales.astype(np.float64)[:, :, None]
+    raw = np.concatenate([pool[bk] for bk in used], axis=1)[:, :n, :]
     return bf16_value(raw) if pool.dtype == np.uint16 else np.asarray(raw, np.float64)
 
 

@@ -390,3 +390,60 @@ def test_layer_two_token_attention_by_hand():
         o.append(w0 * v[0] + (1 - w0) * v[1])
     np.testing.assert_allclose(y[1], x[1] + np.concatenate(o), rtol=1e-13)
     np.testing.assert_allclose(y[0], x[0] + np.concatenate([v[0], v[0]]), rtol=1e-13)
+
+
+# ---------------------------------------------------------------- INT8 KV cache
+
+def test_int8_quantizer_is_a_uniform_quantizer_within_half_a_step():
+    rng = np.random.default_rng(5)
+    x = (rng.normal(size=(64, 128)) * rng.uniform(0.01, 20, size=(64, 1))).astype(np.float32)
+    codes, scale = O.quantize_int8_rows(x)
+    assert codes.dtype == np.int8 and scale.dtype == np.float32
+    assert codes.min() >= -127 and codes.max() <= 127
+    # textbook round-to-nearest bound: every value within half a step of its code
+    err = np.abs(x.astype(np.float64) - codes.astype(np.float64) * scale[:, None])
+    assert (err <= 0.5 * scale[:, None].astype(np.float64) * (1 + 1e-6)).all()
+    # the largest magnitude of each row sits on the end of the code range, with its sign
+    i = np.abs(x).argmax(axis=1)
+    assert (codes[np.arange(64), i] == np.sign(x[np.arange(64), i]) * 127).all()
+    # a step is max|x| / 127
+    np.testing.assert_allclose(scale, np.abs(x).max(axis=1) / 127, rtol=1e-7)
+
+
+def test_int8_quantizer_zero_row_and_exact_grid():
+    codes, scale = O.quantize_int8_rows(np.zeros((2, 16), np.float32))
+    assert scale.tolist() == [0.0, 0.0] and not codes.any()
+    # values already on the grid k * 2^-3 with max 127 * 2^-3 come back exactly
+    k = np.arange(-127, 129, 16)[:16].astype(np.float32)
+    k[0] = -127
+    codes, scale = O.quantize_int8_rows((k * 0.125)[None, :])
+    assert scale[0] == np.float32(0.125) and (codes[0] == k).all()
+
+
+def test_int8_paged_attention_reduces_to_exact_attention_on_grid_values():
+    """K/V rows that are integers times a power of two (with a max of 127 steps) quantize
+    losslessly, so attention through an INT8 pool equals attention through an exact pool."""
+    rng = np.random.default_rng(9)
+    nb, Hkv, bs, d, B, Hq = 6, 2, 4, 8, 2, 4
+    step = 2.0 ** rng.integers(-6, -2, size=(nb, Hkv, bs))
+    ints = rng.integers(-126, 127, size=(nb, Hkv, bs, d)).astype(np.float64)
+    ints[..., 0] = 127                              # every row's max is exactly 127 steps
+    vals = ints * step[..., None]
+    exact_k, exact_v = vals.copy(), vals[::-1].copy()
+    qk = O.QuantPool(np.zeros((nb, Hkv, bs, d), np.int8), np.zeros((nb, Hkv, bs), np.float32))
+    qv = O.QuantPool(np.zeros((nb, Hkv, bs, d), np.int8), np.zeros((nb, Hkv, bs), np.float32))
+    slots = np.arange(nb * bs)
+    O.reshape_and_cache(exact_k.transpose(0, 2, 1, 3).reshape(-1, Hkv, d),
+                        exact_v.transpose(0, 2, 1, 3).reshape(-1, Hkv, d), slots, qk, qv)
+    table = np.array([[3, 0, 5], [1, 4, 2]])
+    ctx = np.array([11, 9])
+    q = rng.normal(size=(B, Hq, d))
+    got = O.paged_attention_decode(q, qk, qv, table, ctx, 0.35)
+    ref = O.paged_attention_decode(q, exact_k, exact_v, table, ctx, 0.35)
+    np.testing.assert_allclose(got, ref, rtol=1e-12, atol=1e-12)
+    # and off the grid the cached rows read back within half a step
+    x = rng.normal(size=(5, Hkv, d))
+    O.reshape_and_cache(x, x, [0, 1, 2, 3, 4], qk, qv)
+    back = O.gather_cache(qk, [0, 1, 2], 5).transpose(1, 0, 2)
+    codes, scale = O.quantize_int8_rows(x)
+    assert (np.abs(back - x) <= 0.5 * scale[..., None] * (1 + 1e-6) + 1e-7).all()
