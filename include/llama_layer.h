@@ -178,6 +178,27 @@ int ll_reshape_and_cache(const void* k, const void* v, const int32_t* slot_mappi
                          int32_t n_kv_heads, int32_t head_dim, int32_t block_size,
                          const ll_kv_pool* pool, int32_t* status, void* stream);
 
+/* An INT8 KV pool (paging page, section "KV Cache quantisation": per-token
+ * granularity, each token's K and V with their own float32 scale).  Codes in the
+ * layout of ll_kv_pool; one scale per token and KV head.  A cached row reads back
+ * as code * scale. */
+typedef struct {
+    void* k;              /* int8 [num_blocks, n_kv_heads, block_size, head_dim] */
+    void* v;              /* same shape */
+    float* k_scale;       /* float32 [num_blocks, n_kv_heads, block_size] */
+    float* v_scale;       /* same shape */
+    int32_t num_blocks;
+} ll_kv_pool_q8;
+
+/* ReshapeAndCache into an INT8 pool, quantising online: for token t and KV head h,
+ * scale = max_i |row_i| / 127 and code_i = round-half-even(row_i / scale) in
+ * float32 (IEEE division), clipped to [-127, 127]; a row of zeros gets scale 0
+ * and codes 0.  Arguments and slot rules as ll_reshape_and_cache; head_dim a
+ * multiple of 32, at most 256.  Codes and scales are bit-exact. */
+int ll_reshape_and_cache_q8(const void* k, const void* v, const int32_t* slot_mapping, int32_t tokens,
+                            int32_t n_kv_heads, int32_t head_dim, int32_t block_size,
+                            const ll_kv_pool_q8* pool, int32_t* status, void* stream);
+
 /* Workspace bytes for ll_paged_attention_decode. */
 size_t ll_attention_workspace_size(int32_t batch, int32_t n_heads, int32_t head_dim,
                                    int32_t max_blocks, int32_t block_size);
@@ -194,6 +215,16 @@ int ll_paged_attention_decode(const void* q, const ll_kv_pool* pool, const int32
                               int32_t n_heads, int32_t n_kv_heads, int32_t head_dim,
                               int32_t block_size, float scale, void* out, void* workspace,
                               size_t workspace_bytes, int32_t* status, void* stream);
+
+/* ll_paged_attention_decode over an INT8 pool: the cached rows are code * scale
+ * (paging page, section "KV Cache quantisation": dequantised as the cache block
+ * is loaded).  head_dim 128; workspace sized by ll_attention_workspace_size; the
+ * other arguments and limits as ll_paged_attention_decode. */
+int ll_paged_attention_decode_q8(const void* q, const ll_kv_pool_q8* pool, const int32_t* block_table,
+                                 int32_t max_blocks, const int32_t* context_lens, int32_t batch,
+                                 int32_t n_heads, int32_t n_kv_heads, int32_t head_dim,
+                                 int32_t block_size, float scale, void* out, void* workspace,
+                                 size_t workspace_bytes, int32_t* status, void* stream);
 
 /* ll_paged_attention_decode for callers that cannot allocate device memory.
  * The pages have no counterpart of this call.  Some callers only own the

@@ -278,3 +278,76 @@ def test_checkpoints_match_oracle_stage_by_stage(mode):
     for name, ref in (("x_hat", want["xh"]), ("q", want["q"].reshape(T, -1)), ("o", want["o"].reshape(T, -1)),
                       ("h", want["h"]), ("h_hat", want["hh"]), ("a", want["a"])):
         assert_close(f64(cp[name]), ref, f"{mode} checkpoint {name}")
+
+
+# ---------------------------------------------------------------- INT8 KV cache
+
+@pytest.mark.parametrize("T,Hkv,d,bs,nb", [(37, 2, 64, 16, 8), (300, 8, 128, 128, 5), (5, 4, 128, 32, 3)])
+def test_reshape_and_cache_q8_bit_exact(T, Hkv, d, bs, nb):
+    g = torch.Generator().manual_seed(T * 7 + d)
+    # rows of very different magnitudes, one all-zero row, one row with a single non-zero
+    mag = torch.exp(torch.randn(T, Hkv, 1, generator=g) * 3)
+    k = (torch.randn(T, Hkv, d, generator=g) * mag).to(torch.bfloat16)
+    v = (torch.randn(T, Hkv, d, generator=g) * mag).to(torch.bfloat16)
+    k[0, 0] = 0
+    v[min(1, T - 1), Hkv - 1] = 0
+    v[min(1, T - 1), Hkv - 1, 3] = -2.5
+    slots = synth.make_slot_mapping(T, nb * bs, seed=T + 11, n_skip=min(2, T - 1))
+    pool = api.PoolQ8.empty(nb, Hkv, bs, d)
+    st = api.reshape_and_cache_q8(k.to(DEV), v.to(DEV), slots.to(DEV), pool)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    qk = O.QuantPool(np.zeros((nb, Hkv, bs, d), np.int8), np.zeros((nb, Hkv, bs), np.float32))
+    qv = O.QuantPool(np.zeros((nb, Hkv, bs, d), np.int8), np.zeros((nb, Hkv, bs), np.float32))
+    O.reshape_and_cache(f64(k), f64(v), slots.numpy(), qk, qv)
+    np.testing.assert_array_equal(pool.k.cpu().numpy(), qk.codes)
+    np.testing.assert_array_equal(pool.v.cpu().numpy(), qv.codes)
+    np.testing.assert_array_equal(pool.k_scale.cpu().numpy().view(np.uint32), qk.scales.view(np.uint32))
+    np.testing.assert_array_equal(pool.v_scale.cpu().numpy().view(np.uint32), qv.scales.view(np.uint32))
+
+
+def _random_q8_pool(nb, Hkv, bs, d, seed):
+    g = torch.Generator().manual_seed(seed)
+    codes = lambda: torch.randint(-127, 128, (nb, Hkv, bs, d), generator=g, dtype=torch.int32).to(torch.int8)
+    scales = lambda: (torch.rand(nb, Hkv, bs, generator=g) * 0.03 + 0.001).float()
+    return codes(), codes(), scales(), scales()
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,bs,ctx_lo,ctx_hi", [
+    (5, 8, 8, 128, 1, 300),             # MHA, ragged
+    (3, 16, 2, 128, 900, 3100),         # GQA 8, several 1024-key splits
+    (4, 4, 4, 32, 1023, 1026),          # split boundaries, 32-row blocks
+    (2, 8, 1, 16, 1, 90),               # 16-row blocks, one KV head
+])
+def test_paged_attention_decode_q8(B, Hq, Hkv, bs, ctx_lo, ctx_hi):
+    d = 128
+    ctx = synth.make_context_lens(B, ctx_lo, ctx_hi, seed=B * 19)
+    ctx[0] = ctx_lo
+    table, nb = synth.make_block_table(ctx.tolist(), bs, seed=B * 23, extra_blocks=3)
+    kc, vc, ks, vs = _random_q8_pool(nb, Hkv, bs, d, seed=B * 29)
+    q = synth.normal_bf16((B, Hq, d), 1.0, seed=B + 5, tag="q")
+    pool = api.PoolQ8(kc.to(DEV), vc.to(DEV), ks.to(DEV), vs.to(DEV))
+    scale = 1 / math.sqrt(d)
+    out = api.paged_attention_decode_q8(q.to(DEV), pool, table.to(DEV), ctx.to(DEV), scale)
+    torch.cuda.synchronize()
+    ref = O.paged_attention_decode(f64(q), O.QuantPool(kc.numpy(), ks.numpy()), O.QuantPool(vc.numpy(), vs.numpy()),
+                                   table.numpy(), ctx.numpy(), scale)
+    assert_close(f64(out), ref, "paged_attention_decode_q8")
+
+
+def test_paged_attention_decode_q8_bad_block_is_flagged_and_finite():
+    B, Hq, Hkv, bs, d = 2, 4, 2, 16, 128
+    ctx = torch.tensor([40, 33], dtype=torch.int32)
+    table, nb = synth.make_block_table(ctx.tolist(), bs, seed=3, extra_blocks=2)
+    table[1, 1] = 10_000                     # beyond the pool: its keys are left out
+    kc, vc, ks, vs = _random_q8_pool(nb, Hkv, bs, d, seed=7)
+    ks[:] = float("inf")                     # stale scales must never reach P
+    ks[table[0, :3].long()] = 0.01
+    ks[table[1, [0, 2]].long()] = 0.01
+    pool = api.PoolQ8(kc.to(DEV), vc.to(DEV), ks.to(DEV), vs.to(DEV))
+    q = synth.normal_bf16((B, Hq, d), 1.0, seed=9, tag="q")
+    status = api.new_status()
+    out = api.paged_attention_decode_q8(q.to(DEV), pool, table.to(DEV), ctx.to(DEV), 0.09, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) & api.LL_DEV_BAD_BLOCK
+    assert torch.isfinite(out.float()).all()

@@ -31,7 +31,7 @@ EXPORTED = [
     "ll_attention_workspace_size", "ll_paged_attention_decode", "ll_linear_workspace_size",
     "ll_linear", "ll_device_sm_count", "ll_trace_begin", "ll_trace_end", "ll_trace_elapsed_ms",
     "ll_trace_name", "ll_paged_attention_decode_noalloc", "ll_selftest_bounded_wait",
-    "ll_workspace_checkpoints",
+    "ll_workspace_checkpoints", "ll_reshape_and_cache_q8", "ll_paged_attention_decode_q8",
 ]
 
 
@@ -51,6 +51,11 @@ class ll_weights(ctypes.Structure):
 
 class ll_kv_pool(ctypes.Structure):
     _fields_ = [("k", ctypes.c_void_p), ("v", ctypes.c_void_p), ("num_blocks", ctypes.c_int32)]
+
+
+class ll_kv_pool_q8(ctypes.Structure):
+    _fields_ = [("k", ctypes.c_void_p), ("v", ctypes.c_void_p), ("k_scale", ctypes.c_void_p),
+                ("v_scale", ctypes.c_void_p), ("num_blocks", ctypes.c_int32)]
 
 
 class ll_checkpoints(ctypes.Structure):
@@ -89,6 +94,10 @@ def _load():
         "ll_trace_name": (ctypes.c_char_p, [I32]),
         "ll_selftest_bounded_wait": (ctypes.c_int, [I32, P, P, P]),
         "ll_workspace_checkpoints": (ctypes.c_int, [cfgp, I32, I32, ctypes.POINTER(ll_checkpoints)]),
+        "ll_reshape_and_cache_q8": (ctypes.c_int, [P, P, P, I32, I32, I32, I32, ctypes.POINTER(ll_kv_pool_q8),
+                                                   P, P]),
+        "ll_paged_attention_decode_q8": (ctypes.c_int, [P, ctypes.POINTER(ll_kv_pool_q8), P, I32, P, I32, I32, I32,
+                                                        I32, I32, ctypes.c_float, P, P, S, P, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -273,6 +282,72 @@ def reshape_and_cache(k, v, slot_mapping, k_pool, v_pool, status=None, stream=No
         _ptr(k), _ptr(v), _ptr(slot_mapping), T, Hkv, d, k_pool.shape[2], ctypes.byref(pool),
         _ptr(status), _stream(stream)))
     return status
+
+
+class PoolQ8:
+    """An INT8 KV pool on the GPU: codes k, v int8 [num_blocks, n_kv_heads, block_size,
+    head_dim] and float32 scales k_scale, v_scale [num_blocks, n_kv_heads, block_size]."""
+
+    def __init__(self, k, v, k_scale, v_scale):
+        _need(k, "k codes", torch.int8)
+        _need(v, "v codes", torch.int8, shape=tuple(k.shape))
+        _need(k_scale, "k_scale", torch.float32, shape=tuple(k.shape[:3]))
+        _need(v_scale, "v_scale", torch.float32, shape=tuple(k.shape[:3]))
+        self.k, self.v, self.k_scale, self.v_scale = k, v, k_scale, v_scale
+
+    @classmethod
+    def empty(cls, num_blocks, n_kv_heads, block_size, head_dim, device="cuda"):
+        shape = (num_blocks, n_kv_heads, block_size, head_dim)
+        return cls(torch.zeros(shape, dtype=torch.int8, device=device),
+                   torch.zeros(shape, dtype=torch.int8, device=device),
+                   torch.zeros(shape[:3], dtype=torch.float32, device=device),
+                   torch.zeros(shape[:3], dtype=torch.float32, device=device))
+
+    @property
+    def block_size(self):
+        return self.k.shape[2]
+
+    def c(self):
+        return ll_kv_pool_q8(self.k.data_ptr(), self.v.data_ptr(), self.k_scale.data_ptr(),
+                             self.v_scale.data_ptr(), self.k.shape[0])
+
+
+def reshape_and_cache_q8(k, v, slot_mapping, pool: PoolQ8, status=None, stream=None):
+    """ll_reshape_and_cache_q8: k, v BF16 [tokens, n_kv_heads, head_dim] quantised into pool."""
+    _need(k, "k", torch.bfloat16)
+    _need(v, "v", torch.bfloat16, shape=tuple(k.shape))
+    T, Hkv, d = k.shape
+    _need(slot_mapping, "slot_mapping", torch.int32, shape=(T,))
+    cp = pool.c()
+    if status is None:
+        status = new_status(k.device)
+    _check("ll_reshape_and_cache_q8", lib.ll_reshape_and_cache_q8(
+        _ptr(k), _ptr(v), _ptr(slot_mapping), T, Hkv, d, pool.block_size, ctypes.byref(cp),
+        _ptr(status), _stream(stream)))
+    return status
+
+
+def paged_attention_decode_q8(q, pool: PoolQ8, block_table, context_lens, scale, out=None, workspace=None,
+                              status=None, stream=None):
+    """ll_paged_attention_decode_q8: q BF16 [batch, n_heads, 128] over an INT8 pool."""
+    _need(q, "q", torch.bfloat16)
+    B, Hq, d = q.shape
+    _need(block_table, "block_table", torch.int32)
+    _need(context_lens, "context_lens", torch.int32, shape=(B,))
+    Hkv, bs = pool.k.shape[1], pool.block_size
+    mb = block_table.shape[1]
+    if out is None:
+        out = torch.empty_like(q)
+    if workspace is None:
+        workspace = torch.empty(max(attention_workspace_size(B, Hq, d, mb, bs), 16), dtype=torch.uint8,
+                                device=q.device)
+    if status is None:
+        status = new_status(q.device)
+    cp = pool.c()
+    _check("ll_paged_attention_decode_q8", lib.ll_paged_attention_decode_q8(
+        _ptr(q), ctypes.byref(cp), _ptr(block_table), mb, _ptr(context_lens), B, Hq, Hkv, d, bs,
+        float(scale), _ptr(out), _ptr(workspace), workspace.numel(), _ptr(status), _stream(stream)))
+    return out
 
 
 def attention_workspace_size(batch, n_heads, head_dim, max_blocks, block_size):

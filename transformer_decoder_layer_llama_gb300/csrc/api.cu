@@ -501,10 +501,72 @@ int ll_reshape_and_cache(const void* k, const void* v, const int32_t* slot_mappi
         static_cast<cudaStream_t>(stream)));
 }
 
+int ll_reshape_and_cache_q8(const void* k, const void* v, const int32_t* slot_mapping, int32_t tokens,
+                            int32_t n_kv_heads, int32_t head_dim, int32_t block_size,
+                            const ll_kv_pool_q8* pool, int32_t* status, void* stream) {
+    ll::clear_last_error();
+    if (!k || !v || !slot_mapping || !status || !pool || !pool->k || !pool->v || !pool->k_scale ||
+        !pool->v_scale || pool->num_blocks <= 0)
+        return LL_ERR_INVALID_ARG;
+    if (tokens < 0 || n_kv_heads <= 0 || head_dim <= 0 || block_size <= 0) return LL_ERR_INVALID_ARG;
+    if (head_dim % 32 != 0 || head_dim > 256) return LL_ERR_UNSUPPORTED;
+    return cuda_rc(ll::launch_reshape_and_cache_q8(
+        static_cast<const __nv_bfloat16*>(k), static_cast<const __nv_bfloat16*>(v), slot_mapping, nullptr,
+        nullptr, nullptr, 0, 1, tokens, n_kv_heads, head_dim, block_size, static_cast<int8_t*>(pool->k),
+        static_cast<int8_t*>(pool->v), pool->k_scale, pool->v_scale, pool->num_blocks, status,
+        static_cast<cudaStream_t>(stream)));
+}
+
 size_t ll_attention_workspace_size(int32_t batch, int32_t n_heads, int32_t head_dim,
                                    int32_t max_blocks, int32_t block_size) {
     if (batch <= 0 || n_heads <= 0 || head_dim <= 0 || max_blocks <= 0 || block_size <= 0) return 0;
     return align_up(ll::attn_decode_scratch_bytes(batch, n_heads, head_dim, max_blocks, block_size));
+}
+
+namespace {
+bool pool_q8_ok(const ll_kv_pool_q8* p) {
+    return p && p->k && p->v && p->k_scale && p->v_scale && p->num_blocks > 0 && aligned16(p->k) &&
+           aligned16(p->v) && aligned16(p->k_scale) && aligned16(p->v_scale);
+}
+}  // namespace
+
+int ll_paged_attention_decode_q8(const void* q, const ll_kv_pool_q8* pool, const int32_t* block_table,
+                                 int32_t max_blocks, const int32_t* context_lens, int32_t batch,
+                                 int32_t n_heads, int32_t n_kv_heads, int32_t head_dim,
+                                 int32_t block_size, float scale, void* out, void* workspace,
+                                 size_t workspace_bytes, int32_t* status, void* stream) {
+    ll::clear_last_error();
+    if (!q || !block_table || !context_lens || !out || !status || !pool_q8_ok(pool)) return LL_ERR_INVALID_ARG;
+    if (batch <= 0 || n_heads <= 0 || n_kv_heads <= 0 || max_blocks <= 0 || block_size <= 0)
+        return LL_ERR_INVALID_ARG;
+    if (head_dim != 128) return LL_ERR_UNSUPPORTED;
+    if (n_heads % n_kv_heads != 0 || n_heads / n_kv_heads > 16) return LL_ERR_UNSUPPORTED;
+    if (!block_size_ok(block_size)) return LL_ERR_UNSUPPORTED;
+    if (!aligned16(q) || !aligned16(out)) return LL_ERR_INVALID_ARG;
+    const size_t need = ll_attention_workspace_size(batch, n_heads, head_dim, max_blocks, block_size);
+    if (!workspace || workspace_bytes < need || !aligned16(workspace)) return LL_ERR_WORKSPACE;
+    ll::AttnDecodeArgs at{};
+    at.q = static_cast<const __nv_bfloat16*>(q);
+    at.k_q8 = static_cast<const int8_t*>(pool->k);
+    at.v_q8 = static_cast<const int8_t*>(pool->v);
+    at.k_scale = pool->k_scale;
+    at.v_scale = pool->v_scale;
+    at.context_lens = context_lens;
+    at.block_table = block_table;
+    at.max_blocks = max_blocks;
+    at.num_blocks = pool->num_blocks;
+    at.block_size = block_size;
+    at.batch = batch;
+    at.n_heads = n_heads;
+    at.n_kv_heads = n_kv_heads;
+    at.head_dim = head_dim;
+    at.scale = scale;
+    at.out = static_cast<__nv_bfloat16*>(out);
+    const size_t rows = (size_t)batch * n_heads * ll::attn_decode_max_splits(max_blocks, block_size);
+    at.part_o = static_cast<float*>(workspace);
+    at.part_ml = at.part_o + rows * head_dim;
+    at.status = status;
+    return cuda_rc(ll::launch_attn_decode_q8(at, static_cast<cudaStream_t>(stream)));
 }
 
 int ll_paged_attention_decode(const void* q, const ll_kv_pool* pool, const int32_t* block_table,

@@ -332,6 +332,312 @@ __global__ void __launch_bounds__(160, 2)
     }
 }
 
+// ---------------------------------------------------------------- decode over an INT8 cache
+// The same split / warp structure over an INT8 pool (head_dim 128; paging page,
+// section "KV Cache quantisation": the cache block is dequantised as it is
+// loaded).  The producer streams each 64-key tile's codes (128-byte rows, the
+// 128-byte swizzle) with TMA and its K and V scales with bulk copies, all on
+// the stage's barrier.  Each consumer warp turns the codes of its own 16 keys
+// into FP16 (exact: |code| <= 127) in a private swizzled tile and runs the
+// tensor-core steps in FP16.  A key's K scale multiplies its score and its V
+// scale its probability before P V, so dequantised values are never formed;
+// the row sum stays the sum of the unscaled probabilities.  Q enters as FP16
+// (exact for BF16 values of FP16's range), P as one FP16 operand (the cache's
+// INT8 rounding dominates its error).
+__global__ void __launch_bounds__(160, 2)
+    attn_decode_split_q8_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                                const AttnDecodeArgs a, int max_splits) {
+    constexpr int D = 128, BN = 64, STAGES = 4, NCONS = 128;
+    constexpr int TILE = BN * D;                       // bytes of one INT8 K or V tile
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* sbase = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* sk = sbase;                               // [STAGES][TILE] codes
+    uint8_t* sv = sk + STAGES * TILE;                  // [STAGES][TILE]
+    float* ssc = reinterpret_cast<float*>(sv + STAGES * TILE);   // [STAGES][2][BN] K, V scales
+    uint8_t* sq = reinterpret_cast<uint8_t*>(ssc + STAGES * 2 * BN);   // [16][D] FP16 q, swizzled rows
+    uint8_t* sh = sq + 16 * D * 2;                     // [4 warps][K, V][16][D] FP16 codes, swizzled rows
+    __shared__ uint64_t full_bar[STAGES], empty_bar[STAGES];
+    __shared__ int abort_s;
+
+    const int split = blockIdx.x, hk = blockIdx.y, b = blockIdx.z;
+    const int G = a.n_heads / a.n_kv_heads;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    pdl_wait();
+    pdl_trigger();
+    int ctx = a.context_lens[b];
+    if (ctx > a.max_blocks * a.block_size || ctx < 0) {
+        if (threadIdx.x == 0 && split == 0 && hk == 0) flag_status(a.status, LL_DEV_BAD_POSITION);
+        ctx = min(max(ctx, 0), a.max_blocks * a.block_size);
+    }
+    const int k_begin = split * kDecodeChunk;
+    const int k_end = min(ctx, k_begin + kDecodeChunk);
+    const size_t part_row = ((size_t)b * a.n_heads + (size_t)hk * G) * max_splits + split;
+    if (k_begin >= k_end) {
+        if (threadIdx.x < G) {
+            float* ml = a.part_ml + 2 * (part_row + (size_t)threadIdx.x * max_splits);
+            ml[0] = -INFINITY;
+            ml[1] = 0.f;
+        }
+        return;
+    }
+    const int32_t* table_row = a.block_table + (size_t)b * a.max_blocks;
+    const int n_kt = (k_end - k_begin + BN - 1) / BN;
+    const int kt_rows = min(a.block_size, BN);
+
+    if (threadIdx.x == 0) {
+        for (int st = 0; st < STAGES; ++st) {
+            mbar_init(&full_bar[st], 1);
+            mbar_init(&empty_bar[st], 4);
+        }
+        abort_s = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+
+    if (warp == 4) {
+        // ------------------------------------------------ producer
+        if (lane == 0) {
+            tma_prefetch_desc(&tmK);
+            tma_prefetch_desc(&tmV);
+            uint32_t issued[STAGES] = {0, 0, 0, 0};
+            for (int kt = 0; kt < n_kt; ++kt) {
+                const int st = kt % STAGES;
+                const uint32_t ph = (uint32_t)(kt / STAGES) & 1u;
+                if (!mbar_wait_bounded(&empty_bar[st], ph ^ 1u, &abort_s, a.status)) break;
+                const int p0 = k_begin + kt * BN;
+                uint32_t bytes = 0;
+                for (int p = p0; p < p0 + BN && p < k_end; p += kt_rows) {
+                    const int blk = table_row[p / a.block_size];
+                    if (blk >= 0 && blk < a.num_blocks) bytes += 2u * kt_rows * (128u + 4u);
+                }
+                mbar_arrive_expect_tx(&full_bar[st], bytes);
+                for (int p = p0, sb = 0; p < p0 + BN && p < k_end; p += kt_rows, ++sb) {
+                    const int blk = table_row[p / a.block_size];
+                    if (blk < 0 || blk >= a.num_blocks) {
+                        flag_status(a.status, LL_DEV_BAD_BLOCK);
+                        continue;
+                    }
+                    const size_t row = ((size_t)blk * a.n_kv_heads + hk) * a.block_size + (p % a.block_size);
+                    const uint32_t off = (uint32_t)(st * TILE + sb * kt_rows * 128);
+                    tma_load_2d(sk + off, &tmK, 0, (int)row, &full_bar[st]);
+                    tma_load_2d(sv + off, &tmV, 0, (int)row, &full_bar[st]);
+                    bulk_load(ssc + (st * 2 + 0) * BN + sb * kt_rows, a.k_scale + row, (uint32_t)kt_rows * 4u,
+                              &full_bar[st]);
+                    bulk_load(ssc + (st * 2 + 1) * BN + sb * kt_rows, a.v_scale + row, (uint32_t)kt_rows * 4u,
+                              &full_bar[st]);
+                }
+                ++issued[st];
+            }
+            if (abort_s) {
+                volatile int never = 0;
+                for (int st = 0; st < STAGES; ++st)
+                    if (issued[st]) mbar_wait_bounded(&full_bar[st], (issued[st] - 1) & 1u, &never, nullptr);
+            }
+        }
+        __syncwarp();
+        return;
+    }
+
+    // ---------------------------------------------------- consumers (warps 0-3)
+    for (int i = threadIdx.x; i < 16 * (D / 8); i += NCONS) {
+        // q rows of the group (zero padding to 16 rows) as FP16
+        const int r = i / (D / 8), c = i % (D / 8);
+        uint4 o = make_uint4(0, 0, 0, 0);
+        if (r < G) {
+            const uint4 w = *reinterpret_cast<const uint4*>(a.q + ((size_t)b * a.n_heads + hk * G + r) * D + c * 8);
+            o.x = pack_f16x2(bf16_lo(w.x), bf16_hi(w.x));
+            o.y = pack_f16x2(bf16_lo(w.y), bf16_hi(w.y));
+            o.z = pack_f16x2(bf16_lo(w.z), bf16_hi(w.z));
+            o.w = pack_f16x2(bf16_lo(w.w), bf16_hi(w.w));
+        }
+        *reinterpret_cast<uint4*>(sq + swz<D>(r, c)) = o;
+    }
+    asm volatile("bar.sync 1, 128;" ::: "memory");
+    uint32_t qf[D / 16][4];
+    {
+        const uint32_t qb = smem_u32(sq);
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) ldmatrix_x4(qf[ks], qb + swz<D>(lane & 15, ks * 2 + (lane >> 4)));
+    }
+    uint8_t* kh = sh + warp * (2 * 16 * D * 2);        // this warp's FP16 K rows
+    uint8_t* vh = kh + 16 * D * 2;                     // ... and V rows
+    const uint32_t khb = smem_u32(kh), vhb = smem_u32(vh);
+
+    const float sl2 = a.scale * kLog2e;
+    const int g = lane >> 2, cq = lane & 3;
+    float acc[D / 8][4];
+#pragma unroll
+    for (int i = 0; i < D / 8; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+
+    for (int kt = 0; kt < n_kt; ++kt) {
+        const int st = kt % STAGES;
+        const uint32_t ph = (uint32_t)(kt / STAGES) & 1u;
+        if (!mbar_wait_bounded(&full_bar[st], ph, &abort_s, a.status)) break;
+        // validity of this warp's 16 keys: inside the split and backed by a valid block
+        const int pbase = k_begin + kt * BN + warp * 16;
+        bool my_ok = false;
+        if (lane < 16) {
+            const int p = pbase + lane;
+            if (p < k_end) {
+                const int blk = table_row[p / a.block_size];
+                my_ok = blk >= 0 && blk < a.num_blocks;
+            }
+        }
+        const uint32_t okmask = __ballot_sync(0xffffffffu, my_ok) & 0xffffu;
+        {
+            // the warp's 16 rows of K and V codes -> FP16 (rows without a valid key -> 0);
+            // lane: row lane / 2, 16-code chunks 4 (lane & 1) .. + 3
+            const int rl = lane >> 1, R = warp * 16 + rl;
+            const bool row_ok = (okmask >> rl) & 1u;
+            __syncwarp();                              // the previous tile's reads are done
+#pragma unroll
+            for (int kv = 0; kv < 2; ++kv) {
+                const uint8_t* src = (kv ? sv : sk) + st * TILE;
+                uint8_t* dst = kv ? vh : kh;
+#pragma unroll
+                for (int jj = 0; jj < 4; ++jj) {
+                    const int j = (lane & 1) * 4 + jj;
+                    uint4 o0 = make_uint4(0, 0, 0, 0), o1 = make_uint4(0, 0, 0, 0);
+                    if (row_ok) {
+                        const uint4 w = *reinterpret_cast<const uint4*>(src + R * 128 + ((j ^ (R & 7)) << 4));
+                        i8x4_to_f16x4(w.x, o0.x, o0.y);
+                        i8x4_to_f16x4(w.y, o0.z, o0.w);
+                        i8x4_to_f16x4(w.z, o1.x, o1.y);
+                        i8x4_to_f16x4(w.w, o1.z, o1.w);
+                    }
+                    *reinterpret_cast<uint4*>(dst + swz<D>(rl, 2 * j)) = o0;
+                    *reinterpret_cast<uint4*>(dst + swz<D>(rl, 2 * j + 1)) = o1;
+                }
+            }
+            __syncwarp();
+        }
+        float s[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+            uint32_t bfr[4];
+            const int r = (lane & 7) + ((lane >> 4) << 3);
+            const int c = ks * 2 + ((lane >> 3) & 1);
+            ldmatrix_x4(bfr, khb + swz<D>(r, c));
+            mma_f16_16816(s[0], qf[ks], bfr[0], bfr[1]);
+            mma_f16_16816(s[1], qf[ks], bfr[2], bfr[3]);
+        }
+        const float* ksc = ssc + (st * 2 + 0) * BN + warp * 16;
+        const float* vsc = ssc + (st * 2 + 1) * BN + warp * 16;
+        float mx0 = -INFINITY, mx1 = -INFINITY;
+        float vs[2][2];
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+            const int kk = nt * 8 + 2 * cq;   // key index within the warp's 16
+            const bool v0 = (okmask >> kk) & 1u, v1 = (okmask >> (kk + 1)) & 1u;
+            const float f0 = sl2 * ksc[kk], f1 = sl2 * ksc[kk + 1];
+            vs[nt][0] = v0 ? vsc[kk] : 0.f;
+            vs[nt][1] = v1 ? vsc[kk + 1] : 0.f;
+            s[nt][0] = v0 ? s[nt][0] * f0 : -INFINITY;
+            s[nt][1] = v1 ? s[nt][1] * f1 : -INFINITY;
+            s[nt][2] = v0 ? s[nt][2] * f0 : -INFINITY;
+            s[nt][3] = v1 ? s[nt][3] * f1 : -INFINITY;
+            mx0 = fmaxf(mx0, fmaxf(s[nt][0], s[nt][1]));
+            mx1 = fmaxf(mx1, fmaxf(s[nt][2], s[nt][3]));
+        }
+#pragma unroll
+        for (int o = 1; o <= 2; o <<= 1) {
+            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
+            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
+        }
+        const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+        const float base0 = (mn0 == -INFINITY) ? 0.f : mn0;
+        const float base1 = (mn1 == -INFINITY) ? 0.f : mn1;
+        const float al0 = exp2f(m0 - base0), al1 = exp2f(m1 - base1);
+        m0 = mn0;
+        m1 = mn1;
+        uint32_t pf[4];
+        float rs0 = 0.f, rs1 = 0.f;
+        {
+            float p[2][4];
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt) {
+                p[nt][0] = exp2f(s[nt][0] - base0);
+                p[nt][1] = exp2f(s[nt][1] - base0);
+                p[nt][2] = exp2f(s[nt][2] - base1);
+                p[nt][3] = exp2f(s[nt][3] - base1);
+                rs0 += p[nt][0] + p[nt][1];
+                rs1 += p[nt][2] + p[nt][3];
+            }
+            // each key's V scale rides on its probability
+            pf[0] = pack_f16x2(p[0][0] * vs[0][0], p[0][1] * vs[0][1]);
+            pf[1] = pack_f16x2(p[0][2] * vs[0][0], p[0][3] * vs[0][1]);
+            pf[2] = pack_f16x2(p[1][0] * vs[1][0], p[1][1] * vs[1][1]);
+            pf[3] = pack_f16x2(p[1][2] * vs[1][0], p[1][3] * vs[1][1]);
+        }
+        l0 = l0 * al0 + rs0;
+        l1 = l1 * al1 + rs1;
+#pragma unroll
+        for (int i = 0; i < D / 8; ++i) {
+            acc[i][0] *= al0;
+            acc[i][1] *= al0;
+            acc[i][2] *= al1;
+            acc[i][3] *= al1;
+        }
+#pragma unroll
+        for (int dp = 0; dp < D / 16; ++dp) {
+            uint32_t bfr[4];
+            const int r = (lane & 7) + (((lane >> 3) & 1) << 3);
+            const int c = dp * 2 + (lane >> 4);
+            ldmatrix_x4_trans(bfr, vhb + swz<D>(r, c));
+            mma_f16_16816(acc[2 * dp], pf, bfr[0], bfr[1]);
+            mma_f16_16816(acc[2 * dp + 1], pf, bfr[2], bfr[3]);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty_bar[st]);
+    }
+#pragma unroll
+    for (int o = 1; o <= 2; o <<= 1) {
+        l0 += __shfl_xor_sync(0xffffffffu, l0, o);
+        l1 += __shfl_xor_sync(0xffffffffu, l1, o);
+    }
+
+    // merge the 4 consumer warps: [4][16] (m, l) and [4][16][D] acc, over the code rings
+    asm volatile("bar.sync 1, 128;" ::: "memory");
+    float* s_ml = reinterpret_cast<float*>(sk);            // [4][16][2]
+    float* s_acc = s_ml + 4 * 16 * 2;                      // [4][16][D]
+    if (cq == 0) {
+        s_ml[(warp * 16 + g) * 2 + 0] = m0;
+        s_ml[(warp * 16 + g) * 2 + 1] = l0;
+        s_ml[(warp * 16 + g + 8) * 2 + 0] = m1;
+        s_ml[(warp * 16 + g + 8) * 2 + 1] = l1;
+    }
+#pragma unroll
+    for (int i = 0; i < D / 8; ++i) {
+        const int col = i * 8 + 2 * cq;
+        s_acc[(warp * 16 + g) * D + col] = acc[i][0];
+        s_acc[(warp * 16 + g) * D + col + 1] = acc[i][1];
+        s_acc[(warp * 16 + g + 8) * D + col] = acc[i][2];
+        s_acc[(warp * 16 + g + 8) * D + col + 1] = acc[i][3];
+    }
+    asm volatile("bar.sync 1, 128;" ::: "memory");
+    for (int i = threadIdx.x; i < G * D; i += NCONS) {
+        const int r = i / D, col = i % D;
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < 4; ++w) M = fmaxf(M, s_ml[(w * 16 + r) * 2]);
+        const float base = (M == -INFINITY) ? 0.f : M;
+        float num = 0.f, den = 0.f;
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+            const float e = exp2f(s_ml[(w * 16 + r) * 2] - base);
+            num += e * s_acc[(w * 16 + r) * D + col];
+            den += e * s_ml[(w * 16 + r) * 2 + 1];
+        }
+        const size_t pr = part_row + (size_t)r * max_splits;
+        a.part_o[pr * D + col] = den > 0.f ? num / den : 0.f;
+        if (col == 0) {
+            a.part_ml[2 * pr] = M;
+            a.part_ml[2 * pr + 1] = den;
+        }
+    }
+}
+
 // out[b][h] = sum_s 2^(m_s - M) l_s o_s / sum_s 2^(m_s - M) l_s over the splits of (b, h)
 __global__ void attn_decode_combine_kernel(const AttnDecodeArgs a, int max_splits) {
     pdl_wait();
@@ -388,6 +694,36 @@ cudaError_t decode_for(const AttnDecodeArgs& a, cudaStream_t stream) {
     return record(cudaGetLastError(), "attn_decode_combine_kernel launch");
 }
 
+cudaError_t decode_q8(const AttnDecodeArgs& a, cudaStream_t stream) {
+    constexpr int D = 128, BN = 64, STAGES = 4;
+    const int max_splits = attn_decode_max_splits(a.max_blocks, a.block_size);
+    const size_t smem = (size_t)STAGES * 2 * BN * D + STAGES * 2 * BN * 4 + 16 * D * 2 + 4 * 2 * 16 * D * 2 + 1024;
+    static bool configured = false;
+    if (!configured) {
+        cudaError_t e = cudaFuncSetAttribute(attn_decode_split_q8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)smem);
+        if (e != cudaSuccess) return record(e, "cudaFuncSetAttribute(attn_decode_split_q8_kernel)");
+        configured = true;
+    }
+    CUtensorMap tmK, tmV;
+    const uint64_t rows = (uint64_t)a.num_blocks * a.n_kv_heads * a.block_size;
+    const uint32_t box_rows = (uint32_t)std::min(a.block_size, BN);
+    if (!make_tmap_u8_sw128(&tmK, a.k_q8, rows, box_rows) || !make_tmap_u8_sw128(&tmV, a.v_q8, rows, box_rows))
+        return cudaErrorInvalidValue;
+    dim3 grid(max_splits, a.n_kv_heads, a.batch);
+    trace_before("attn_decode_split", stream);
+    cudaError_t e = launch_pdl(attn_decode_split_q8_kernel, grid, dim3(160), smem, stream, 1, tmK, tmV, a,
+                               max_splits);
+    trace_after(stream);
+    if (e == cudaSuccess) e = cudaGetLastError();
+    if (e != cudaSuccess) return record(e, "attn_decode_split_q8_kernel launch");
+    trace_before("attn_decode_combine", stream);
+    e = launch_pdl(attn_decode_combine_kernel, dim3(a.n_heads, a.batch), dim3(D), 0, stream, 1, a, max_splits);
+    trace_after(stream);
+    if (e != cudaSuccess) return record(e, "attn_decode_combine_kernel launch");
+    return record(cudaGetLastError(), "attn_decode_combine_kernel launch");
+}
+
 }  // namespace
 
 int attn_decode_max_splits(int max_blocks, int block_size) {
@@ -399,6 +735,12 @@ size_t attn_decode_scratch_bytes(int batch, int n_heads, int head_dim, int max_b
                                  int block_size) {
     const size_t rows = (size_t)batch * n_heads * attn_decode_max_splits(max_blocks, block_size);
     return rows * head_dim * sizeof(float) + rows * 2 * sizeof(float);
+}
+
+cudaError_t launch_attn_decode_q8(const AttnDecodeArgs& a, cudaStream_t stream) {
+    if (a.batch <= 0) return cudaSuccess;
+    if (a.head_dim != 128) return cudaErrorInvalidValue;
+    return decode_q8(a, stream);
 }
 
 cudaError_t launch_attn_decode(const AttnDecodeArgs& a, cudaStream_t stream) {

@@ -937,6 +937,29 @@ bool make_tmap_bf16_sw128(CUtensorMap* m, const void* ptr, uint64_t inner, uint6
     return true;
 }
 
+bool make_tmap_u8_sw128(CUtensorMap* m, const void* ptr, uint64_t rows, uint32_t box_rows) {
+    auto fn = encode_fn();
+    if (!fn) {
+        set_last_error("cuTensorMapEncodeTiled", "driver entry point not found");
+        return false;
+    }
+    cuuint64_t dims[2] = {128, rows};
+    cuuint64_t strides[1] = {128};
+    cuuint32_t box[2] = {128, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        char msg[160];
+        snprintf(msg, sizeof(msg), "CUresult %d (uint8 rows %llu, box 128 x %u)", (int)r, (unsigned long long)rows,
+                 box_rows);
+        set_last_error("cuTensorMapEncodeTiled", msg);
+        return false;
+    }
+    return true;
+}
+
 int device_sm_count() {
     int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return -1;

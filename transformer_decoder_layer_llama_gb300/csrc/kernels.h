@@ -98,6 +98,10 @@ cudaError_t launch_gemm(const GemmProblem& p, cudaStream_t stream);
 bool make_tmap_bf16_sw128(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t rows,
                           uint32_t box_rows);
 
+// Tensor map of 128-byte rows of bytes [rows, 128] (an INT8 K/V pool with head_dim
+// 128) read in boxes of box_rows full rows with the 128-byte swizzle.
+bool make_tmap_u8_sw128(CUtensorMap* m, const void* ptr, uint64_t rows, uint32_t box_rows);
+
 int device_sm_count();
 
 // Records why the current call failed (thread-local; read by ll_last_error).
@@ -118,6 +122,16 @@ cudaError_t launch_rmsnorm(const __nv_bfloat16* x, const float* g, __nv_bfloat16
 cudaError_t launch_rmsnorm_f32(const float* x, const float* g, __nv_bfloat16* out, int tokens,
                                int hidden, float eps, cudaStream_t stream);
 
+// ReshapeAndCache into an INT8 pool (one warp per token and KV head: absmax, float32
+// scale = absmax / 127, round-half-even codes).  A token's slot comes from `slots`
+// when non-null, else from its position (positions[t], or context_lens[t / seq_len] - 1
+// when positions is null) through block_table (sequence t / seq_len).
+cudaError_t launch_reshape_and_cache_q8(const __nv_bfloat16* k, const __nv_bfloat16* v, const int32_t* slots,
+                                        const int32_t* positions, const int32_t* context_lens,
+                                        const int32_t* block_table, int max_blocks, int seq_len, int tokens,
+                                        int n_kv_heads, int head_dim, int block_size, int8_t* k_pool,
+                                        int8_t* v_pool, float* k_scale, float* v_scale, int num_blocks,
+                                        int32_t* status, cudaStream_t stream);
 cudaError_t launch_reshape_and_cache(const __nv_bfloat16* k, const __nv_bfloat16* v,
                                      const int32_t* slots, int tokens, int n_kv_heads, int head_dim,
                                      int block_size, __nv_bfloat16* k_pool, __nv_bfloat16* v_pool,
@@ -150,11 +164,17 @@ struct AttnDecodeArgs {
     float* part_o;                 // scratch [batch, n_heads, max_splits, d]
     float* part_ml;                // scratch [batch, n_heads, max_splits, 2]
     int32_t* status;
+    const int8_t* k_q8;            // INT8 pool codes (launch_attn_decode_q8) ...
+    const int8_t* v_q8;
+    const float* k_scale;          // ... and their scales [num_blocks, n_kv_heads, block_size]
+    const float* v_scale;
 };
 int attn_decode_max_splits(int max_blocks, int block_size);
 size_t attn_decode_scratch_bytes(int batch, int n_heads, int head_dim, int max_blocks,
                                  int block_size);
 cudaError_t launch_attn_decode(const AttnDecodeArgs& a, cudaStream_t stream);
+// Decode attention over an INT8 pool (k_q8/v_q8 + scales; head_dim 128).
+cudaError_t launch_attn_decode_q8(const AttnDecodeArgs& a, cudaStream_t stream);
 
 // Weight packing helpers.
 cudaError_t launch_pack_rows(const __nv_bfloat16* src, __nv_bfloat16* dst, int rows, int cols,

@@ -115,6 +115,73 @@ __global__ void reshape_and_cache_kernel(const uint4* __restrict__ k, const uint
     v_pool[dst] = v[idx];
 }
 
+// ReshapeAndCache into an INT8 pool: one warp per (token, KV head) row of
+// head_dim values, E = head_dim / 32 per lane.  scale = absmax / 127 and
+// code = round-half-even(x / scale) in float32 with IEEE division (the same
+// decisions as the reference quantiser); a zero row gets scale 0, codes 0.
+template <int E>
+__global__ void reshape_and_cache_q8_kernel(const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __restrict__ v,
+                                            const int32_t* __restrict__ slots, const int32_t* __restrict__ positions,
+                                            const int32_t* __restrict__ context_lens,
+                                            const int32_t* __restrict__ block_table, int max_blocks, int seq_len,
+                                            int tokens, int n_kv_heads, int block_size, int8_t* __restrict__ k_pool,
+                                            int8_t* __restrict__ v_pool, float* __restrict__ k_scale,
+                                            float* __restrict__ v_scale, int num_blocks, int32_t* status) {
+    pdl_wait();
+    pdl_trigger();
+    const long long row = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    if (row >= (long long)tokens * n_kv_heads) return;          // whole warps
+    const int t = (int)(row / n_kv_heads), h = (int)(row - (long long)t * n_kv_heads);
+    constexpr int D = 32 * E;
+    long long slot;
+    if (slots) {
+        slot = slots[t];
+    } else {
+        const int seq = t / seq_len;
+        const int pos = positions ? positions[t] : context_lens[seq] - 1;
+        if (pos < 0 || pos / block_size >= max_blocks) {
+            if (h == 0 && lane == 0) flag_status(status, LL_DEV_BAD_POSITION);
+            return;
+        }
+        const int blk = block_table[(size_t)seq * max_blocks + pos / block_size];
+        slot = blk < 0 ? (long long)num_blocks * block_size : (long long)blk * block_size + pos % block_size;
+    }
+    if (slot < 0) return;
+    if (slot >= (long long)num_blocks * block_size) {
+        if (h == 0 && lane == 0) flag_status(status, slots ? LL_DEV_BAD_SLOT : LL_DEV_BAD_BLOCK);
+        return;
+    }
+    const long long blk = slot / block_size;
+    const int off = (int)(slot - blk * block_size);
+    const size_t srow = (size_t)row * D + lane * E;
+    const size_t drow = (((size_t)blk * n_kv_heads + h) * block_size + off);
+#pragma unroll
+    for (int kv = 0; kv < 2; ++kv) {
+        const __nv_bfloat16* src = (kv ? v : k) + srow;
+        float x[E];
+        float amax = 0.f;
+#pragma unroll
+        for (int i = 0; i < E; ++i) {
+            x[i] = __bfloat162float(src[i]);
+            amax = fmaxf(amax, fabsf(x[i]));
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+        const float sc = __fdiv_rn(amax, 127.f);
+        int8_t q[E];
+#pragma unroll
+        for (int i = 0; i < E; ++i) {
+            int c = sc > 0.f ? __float2int_rn(__fdiv_rn(x[i], sc)) : 0;
+            q[i] = (int8_t)min(127, max(-127, c));
+        }
+        int8_t* dst = (kv ? v_pool : k_pool) + drow * D + lane * E;
+#pragma unroll
+        for (int i = 0; i < E; ++i) dst[i] = q[i];
+        if (lane == 0) (kv ? v_scale : k_scale)[drow] = sc;
+    }
+}
+
 // Packs rows of a [rows, cols] matrix.  mode 0: copy.  mode 1: the merged QKV
 // weight, whose first q_k_rows rows (the Q and K heads) are reordered inside
 // each head so that packed row 2i holds element i and row 2i+1 holds element
@@ -219,6 +286,37 @@ cudaError_t launch_reshape_and_cache(const __nv_bfloat16* k, const __nv_bfloat16
         (long long)num_blocks * block_size, status);
     trace_after(stream);
     return record(cudaGetLastError(), "reshape_and_cache launch");
+}
+
+cudaError_t launch_reshape_and_cache_q8(const __nv_bfloat16* k, const __nv_bfloat16* v, const int32_t* slots,
+                                        const int32_t* positions, const int32_t* context_lens,
+                                        const int32_t* block_table, int max_blocks, int seq_len, int tokens,
+                                        int n_kv_heads, int head_dim, int block_size, int8_t* k_pool,
+                                        int8_t* v_pool, float* k_scale, float* v_scale, int num_blocks,
+                                        int32_t* status, cudaStream_t stream) {
+    if (tokens <= 0) return cudaSuccess;
+    const long long threads = (long long)tokens * n_kv_heads * 32;
+    trace_before("reshape_and_cache_q8", stream);
+    cudaError_t e = cudaErrorInvalidValue;
+#define LL_Q8_LAUNCH(E_)                                                                                    \
+    e = launch_pdl(reshape_and_cache_q8_kernel<E_>, dim3(blocks_for(threads, 256)), dim3(256), 0, stream, 1, \
+                   k, v, slots, positions, context_lens, block_table, max_blocks, seq_len, tokens,            \
+                   n_kv_heads, block_size, k_pool, v_pool, k_scale, v_scale, num_blocks, status)
+    switch (head_dim) {
+        case 32: LL_Q8_LAUNCH(1); break;
+        case 64: LL_Q8_LAUNCH(2); break;
+        case 96: LL_Q8_LAUNCH(3); break;
+        case 128: LL_Q8_LAUNCH(4); break;
+        case 160: LL_Q8_LAUNCH(5); break;
+        case 192: LL_Q8_LAUNCH(6); break;
+        case 224: LL_Q8_LAUNCH(7); break;
+        case 256: LL_Q8_LAUNCH(8); break;
+        default: break;
+    }
+#undef LL_Q8_LAUNCH
+    trace_after(stream);
+    if (e != cudaSuccess) return record(e, "reshape_and_cache_q8 launch");
+    return record(cudaGetLastError(), "reshape_and_cache_q8 launch");
 }
 
 cudaError_t launch_pack_rows(const __nv_bfloat16* src, __nv_bfloat16* dst, int rows, int cols,
