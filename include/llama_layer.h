@@ -95,6 +95,18 @@ typedef struct {
     int32_t num_blocks;
 } ll_kv_pool;
 
+/* An INT8 KV pool (paging page, section "KV Cache quantisation": per-token
+ * granularity, each token's K and V with their own float32 scale).  Codes in the
+ * layout of ll_kv_pool; one scale per token and KV head.  A cached row reads back
+ * as code * scale. */
+typedef struct {
+    void* k;              /* int8 [num_blocks, n_kv_heads, block_size, head_dim] */
+    void* v;              /* same shape */
+    float* k_scale;       /* float32 [num_blocks, n_kv_heads, block_size] */
+    float* v_scale;       /* same shape */
+    int32_t num_blocks;
+} ll_kv_pool_q8;
+
 /* Human-readable name of an LL_ERR_* code (static string). */
 const char* ll_strerror(int code);
 
@@ -168,6 +180,16 @@ int ll_layer_decode_step(const ll_config* cfg, const void* packed, const void* x
                          const int32_t* context_lens, int32_t batch, void* y, void* workspace,
                          size_t workspace_bytes, int32_t* status, void* stream);
 
+/* ll_layer_decode_step over an INT8 pool: the new tokens' K and V (after RoPE,
+ * BF16) are quantised into the pool as ll_reshape_and_cache_q8 does, and the
+ * attention reads code * scale (ll_paged_attention_decode_q8).  head_dim 128;
+ * workspace from ll_workspace_size; other arguments as ll_layer_decode_step.
+ * (Prefill into an INT8 pool is not provided.) */
+int ll_layer_decode_step_q8(const ll_config* cfg, const void* packed, const void* x, const ll_kv_pool_q8* pool,
+                            const int32_t* block_table, int32_t max_blocks, const int32_t* context_lens,
+                            int32_t batch, void* y, void* workspace, size_t workspace_bytes, int32_t* status,
+                            void* stream);
+
 /* ReshapeAndCache (paging page, section "KV Cache memory wall",
  * ReshapeAndCacheOperation): k, v BF16 [tokens, n_kv_heads, head_dim];
  * slot_mapping int32 [tokens]; token t's rows go to
@@ -178,17 +200,6 @@ int ll_reshape_and_cache(const void* k, const void* v, const int32_t* slot_mappi
                          int32_t n_kv_heads, int32_t head_dim, int32_t block_size,
                          const ll_kv_pool* pool, int32_t* status, void* stream);
 
-/* An INT8 KV pool (paging page, section "KV Cache quantisation": per-token
- * granularity, each token's K and V with their own float32 scale).  Codes in the
- * layout of ll_kv_pool; one scale per token and KV head.  A cached row reads back
- * as code * scale. */
-typedef struct {
-    void* k;              /* int8 [num_blocks, n_kv_heads, block_size, head_dim] */
-    void* v;              /* same shape */
-    float* k_scale;       /* float32 [num_blocks, n_kv_heads, block_size] */
-    float* v_scale;       /* same shape */
-    int32_t num_blocks;
-} ll_kv_pool_q8;
 
 /* ReshapeAndCache into an INT8 pool, quantising online: for token t and KV head h,
  * scale = max_i |row_i| / 127 and code_i = round-half-even(row_i / scale) in

@@ -351,3 +351,34 @@ def test_paged_attention_decode_q8_bad_block_is_flagged_and_finite():
     torch.cuda.synchronize()
     assert int(status.item()) & api.LL_DEV_BAD_BLOCK
     assert torch.isfinite(out.float()).all()
+
+
+def test_layer_decode_steps_over_int8_cache():
+    """Decode steps of a GQA layer (head_dim 128) over a pre-filled INT8 pool: each step
+    quantises the new token's K/V into the pool and attends over code * scale."""
+    d = synth.LayerDims(512, 4, 2, 128, 1024, 16)
+    B, steps = 3, 4
+    W = synth.make_weights(d, 0.02, seed=91)
+    Wn = {k: f64(v) for k, v in W.items()}
+    ctx0 = synth.make_context_lens(B, 20, 140, seed=92)
+    table, nb = synth.make_block_table((ctx0 + steps).tolist(), d.block_size, seed=93, extra_blocks=2)
+    kc, vc, ks, vs = _random_q8_pool(nb, d.n_kv_heads, d.block_size, d.head_dim, seed=94)
+    pool = api.PoolQ8(kc.to(DEV), vc.to(DEV), ks.to(DEV), vs.to(DEV))
+    qk, qv = O.QuantPool(kc.numpy().copy(), ks.numpy().copy()), O.QuantPool(vc.numpy().copy(), vs.numpy().copy())
+    cfg = api.make_config(d, max_position=int(ctx0.max()) + steps + 1)
+    packed = api.pack_weights(cfg, {k: v.to(DEV) for k, v in W.items()})
+    td = table.to(DEV)
+    status = api.new_status()
+    for step in range(steps):
+        ctx = (ctx0 + step + 1).to(torch.int32)
+        x = synth.make_x(B, d.hidden, seed=95 + step)
+        y = api.layer_decode_step_q8(cfg, packed, x.to(DEV), pool, td, ctx.to(DEV), status=status)
+        torch.cuda.synchronize()
+        y_ref = O.layer_decode_step(d, Wn, f64(x), qk, qv, table.numpy(), ctx.numpy())
+        assert int(status.item()) == 0
+        assert_close(f64(y), y_ref, f"INT8-cache decode step {step}")
+    # the appended rows: codes within one step of the oracle's (its K/V may round the other
+    # way in a last bit), scales within a few parts in a thousand
+    gk, gs = pool.k.cpu().numpy(), pool.k_scale.cpu().numpy()
+    assert np.abs(gk.astype(np.int32) - qk.codes.astype(np.int32)).max() <= 1
+    np.testing.assert_allclose(gs, qk.scales, rtol=5e-3)

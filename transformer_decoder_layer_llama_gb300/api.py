@@ -32,6 +32,7 @@ EXPORTED = [
     "ll_linear", "ll_device_sm_count", "ll_trace_begin", "ll_trace_end", "ll_trace_elapsed_ms",
     "ll_trace_name", "ll_paged_attention_decode_noalloc", "ll_selftest_bounded_wait",
     "ll_workspace_checkpoints", "ll_reshape_and_cache_q8", "ll_paged_attention_decode_q8",
+    "ll_layer_decode_step_q8",
 ]
 
 
@@ -98,6 +99,8 @@ def _load():
                                                    P, P]),
         "ll_paged_attention_decode_q8": (ctypes.c_int, [P, ctypes.POINTER(ll_kv_pool_q8), P, I32, P, I32, I32, I32,
                                                         I32, I32, ctypes.c_float, P, P, S, P, P]),
+        "ll_layer_decode_step_q8": (ctypes.c_int, [cfgp, P, P, ctypes.POINTER(ll_kv_pool_q8), P, I32, P, I32, P, P,
+                                                   S, P, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -266,6 +269,28 @@ def layer_decode_step(cfg, packed, x, k_pool, v_pool, block_table, context_lens,
         ctypes.byref(cfg), _ptr(packed), _ptr(x), ctypes.byref(pool), _ptr(block_table),
         block_table.shape[1], _ptr(context_lens), B, _ptr(y), _ptr(workspace), workspace.numel(),
         _ptr(status), _stream(stream)))
+    return y
+
+
+def layer_decode_step_q8(cfg, packed, x, pool, block_table, context_lens, y=None, workspace=None, status=None,
+                         stream=None):
+    """ll_layer_decode_step_q8 over an INT8 pool (PoolQ8).  Returns y (BF16 [batch, hidden])."""
+    B = x.shape[0]
+    _need(x, "x", torch.bfloat16, shape=(B, cfg.hidden))
+    _need(context_lens, "context_lens", torch.int32, shape=(B,))
+    _need(block_table, "block_table", torch.int32)
+    if block_table.dim() != 2 or block_table.shape[0] < B:
+        raise ValueError("block_table must be [batch, max_blocks]")
+    cp = pool.c()
+    if y is None:
+        y = torch.empty_like(x)
+    if workspace is None:
+        workspace = new_workspace(cfg, B, block_table.shape[1], x.device)
+    if status is None:
+        status = new_status(x.device)
+    _check("ll_layer_decode_step_q8", lib.ll_layer_decode_step_q8(
+        ctypes.byref(cfg), _ptr(packed), _ptr(x), ctypes.byref(cp), _ptr(block_table), block_table.shape[1],
+        _ptr(context_lens), B, _ptr(y), _ptr(workspace), workspace.numel(), _ptr(status), _stream(stream)))
     return y
 
 

@@ -100,7 +100,7 @@ Packed packed_view(const ll_config* c, const void* base) {
 
 // Workspace of a layer call over T tokens with block tables max_blocks wide.
 struct WsLayout {
-    size_t xh, q, o, h, hh, a, partials, counters, attn, total;
+    size_t xh, q, o, h, hh, a, kst, vst, partials, counters, attn, total;
     size_t partial_bytes;
     int counter_words;       // per GEMM
 };
@@ -117,6 +117,10 @@ WsLayout ws_layout(const ll_config* c, int T, int max_blocks) {
     L.h = at;  at = align_up(at + (size_t)T * H * 4);   // float32 residual stream
     L.hh = at; at = align_up(at + (size_t)T * H * 2);
     L.a = at;  at = align_up(at + (size_t)T * I * 2);
+    // the new tokens' K and V before quantisation into an INT8 pool
+    const size_t kv_row = (size_t)c->n_kv_heads * c->head_dim * 2;
+    L.kst = at; at = align_up(at + (size_t)T * kv_row);
+    L.vst = at; at = align_up(at + (size_t)T * kv_row);
     L.partial_bytes = ll::gemm_partial_bound_bytes(T);
     L.partials = at; at = align_up(at + L.partial_bytes);
     L.counter_words = std::max({ll::gemm_counter_bound(nqkv), ll::gemm_counter_bound((int)H),
@@ -140,7 +144,8 @@ bool pool_ok(const ll_kv_pool* p) {
 int run_layer(const ll_config* cfg, const void* packed, const void* x, const int32_t* positions,
               const int32_t* context_lens, int T, int seq_len, int batch, const ll_kv_pool* pool,
               const int32_t* block_table, int max_blocks, void* y, void* workspace,
-              size_t workspace_bytes, int32_t* status, cudaStream_t stream, bool decode) {
+              size_t workspace_bytes, int32_t* status, cudaStream_t stream, bool decode,
+              const ll_kv_pool_q8* pq8 = nullptr) {
     WsLayout L = ws_layout(cfg, T, max_blocks);
     if (!workspace || workspace_bytes < L.total || !aligned16(workspace)) return LL_ERR_WORKSPACE;
     Packed P = packed_view(cfg, packed);
@@ -179,21 +184,37 @@ int run_layer(const ll_config* cfg, const void* packed, const void* x, const int
     g.counters = counters;
     g.ep.kind = ll::EPI_QKV;
     g.ep.q_out = q;
-    g.ep.k_pool = static_cast<__nv_bfloat16*>(pool->k);
-    g.ep.v_pool = static_cast<__nv_bfloat16*>(pool->v);
     g.ep.positions = decode ? nullptr : positions;
     g.ep.context_lens = decode ? context_lens : nullptr;
     g.ep.block_table = block_table;
     g.ep.max_blocks = max_blocks;
     g.ep.seq_len = seq_len;
-    g.ep.num_blocks = pool->num_blocks;
-    g.ep.block_size = cfg->block_size;
+    if (pq8) {
+        // K/V go to staging rows, then into the INT8 pool with their scales
+        g.ep.kv_stage = 1;
+        g.ep.k_pool = reinterpret_cast<__nv_bfloat16*>(ws + L.kst);
+        g.ep.v_pool = reinterpret_cast<__nv_bfloat16*>(ws + L.vst);
+        g.ep.num_blocks = pq8->num_blocks;
+        g.ep.block_size = 1;
+    } else {
+        g.ep.k_pool = static_cast<__nv_bfloat16*>(pool->k);
+        g.ep.v_pool = static_cast<__nv_bfloat16*>(pool->v);
+        g.ep.num_blocks = pool->num_blocks;
+        g.ep.block_size = cfg->block_size;
+    }
     g.ep.n_heads = cfg->n_heads;
     g.ep.n_kv_heads = cfg->n_kv_heads;
     g.ep.head_dim = d;
     g.ep.max_position = cfg->max_position;
     g.ep.rope_cs = P.rope;
     if ((e = ll::launch_gemm(g, stream)) != cudaSuccess) return LL_ERR_CUDA;
+    if (pq8 &&
+        (e = ll::launch_reshape_and_cache_q8(g.ep.k_pool, g.ep.v_pool, nullptr, decode ? nullptr : positions,
+                                             decode ? context_lens : nullptr, block_table, max_blocks, seq_len, T,
+                                             cfg->n_kv_heads, d, cfg->block_size, static_cast<int8_t*>(pq8->k),
+                                             static_cast<int8_t*>(pq8->v), pq8->k_scale, pq8->v_scale,
+                                             pq8->num_blocks, status, stream)) != cudaSuccess)
+        return LL_ERR_CUDA;
 
     // attention
     const float scale = 1.0f / std::sqrt((float)d);
@@ -219,12 +240,19 @@ int run_layer(const ll_config* cfg, const void* packed, const void* x, const int
     } else {
         ll::AttnDecodeArgs at{};
         at.q = q;
-        at.k_pool = g.ep.k_pool;
-        at.v_pool = g.ep.v_pool;
+        if (pq8) {
+            at.k_q8 = static_cast<const int8_t*>(pq8->k);
+            at.v_q8 = static_cast<const int8_t*>(pq8->v);
+            at.k_scale = pq8->k_scale;
+            at.v_scale = pq8->v_scale;
+        } else {
+            at.k_pool = g.ep.k_pool;
+            at.v_pool = g.ep.v_pool;
+        }
         at.context_lens = context_lens;
         at.block_table = block_table;
         at.max_blocks = max_blocks;
-        at.num_blocks = pool->num_blocks;
+        at.num_blocks = g.ep.num_blocks;
         at.block_size = cfg->block_size;
         at.batch = batch;
         at.n_heads = cfg->n_heads;
@@ -237,7 +265,8 @@ int run_layer(const ll_config* cfg, const void* packed, const void* x, const int
         at.part_o = reinterpret_cast<float*>(ws + L.attn);
         at.part_ml = at.part_o + rows * d;
         at.status = status;
-        if ((e = ll::launch_attn_decode(at, stream)) != cudaSuccess) return LL_ERR_CUDA;
+        if ((e = pq8 ? ll::launch_attn_decode_q8(at, stream) : ll::launch_attn_decode(at, stream)) != cudaSuccess)
+            return LL_ERR_CUDA;
     }
 
     // O projection + residual
@@ -567,6 +596,22 @@ int ll_paged_attention_decode_q8(const void* q, const ll_kv_pool_q8* pool, const
     at.part_ml = at.part_o + rows * head_dim;
     at.status = status;
     return cuda_rc(ll::launch_attn_decode_q8(at, static_cast<cudaStream_t>(stream)));
+}
+
+int ll_layer_decode_step_q8(const ll_config* cfg, const void* packed, const void* x, const ll_kv_pool_q8* pool,
+                            const int32_t* block_table, int32_t max_blocks, const int32_t* context_lens,
+                            int32_t batch, void* y, void* workspace, size_t workspace_bytes, int32_t* status,
+                            void* stream) {
+    ll::clear_last_error();
+    int rc = config_supported(cfg);
+    if (rc != LL_OK) return rc;
+    if (cfg->head_dim != 128) return LL_ERR_UNSUPPORTED;
+    if (!packed || !x || !context_lens || !block_table || !y || !status || !pool_q8_ok(pool))
+        return LL_ERR_INVALID_ARG;
+    if (batch <= 0 || max_blocks <= 0 || x == y) return LL_ERR_INVALID_ARG;
+    if (!aligned16(packed) || !aligned16(x) || !aligned16(y)) return LL_ERR_INVALID_ARG;
+    return run_layer(cfg, packed, x, nullptr, context_lens, batch, 1, batch, nullptr, block_table, max_blocks, y,
+                     workspace, workspace_bytes, status, static_cast<cudaStream_t>(stream), true, pool);
 }
 
 int ll_paged_attention_decode(const void* q, const ll_kv_pool* pool, const int32_t* block_table,

@@ -78,6 +78,10 @@ LL_DEVINL TokenSlot token_slot(const EpiParams& ep, int t) {
         return s;
     }
     s.pos = pos;
+    if (ep.kv_stage) {                           // staging rows [token][kv head]
+        s.kv_row = (long long)t * ep.n_kv_heads;
+        return s;
+    }
     int seq = t / ep.seq_len;
     int lb = pos / ep.block_size;
     if (lb >= ep.max_blocks) {

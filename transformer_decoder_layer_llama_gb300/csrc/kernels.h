@@ -54,8 +54,9 @@ struct EpiParams {
     float* out_f32;                // RESID: float32 destination [tokens, n] instead of `out`
     // EPI_QKV
     __nv_bfloat16* q_out;          // [tokens, n_heads * head_dim]
-    __nv_bfloat16* k_pool;
-    __nv_bfloat16* v_pool;
+    __nv_bfloat16* k_pool;         // the paged pool, or with kv_stage a staging buffer
+    __nv_bfloat16* v_pool;         // [tokens, n_kv_heads, head_dim] (block_size then 1)
+    int kv_stage;
     const int32_t* positions;      // prefill: position of each token (null in decode)
     const int32_t* context_lens;   // decode: position = context_lens[token] - 1
     const int32_t* block_table;
