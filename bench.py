@@ -96,6 +96,11 @@ def kv_bytes_read(d, ctx):
     return 2.0 * d.n_kv_heads * d.head_dim * 2 * float(np.sum(ctx, dtype=np.float64))
 
 
+def kv_bytes_read_q8(d, ctx):
+    """INT8 cache: one byte per K and V element plus a float32 scale per token, head and K/V."""
+    return 2.0 * d.n_kv_heads * (d.head_dim + 4) * float(np.sum(ctx, dtype=np.float64))
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -255,6 +260,29 @@ class Decode:
 
     def roofline_s(self, peaks):
         return max(self.flops / (peaks["bf16_tflops"] * 1e12), self.min_bytes / (peaks["hbm_gbs"] * 1e9))
+
+
+class DecodeQ8(Decode):
+    """The decode workload over an INT8 pool: codes ~U{-127..127}, scales ~U(0.001, 0.031)."""
+
+    def __init__(self, api, wl, seed):
+        super().__init__(api, wl, seed)
+        d = self.d
+        nb = self.kp.shape[0]
+        del self.kp, self.vp
+        gen = torch.Generator(device="cuda")
+        gen.manual_seed(seed + 5)
+        shape = (nb, d.n_kv_heads, d.block_size, d.head_dim)
+        codes = lambda: torch.randint(-127, 128, shape, generator=gen, device="cuda", dtype=torch.int8)
+        scales = lambda: torch.rand(shape[:3], generator=gen, device="cuda") * 0.03 + 0.001
+        self.pool = api.PoolQ8(codes(), codes(), scales(), scales())
+        self.kv_read = kv_bytes_read_q8(d, self.ctx_np)
+        self.min_bytes = (weight_bytes(d) + self.kv_read + 2 * self.B * d.hidden * 2
+                          + self.B * 2 * d.n_kv_heads * (d.head_dim + 4))
+
+    def step(self, stream):
+        self.api.layer_decode_step_q8(self.cfg, self.packed, self.x, self.pool, self.table, self.ctx, y=self.y,
+                                      workspace=self.ws, status=self.status, stream=stream)
 
 
 def continuous_batching(api, wl, steps, warmup, stream, peaks, seed=4321):
@@ -489,7 +517,8 @@ def main():
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle CPU baseline")
     ap.add_argument("--no-stack", action="store_true", help="skip the 32-layer continuous batching")
     ap.add_argument("--ncu-target", choices=["llama2_7b_prefill", "llama2_7b_decode",
-                                             "llama70b_gqa_decode"],
+                                             "llama70b_gqa_decode", "llama2_7b_decode_int8kv",
+                                             "llama70b_gqa_decode_int8kv"],
                     help="set up one workload, run --calls untimed layer calls and exit (for ncu)")
     ap.add_argument("--calls", type=int, default=2)
     args = ap.parse_args()
@@ -497,8 +526,11 @@ def main():
         from transformer_decoder_layer_llama_gb300 import api
         torch.cuda.set_device(0)
         st = torch.cuda.Stream()
-        wl = synth.WORKLOADS[args.ncu_target]
-        w = Prefill(api, wl, 1234) if wl.prefill_len else Decode(api, wl, 99)
+        wl = synth.WORKLOADS[args.ncu_target.replace("_int8kv", "")]
+        if wl.prefill_len:
+            w = Prefill(api, wl, 1234)
+        else:
+            w = (DecodeQ8 if args.ncu_target.endswith("_int8kv") else Decode)(api, wl, 99)
         for _ in range(args.calls):
             w.step(st)
         st.synchronize()
@@ -626,9 +658,11 @@ def main():
 
     if not args.no_extras:
         extras = {}
-        for name in ("llama2_7b_decode", "llama70b_gqa_decode"):
-            w2 = synth.WORKLOADS[name]
-            dw = Decode(api, w2, seed=99 + rank)
+        for name in ("llama2_7b_decode", "llama70b_gqa_decode", "llama2_7b_decode_int8kv",
+                     "llama70b_gqa_decode_int8kv"):
+            q8 = name.endswith("_int8kv")
+            w2 = synth.WORKLOADS[name.replace("_int8kv", "")]
+            dw = (DecodeQ8 if q8 else Decode)(api, w2, seed=99 + rank)
             for _ in range(args.warmup):
                 dw.step(stream)
             stream.synchronize()

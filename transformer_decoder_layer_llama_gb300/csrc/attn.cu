@@ -357,6 +357,7 @@ __global__ void __launch_bounds__(160, 2)
     uint8_t* sq = reinterpret_cast<uint8_t*>(ssc + STAGES * 2 * BN);   // [16][D] FP16 q, swizzled rows
     uint8_t* sh = sq + 16 * D * 2;                     // [4 warps][K, V][16][D] FP16 codes, swizzled rows
     __shared__ uint64_t full_bar[STAGES], empty_bar[STAGES];
+    __shared__ unsigned long long valid_s[STAGES];     // per stage: bit k = key k of the tile is cached
     __shared__ int abort_s;
 
     const int split = blockIdx.x, hk = blockIdx.y, b = blockIdx.z;
@@ -406,10 +407,16 @@ __global__ void __launch_bounds__(160, 2)
                 if (!mbar_wait_bounded(&empty_bar[st], ph ^ 1u, &abort_s, a.status)) break;
                 const int p0 = k_begin + kt * BN;
                 uint32_t bytes = 0;
-                for (int p = p0; p < p0 + BN && p < k_end; p += kt_rows) {
+                unsigned long long valid = 0;
+                for (int p = p0, sb = 0; p < p0 + BN && p < k_end; p += kt_rows, ++sb) {
                     const int blk = table_row[p / a.block_size];
-                    if (blk >= 0 && blk < a.num_blocks) bytes += 2u * kt_rows * (128u + 4u);
+                    if (blk >= 0 && blk < a.num_blocks) {
+                        bytes += 2u * kt_rows * (128u + 4u);
+                        const int nk = min(kt_rows, k_end - p);
+                        valid |= (nk == 64 ? ~0ull : ((1ull << nk) - 1ull)) << (sb * kt_rows);
+                    }
                 }
+                valid_s[st] = valid;                       // released by the arrive below
                 mbar_arrive_expect_tx(&full_bar[st], bytes);
                 for (int p = p0, sb = 0; p < p0 + BN && p < k_end; p += kt_rows, ++sb) {
                     const int blk = table_row[p / a.block_size];
@@ -474,21 +481,14 @@ __global__ void __launch_bounds__(160, 2)
         const int st = kt % STAGES;
         const uint32_t ph = (uint32_t)(kt / STAGES) & 1u;
         if (!mbar_wait_bounded(&full_bar[st], ph, &abort_s, a.status)) break;
-        // validity of this warp's 16 keys: inside the split and backed by a valid block
-        const int pbase = k_begin + kt * BN + warp * 16;
-        bool my_ok = false;
-        if (lane < 16) {
-            const int p = pbase + lane;
-            if (p < k_end) {
-                const int blk = table_row[p / a.block_size];
-                my_ok = blk >= 0 && blk < a.num_blocks;
-            }
-        }
-        const uint32_t okmask = __ballot_sync(0xffffffffu, my_ok) & 0xffffu;
+        // validity of this warp's 16 keys (inside the split and backed by a valid block), as
+        // the producer found it
+        const uint32_t okmask = (uint32_t)(valid_s[st] >> (warp * 16)) & 0xffffu;
         {
             // the warp's 16 rows of K and V codes -> FP16 (rows without a valid key -> 0);
-            // lane: row lane / 2, 16-code chunks 4 (lane & 1) .. + 3
-            const int rl = lane >> 1, R = warp * 16 + rl;
+            // lane: row lane % 16, 16-code chunks 4 (lane / 16) .. + 3 (spreads each store over
+            // all banks)
+            const int rl = lane & 15, R = warp * 16 + rl;
             const bool row_ok = (okmask >> rl) & 1u;
             __syncwarp();                              // the previous tile's reads are done
 #pragma unroll
@@ -497,7 +497,7 @@ __global__ void __launch_bounds__(160, 2)
                 uint8_t* dst = kv ? vh : kh;
 #pragma unroll
                 for (int jj = 0; jj < 4; ++jj) {
-                    const int j = (lane & 1) * 4 + jj;
+                    const int j = (lane >> 4) * 4 + jj;
                     uint4 o0 = make_uint4(0, 0, 0, 0), o1 = make_uint4(0, 0, 0, 0);
                     if (row_ok) {
                         const uint4 w = *reinterpret_cast<const uint4*>(src + R * 128 + ((j ^ (R & 7)) << 4));
@@ -548,7 +548,7 @@ __global__ void __launch_bounds__(160, 2)
         const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
         const float base0 = (mn0 == -INFINITY) ? 0.f : mn0;
         const float base1 = (mn1 == -INFINITY) ? 0.f : mn1;
-        const float al0 = exp2f(m0 - base0), al1 = exp2f(m1 - base1);
+        const float al0 = ex2_approx(m0 - base0), al1 = ex2_approx(m1 - base1);
         m0 = mn0;
         m1 = mn1;
         uint32_t pf[4];
@@ -557,10 +557,10 @@ __global__ void __launch_bounds__(160, 2)
             float p[2][4];
 #pragma unroll
             for (int nt = 0; nt < 2; ++nt) {
-                p[nt][0] = exp2f(s[nt][0] - base0);
-                p[nt][1] = exp2f(s[nt][1] - base0);
-                p[nt][2] = exp2f(s[nt][2] - base1);
-                p[nt][3] = exp2f(s[nt][3] - base1);
+                p[nt][0] = ex2_approx(s[nt][0] - base0);
+                p[nt][1] = ex2_approx(s[nt][1] - base0);
+                p[nt][2] = ex2_approx(s[nt][2] - base1);
+                p[nt][3] = ex2_approx(s[nt][3] - base1);
                 rs0 += p[nt][0] + p[nt][1];
                 rs1 += p[nt][2] + p[nt][3];
             }
