@@ -545,12 +545,26 @@ __global__ void __launch_bounds__(160, 2)
             mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
             mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
         }
-        const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-        const float base0 = (mn0 == -INFINITY) ? 0.f : mn0;
-        const float base1 = (mn1 == -INFINITY) ? 0.f : mn1;
-        const float al0 = ex2_approx(m0 - base0), al1 = ex2_approx(m1 - base1);
-        m0 = mn0;
-        m1 = mn1;
+        // The exponent base of a row moves only when its max grows by more than 2^8 (P then
+        // stays below 256); otherwise the running sums need no rescaling this tile.
+        if (__any_sync(0xffffffffu, mx0 > m0 + 8.f || mx1 > m1 + 8.f)) {
+            const float mn0 = mx0 > m0 + 8.f ? mx0 : m0, mn1 = mx1 > m1 + 8.f ? mx1 : m1;
+            const float al0 = mn0 == m0 ? 1.f : ex2_approx(m0 - mn0);
+            const float al1 = mn1 == m1 ? 1.f : ex2_approx(m1 - mn1);
+            l0 *= al0;
+            l1 *= al1;
+#pragma unroll
+            for (int i = 0; i < D / 8; ++i) {
+                acc[i][0] *= al0;
+                acc[i][1] *= al0;
+                acc[i][2] *= al1;
+                acc[i][3] *= al1;
+            }
+            m0 = mn0;
+            m1 = mn1;
+        }
+        const float base0 = (m0 == -INFINITY) ? 0.f : m0;
+        const float base1 = (m1 == -INFINITY) ? 0.f : m1;
         uint32_t pf[4];
         float rs0 = 0.f, rs1 = 0.f;
         {
@@ -570,15 +584,8 @@ __global__ void __launch_bounds__(160, 2)
             pf[2] = pack_f16x2(p[1][0] * vs[1][0], p[1][1] * vs[1][1]);
             pf[3] = pack_f16x2(p[1][2] * vs[1][0], p[1][3] * vs[1][1]);
         }
-        l0 = l0 * al0 + rs0;
-        l1 = l1 * al1 + rs1;
-#pragma unroll
-        for (int i = 0; i < D / 8; ++i) {
-            acc[i][0] *= al0;
-            acc[i][1] *= al0;
-            acc[i][2] *= al1;
-            acc[i][3] *= al1;
-        }
+        l0 += rs0;
+        l1 += rs1;
 #pragma unroll
         for (int dp = 0; dp < D / 16; ++dp) {
             uint32_t bfr[4];
