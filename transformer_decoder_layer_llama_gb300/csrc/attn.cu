@@ -344,10 +344,10 @@ __global__ void __launch_bounds__(160, 2)
 // the row sum stays the sum of the unscaled probabilities.  Q enters as FP16
 // (exact for BF16 values of FP16's range), P as one FP16 operand (the cache's
 // INT8 rounding dominates its error).
-__global__ void __launch_bounds__(160, 2)
+__global__ void __launch_bounds__(160, 3)
     attn_decode_split_q8_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                                 const AttnDecodeArgs a, int max_splits) {
-    constexpr int D = 128, BN = 64, STAGES = 4, NCONS = 128;
+    constexpr int D = 128, BN = 64, STAGES = 3, NCONS = 128;
     constexpr int TILE = BN * D;                       // bytes of one INT8 K or V tile
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sbase = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -355,7 +355,7 @@ __global__ void __launch_bounds__(160, 2)
     uint8_t* sv = sk + STAGES * TILE;                  // [STAGES][TILE]
     float* ssc = reinterpret_cast<float*>(sv + STAGES * TILE);   // [STAGES][2][BN] K, V scales
     uint8_t* sq = reinterpret_cast<uint8_t*>(ssc + STAGES * 2 * BN);   // [16][D] FP16 q, swizzled rows
-    uint8_t* sh = sq + 16 * D * 2;                     // [4 warps][K, V][16][D] FP16 codes, swizzled rows
+    uint8_t* sh = sq + 16 * D * 2;                     // [4 warps][16][D] FP16 codes (K, then V), swizzled
     __shared__ uint64_t full_bar[STAGES], empty_bar[STAGES];
     __shared__ unsigned long long valid_s[STAGES];     // per stage: bit k = key k of the tile is cached
     __shared__ int abort_s;
@@ -400,7 +400,7 @@ __global__ void __launch_bounds__(160, 2)
         if (lane == 0) {
             tma_prefetch_desc(&tmK);
             tma_prefetch_desc(&tmV);
-            uint32_t issued[STAGES] = {0, 0, 0, 0};
+            uint32_t issued[STAGES] = {0, 0, 0};
             for (int kt = 0; kt < n_kt; ++kt) {
                 const int st = kt % STAGES;
                 const uint32_t ph = (uint32_t)(kt / STAGES) & 1u;
@@ -460,15 +460,9 @@ __global__ void __launch_bounds__(160, 2)
         *reinterpret_cast<uint4*>(sq + swz<D>(r, c)) = o;
     }
     asm volatile("bar.sync 1, 128;" ::: "memory");
-    uint32_t qf[D / 16][4];
-    {
-        const uint32_t qb = smem_u32(sq);
-#pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) ldmatrix_x4(qf[ks], qb + swz<D>(lane & 15, ks * 2 + (lane >> 4)));
-    }
-    uint8_t* kh = sh + warp * (2 * 16 * D * 2);        // this warp's FP16 K rows
-    uint8_t* vh = kh + 16 * D * 2;                     // ... and V rows
-    const uint32_t khb = smem_u32(kh), vhb = smem_u32(vh);
+    const uint32_t qb = smem_u32(sq);                  // q fragments are re-read each tile (registers)
+    uint8_t* hbuf = sh + warp * (16 * D * 2);          // this warp's FP16 rows: K, then V
+    const uint32_t hb = smem_u32(hbuf);
 
     const float sl2 = a.scale * kLog2e;
     const int g = lane >> 2, cq = lane & 3;
@@ -484,44 +478,43 @@ __global__ void __launch_bounds__(160, 2)
         // validity of this warp's 16 keys (inside the split and backed by a valid block), as
         // the producer found it
         const uint32_t okmask = (uint32_t)(valid_s[st] >> (warp * 16)) & 0xffffu;
-        {
-            // the warp's 16 rows of K and V codes -> FP16 (rows without a valid key -> 0);
-            // lane: row lane % 16, 16-code chunks 4 (lane / 16) .. + 3 (spreads each store over
-            // all banks)
+        // the warp's 16 rows of K (kv 0) or V (kv 1) codes -> FP16 in hbuf (rows without a
+        // valid key -> 0); lane: row lane % 16, 16-code chunks 4 (lane / 16) .. + 3 (each store
+        // spreads over all banks)
+        auto convert = [&](int kv) {
             const int rl = lane & 15, R = warp * 16 + rl;
             const bool row_ok = (okmask >> rl) & 1u;
-            __syncwarp();                              // the previous tile's reads are done
+            const uint8_t* src = (kv ? sv : sk) + st * TILE;
+            __syncwarp();                              // hbuf's previous contents are consumed
 #pragma unroll
-            for (int kv = 0; kv < 2; ++kv) {
-                const uint8_t* src = (kv ? sv : sk) + st * TILE;
-                uint8_t* dst = kv ? vh : kh;
-#pragma unroll
-                for (int jj = 0; jj < 4; ++jj) {
-                    const int j = (lane >> 4) * 4 + jj;
-                    uint4 o0 = make_uint4(0, 0, 0, 0), o1 = make_uint4(0, 0, 0, 0);
-                    if (row_ok) {
-                        const uint4 w = *reinterpret_cast<const uint4*>(src + R * 128 + ((j ^ (R & 7)) << 4));
-                        i8x4_to_f16x4(w.x, o0.x, o0.y);
-                        i8x4_to_f16x4(w.y, o0.z, o0.w);
-                        i8x4_to_f16x4(w.z, o1.x, o1.y);
-                        i8x4_to_f16x4(w.w, o1.z, o1.w);
-                    }
-                    *reinterpret_cast<uint4*>(dst + swz<D>(rl, 2 * j)) = o0;
-                    *reinterpret_cast<uint4*>(dst + swz<D>(rl, 2 * j + 1)) = o1;
+            for (int jj = 0; jj < 4; ++jj) {
+                const int j = (lane >> 4) * 4 + jj;
+                uint4 o0 = make_uint4(0, 0, 0, 0), o1 = make_uint4(0, 0, 0, 0);
+                if (row_ok) {
+                    const uint4 w = *reinterpret_cast<const uint4*>(src + R * 128 + ((j ^ (R & 7)) << 4));
+                    i8x4_to_f16x4(w.x, o0.x, o0.y);
+                    i8x4_to_f16x4(w.y, o0.z, o0.w);
+                    i8x4_to_f16x4(w.z, o1.x, o1.y);
+                    i8x4_to_f16x4(w.w, o1.z, o1.w);
                 }
+                *reinterpret_cast<uint4*>(hbuf + swz<D>(rl, 2 * j)) = o0;
+                *reinterpret_cast<uint4*>(hbuf + swz<D>(rl, 2 * j + 1)) = o1;
             }
             __syncwarp();
-        }
+        };
+        convert(0);
         float s[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
-            uint32_t bfr[4];
+            uint32_t af[4], bfr[4];
+            ldmatrix_x4(af, qb + swz<D>(lane & 15, ks * 2 + (lane >> 4)));
             const int r = (lane & 7) + ((lane >> 4) << 3);
             const int c = ks * 2 + ((lane >> 3) & 1);
-            ldmatrix_x4(bfr, khb + swz<D>(r, c));
-            mma_f16_16816(s[0], qf[ks], bfr[0], bfr[1]);
-            mma_f16_16816(s[1], qf[ks], bfr[2], bfr[3]);
+            ldmatrix_x4(bfr, hb + swz<D>(r, c));
+            mma_f16_16816(s[0], af, bfr[0], bfr[1]);
+            mma_f16_16816(s[1], af, bfr[2], bfr[3]);
         }
+        convert(1);
         const float* ksc = ssc + (st * 2 + 0) * BN + warp * 16;
         const float* vsc = ssc + (st * 2 + 1) * BN + warp * 16;
         float mx0 = -INFINITY, mx1 = -INFINITY;
@@ -591,7 +584,7 @@ __global__ void __launch_bounds__(160, 2)
             uint32_t bfr[4];
             const int r = (lane & 7) + (((lane >> 3) & 1) << 3);
             const int c = dp * 2 + (lane >> 4);
-            ldmatrix_x4_trans(bfr, vhb + swz<D>(r, c));
+            ldmatrix_x4_trans(bfr, hb + swz<D>(r, c));
             mma_f16_16816(acc[2 * dp], pf, bfr[0], bfr[1]);
             mma_f16_16816(acc[2 * dp + 1], pf, bfr[2], bfr[3]);
         }
@@ -702,9 +695,9 @@ cudaError_t decode_for(const AttnDecodeArgs& a, cudaStream_t stream) {
 }
 
 cudaError_t decode_q8(const AttnDecodeArgs& a, cudaStream_t stream) {
-    constexpr int D = 128, BN = 64, STAGES = 4;
+    constexpr int D = 128, BN = 64, STAGES = 3;
     const int max_splits = attn_decode_max_splits(a.max_blocks, a.block_size);
-    const size_t smem = (size_t)STAGES * 2 * BN * D + STAGES * 2 * BN * 4 + 16 * D * 2 + 4 * 2 * 16 * D * 2 + 1024;
+    const size_t smem = (size_t)STAGES * 2 * BN * D + STAGES * 2 * BN * 4 + 16 * D * 2 + 4 * 16 * D * 2 + 1024;
     static bool configured = false;
     if (!configured) {
         cudaError_t e = cudaFuncSetAttribute(attn_decode_split_q8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
