@@ -355,7 +355,6 @@ __global__ void __launch_bounds__(160, 3)
     uint8_t* sv = sk + STAGES * TILE;                  // [STAGES][TILE]
     float* ssc = reinterpret_cast<float*>(sv + STAGES * TILE);   // [STAGES][2][BN] K, V scales
     uint8_t* sq = reinterpret_cast<uint8_t*>(ssc + STAGES * 2 * BN);   // [16][D] FP16 q, swizzled rows
-    uint8_t* sh = sq + 16 * D * 2;                     // [4 warps][16][D] FP16 codes (K, then V), swizzled
     __shared__ uint64_t full_bar[STAGES], empty_bar[STAGES];
     __shared__ unsigned long long valid_s[STAGES];     // per stage: bit k = key k of the tile is cached
     __shared__ int abort_s;
@@ -460,10 +459,6 @@ __global__ void __launch_bounds__(160, 3)
         *reinterpret_cast<uint4*>(sq + swz<D>(r, c)) = o;
     }
     asm volatile("bar.sync 1, 128;" ::: "memory");
-    const uint32_t qb = smem_u32(sq);                  // q fragments are re-read each tile (registers)
-    uint8_t* hbuf = sh + warp * (16 * D * 2);          // this warp's FP16 rows: K, then V
-    const uint32_t hb = smem_u32(hbuf);
-
     const float sl2 = a.scale * kLog2e;
     const int g = lane >> 2, cq = lane & 3;
     float acc[D / 8][4];
@@ -478,43 +473,37 @@ __global__ void __launch_bounds__(160, 3)
         // validity of this warp's 16 keys (inside the split and backed by a valid block), as
         // the producer found it
         const uint32_t okmask = (uint32_t)(valid_s[st] >> (warp * 16)) & 0xffffu;
-        // the warp's 16 rows of K (kv 0) or V (kv 1) codes -> FP16 in hbuf (rows without a
-        // valid key -> 0); lane: row lane % 16, 16-code chunks 4 (lane / 16) .. + 3 (each store
-        // spreads over all banks)
-        auto convert = [&](int kv) {
-            const int rl = lane & 15, R = warp * 16 + rl;
-            const bool row_ok = (okmask >> rl) & 1u;
-            const uint8_t* src = (kv ? sv : sk) + st * TILE;
-            __syncwarp();                              // hbuf's previous contents are consumed
+        const uint8_t* ktile = sk + st * TILE;
+        const uint8_t* vtile = sv + st * TILE;
+        // S = Q K^T, the codes converted straight into MMA fragments.  The head dims are
+        // permuted alike in Q and K: MMA step ks gives k indices 2 cq + e and 2 cq + 8 + e
+        // (e = 0, 1) the dims 32 cq + 4 ks + e and 32 cq + 4 ks + 2 + e, so that lane cq
+        // reads 32 consecutive code bytes of its key row.  Keys without a valid block hold
+        // stale (finite) codes; their scores are masked below.
+        uint32_t kw[2][8];
 #pragma unroll
-            for (int jj = 0; jj < 4; ++jj) {
-                const int j = (lane >> 4) * 4 + jj;
-                uint4 o0 = make_uint4(0, 0, 0, 0), o1 = make_uint4(0, 0, 0, 0);
-                if (row_ok) {
-                    const uint4 w = *reinterpret_cast<const uint4*>(src + R * 128 + ((j ^ (R & 7)) << 4));
-                    i8x4_to_f16x4(w.x, o0.x, o0.y);
-                    i8x4_to_f16x4(w.y, o0.z, o0.w);
-                    i8x4_to_f16x4(w.z, o1.x, o1.y);
-                    i8x4_to_f16x4(w.w, o1.z, o1.w);
-                }
-                *reinterpret_cast<uint4*>(hbuf + swz<D>(rl, 2 * j)) = o0;
-                *reinterpret_cast<uint4*>(hbuf + swz<D>(rl, 2 * j + 1)) = o1;
-            }
-            __syncwarp();
-        };
-        convert(0);
+        for (int nt = 0; nt < 2; ++nt) {
+            const int R = warp * 16 + nt * 8 + g;
+            const uint4 w0 = *reinterpret_cast<const uint4*>(ktile + R * 128 + (((2 * cq) ^ (R & 7)) << 4));
+            const uint4 w1 = *reinterpret_cast<const uint4*>(ktile + R * 128 + (((2 * cq + 1) ^ (R & 7)) << 4));
+            kw[nt][0] = w0.x; kw[nt][1] = w0.y; kw[nt][2] = w0.z; kw[nt][3] = w0.w;
+            kw[nt][4] = w1.x; kw[nt][5] = w1.y; kw[nt][6] = w1.z; kw[nt][7] = w1.w;
+        }
         float s[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
-            uint32_t af[4], bfr[4];
-            ldmatrix_x4(af, qb + swz<D>(lane & 15, ks * 2 + (lane >> 4)));
-            const int r = (lane & 7) + ((lane >> 4) << 3);
-            const int c = ks * 2 + ((lane >> 3) & 1);
-            ldmatrix_x4(bfr, hb + swz<D>(r, c));
-            mma_f16_16816(s[0], af, bfr[0], bfr[1]);
-            mma_f16_16816(s[1], af, bfr[2], bfr[3]);
+            // q rows g and g + 8, dims 32 cq + 4 ks .. + 3: 8 bytes of a swizzled 16-byte chunk
+            const uint32_t qoff = (uint32_t)((ks & 1) * 8);
+            const uint2 qa = *reinterpret_cast<const uint2*>(sq + swz<D>(g, 4 * cq + (ks >> 1)) + qoff);
+            const uint2 qc = *reinterpret_cast<const uint2*>(sq + swz<D>(g + 8, 4 * cq + (ks >> 1)) + qoff);
+            const uint32_t af[4] = {qa.x, qc.x, qa.y, qc.y};
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt) {
+                uint32_t b0, b1;
+                i8x4_to_f16x4(kw[nt][ks], b0, b1);
+                mma_f16_16816(s[nt], af, b0, b1);
+            }
         }
-        convert(1);
         const float* ksc = ssc + (st * 2 + 0) * BN + warp * 16;
         const float* vsc = ssc + (st * 2 + 1) * BN + warp * 16;
         float mx0 = -INFINITY, mx1 = -INFINITY;
@@ -579,14 +568,31 @@ __global__ void __launch_bounds__(160, 3)
         }
         l0 += rs0;
         l1 += rs1;
+        // O += P V, the codes converted straight into MMA fragments with the output columns
+        // permuted: column n of step t is dim 16 n + t, so lane g reads one 16-byte chunk (dims
+        // 16 g .. 16 g + 15) of each of its key rows 2 cq, 2 cq + 1, 2 cq + 8, 2 cq + 9, and
+        // byte-interleaves the rows of a key pair into FP16 pairs.
+        uint32_t vw[4][4];
 #pragma unroll
-        for (int dp = 0; dp < D / 16; ++dp) {
-            uint32_t bfr[4];
-            const int r = (lane & 7) + (((lane >> 3) & 1) << 3);
-            const int c = dp * 2 + (lane >> 4);
-            ldmatrix_x4_trans(bfr, hb + swz<D>(r, c));
-            mma_f16_16816(acc[2 * dp], pf, bfr[0], bfr[1]);
-            mma_f16_16816(acc[2 * dp + 1], pf, bfr[2], bfr[3]);
+        for (int q4 = 0; q4 < 4; ++q4) {
+            const int R = warp * 16 + 2 * cq + (q4 & 1) + (q4 >> 1) * 8;
+            const uint4 w = *reinterpret_cast<const uint4*>(vtile + R * 128 + ((g ^ (R & 7)) << 4));
+            vw[q4][0] = w.x; vw[q4][1] = w.y; vw[q4][2] = w.z; vw[q4][3] = w.w;
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            uint32_t x01, y01, x23, y23;
+            asm("prmt.b32 %0, %1, %2, 0x5140;" : "=r"(x01) : "r"(vw[0][i]), "r"(vw[1][i]));
+            asm("prmt.b32 %0, %1, %2, 0x7362;" : "=r"(y01) : "r"(vw[0][i]), "r"(vw[1][i]));
+            asm("prmt.b32 %0, %1, %2, 0x5140;" : "=r"(x23) : "r"(vw[2][i]), "r"(vw[3][i]));
+            asm("prmt.b32 %0, %1, %2, 0x7362;" : "=r"(y23) : "r"(vw[2][i]), "r"(vw[3][i]));
+            uint32_t b0[4], b1[4];
+            i8x4_to_f16x4(x01, b0[0], b0[1]);        // steps 4 i, 4 i + 1
+            i8x4_to_f16x4(y01, b0[2], b0[3]);        // steps 4 i + 2, 4 i + 3
+            i8x4_to_f16x4(x23, b1[0], b1[1]);
+            i8x4_to_f16x4(y23, b1[2], b1[3]);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) mma_f16_16816(acc[4 * i + u], pf, b0[u], b1[u]);
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty_bar[st]);
@@ -608,12 +614,13 @@ __global__ void __launch_bounds__(160, 3)
         s_ml[(warp * 16 + g + 8) * 2 + 1] = l1;
     }
 #pragma unroll
-    for (int i = 0; i < D / 8; ++i) {
-        const int col = i * 8 + 2 * cq;
-        s_acc[(warp * 16 + g) * D + col] = acc[i][0];
-        s_acc[(warp * 16 + g) * D + col + 1] = acc[i][1];
-        s_acc[(warp * 16 + g + 8) * D + col] = acc[i][2];
-        s_acc[(warp * 16 + g + 8) * D + col + 1] = acc[i][3];
+    for (int t = 0; t < D / 8; ++t) {
+        // step t's columns 2 cq and 2 cq + 1 are dims 32 cq + t and 32 cq + 16 + t
+        const int col = 32 * cq + t;
+        s_acc[(warp * 16 + g) * D + col] = acc[t][0];
+        s_acc[(warp * 16 + g) * D + col + 16] = acc[t][1];
+        s_acc[(warp * 16 + g + 8) * D + col] = acc[t][2];
+        s_acc[(warp * 16 + g + 8) * D + col + 16] = acc[t][3];
     }
     asm volatile("bar.sync 1, 128;" ::: "memory");
     for (int i = threadIdx.x; i < G * D; i += NCONS) {
@@ -697,7 +704,7 @@ cudaError_t decode_for(const AttnDecodeArgs& a, cudaStream_t stream) {
 cudaError_t decode_q8(const AttnDecodeArgs& a, cudaStream_t stream) {
     constexpr int D = 128, BN = 64, STAGES = 3;
     const int max_splits = attn_decode_max_splits(a.max_blocks, a.block_size);
-    const size_t smem = (size_t)STAGES * 2 * BN * D + STAGES * 2 * BN * 4 + 16 * D * 2 + 4 * 16 * D * 2 + 1024;
+    const size_t smem = (size_t)STAGES * 2 * BN * D + STAGES * 2 * BN * 4 + 16 * D * 2 + 1024;
     static bool configured = false;
     if (!configured) {
         cudaError_t e = cudaFuncSetAttribute(attn_decode_split_q8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
