@@ -318,6 +318,8 @@ def _random_q8_pool(nb, Hkv, bs, d, seed):
     (3, 16, 2, 128, 900, 3100),         # GQA 8, several 1024-key splits
     (4, 4, 4, 32, 1023, 1026),          # split boundaries, 32-row blocks
     (2, 8, 1, 16, 1, 90),               # 16-row blocks, one KV head
+    (3, 12, 3, 128, 1, 700),            # GQA 4: half the query columns padding
+    (2, 16, 1, 64, 500, 2100),          # GQA 16: two query column tiles
 ])
 def test_paged_attention_decode_q8(B, Hq, Hkv, bs, ctx_lo, ctx_hi):
     d = 128

@@ -337,14 +337,21 @@ __global__ void __launch_bounds__(160, 2)
 // section "KV Cache quantisation": the cache block is dequantised as it is
 // loaded).  The producer streams each 64-key tile's codes (128-byte rows, the
 // 128-byte swizzle) with TMA and its K and V scales with bulk copies, all on
-// the stage's barrier.  Each consumer warp turns the codes of its own 16 keys
-// into FP16 (exact: |code| <= 127) in a private swizzled tile and runs the
-// tensor-core steps in FP16.  A key's K scale multiplies its score and its V
-// scale its probability before P V, so dequantised values are never formed;
-// the row sum stays the sum of the unscaled probabilities.  Q enters as FP16
-// (exact for BF16 values of FP16's range), P as one FP16 operand (the cache's
-// INT8 rounding dominates its error).
-__global__ void __launch_bounds__(160, 3)
+// the stage's barrier.  Each consumer warp owns 16 keys of every tile and runs
+// both products transposed, so that its keys (then the head dims) fill the
+// MMA's 16 rows and the group's query rows its 8 columns (NT column tiles for
+// groups of 9 to 16): S^T = K Q^T and O^T = V^T P^T, the codes converted
+// straight from shared memory into FP16 A fragments (exact: |code| <= 127).
+// The S^T fragment of a lane holds two keys of two query columns; transposing
+// its two 8x8 FP16 halves (movmatrix) gives the B fragment of P^T.  A key's K
+// scale multiplies its score and its V scale its probability before P V, so
+// dequantised values are never formed; the row sum stays the sum of the
+// unscaled probabilities.  Q enters as FP16 (exact for BF16 values of FP16's
+// range), P as one FP16 operand (the cache's INT8 rounding dominates its error).
+// One column tile runs four CTAs per SM (94 registers); two run two (their
+// accumulators take 64 registers).
+template <int NT>
+__global__ void __launch_bounds__(160, NT == 1 ? 4 : 2)
     attn_decode_split_q8_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                                 const AttnDecodeArgs a, int max_splits) {
     constexpr int D = 128, BN = 64, STAGES = 3, NCONS = 128;
@@ -461,10 +468,28 @@ __global__ void __launch_bounds__(160, 3)
     asm volatile("bar.sync 1, 128;" ::: "memory");
     const float sl2 = a.scale * kLog2e;
     const int g = lane >> 2, cq = lane & 3;
-    float acc[D / 8][4];
+    // B fragments of Q^T, column g of tile nt = query row 8 nt + g.  The head dims are permuted
+    // alike in Q and K: MMA step ks gives k indices 2 cq + e and 2 cq + 8 + e (e = 0, 1) the
+    // dims 32 cq + 4 ks + e and 32 cq + 4 ks + 2 + e, so that lane cq reads 32 consecutive
+    // code bytes of each of its key rows.
+    uint2 qf[NT][D / 16];
 #pragma unroll
-    for (int i = 0; i < D / 8; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
-    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks)
+            qf[nt][ks] = *reinterpret_cast<const uint2*>(sq + swz<D>(8 * nt + g, 4 * cq + (ks >> 1)) + (ks & 1) * 8);
+    // O^T: row r of tile t is head dim 16 (r & 7) + 2 t + (r >> 3), column n of tile nt
+    // query row 8 nt + n.  Per query column: running max m (the exponent base) and the lane's
+    // part of the row sum l.
+    float acc[NT][D / 16][4];
+    float m[NT][2], l[NT][2];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+        for (int t = 0; t < D / 16; ++t) acc[nt][t][0] = acc[nt][t][1] = acc[nt][t][2] = acc[nt][t][3] = 0.f;
+        m[nt][0] = m[nt][1] = -INFINITY;
+        l[nt][0] = l[nt][1] = 0.f;
+    }
 
     for (int kt = 0; kt < n_kt; ++kt) {
         const int st = kt % STAGES;
@@ -475,103 +500,97 @@ __global__ void __launch_bounds__(160, 3)
         const uint32_t okmask = (uint32_t)(valid_s[st] >> (warp * 16)) & 0xffffu;
         const uint8_t* ktile = sk + st * TILE;
         const uint8_t* vtile = sv + st * TILE;
-        // S = Q K^T, the codes converted straight into MMA fragments.  The head dims are
-        // permuted alike in Q and K: MMA step ks gives k indices 2 cq + e and 2 cq + 8 + e
-        // (e = 0, 1) the dims 32 cq + 4 ks + e and 32 cq + 4 ks + 2 + e, so that lane cq
-        // reads 32 consecutive code bytes of its key row.  Keys without a valid block hold
-        // stale (finite) codes; their scores are masked below.
+        // S^T = K Q^T: A rows g and g + 8 are the warp's keys g and g + 8.  Keys without a
+        // valid block hold stale (finite) codes; their scores are masked below.
         uint32_t kw[2][8];
 #pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
-            const int R = warp * 16 + nt * 8 + g;
+        for (int j = 0; j < 2; ++j) {
+            const int R = warp * 16 + j * 8 + g;
             const uint4 w0 = *reinterpret_cast<const uint4*>(ktile + R * 128 + (((2 * cq) ^ (R & 7)) << 4));
             const uint4 w1 = *reinterpret_cast<const uint4*>(ktile + R * 128 + (((2 * cq + 1) ^ (R & 7)) << 4));
-            kw[nt][0] = w0.x; kw[nt][1] = w0.y; kw[nt][2] = w0.z; kw[nt][3] = w0.w;
-            kw[nt][4] = w1.x; kw[nt][5] = w1.y; kw[nt][6] = w1.z; kw[nt][7] = w1.w;
+            kw[j][0] = w0.x; kw[j][1] = w0.y; kw[j][2] = w0.z; kw[j][3] = w0.w;
+            kw[j][4] = w1.x; kw[j][5] = w1.y; kw[j][6] = w1.z; kw[j][7] = w1.w;
         }
-        float s[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+        float s[NT][4];
+        {
+            // two accumulators per column tile (even and odd steps) halve the MMA chain
+            float sp[NT][2][4];
 #pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) {
-            // q rows g and g + 8, dims 32 cq + 4 ks .. + 3: 8 bytes of a swizzled 16-byte chunk
-            const uint32_t qoff = (uint32_t)((ks & 1) * 8);
-            const uint2 qa = *reinterpret_cast<const uint2*>(sq + swz<D>(g, 4 * cq + (ks >> 1)) + qoff);
-            const uint2 qc = *reinterpret_cast<const uint2*>(sq + swz<D>(g + 8, 4 * cq + (ks >> 1)) + qoff);
-            const uint32_t af[4] = {qa.x, qc.x, qa.y, qc.y};
+            for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-            for (int nt = 0; nt < 2; ++nt) {
-                uint32_t b0, b1;
-                i8x4_to_f16x4(kw[nt][ks], b0, b1);
-                mma_f16_16816(s[nt], af, b0, b1);
+                for (int h = 0; h < 2; ++h) sp[nt][h][0] = sp[nt][h][1] = sp[nt][h][2] = sp[nt][h][3] = 0.f;
+#pragma unroll
+            for (int ks = 0; ks < D / 16; ++ks) {
+                uint32_t af[4];
+                i8x4_to_f16x4(kw[0][ks], af[0], af[2]);
+                i8x4_to_f16x4(kw[1][ks], af[1], af[3]);
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) {
+                    mma_f16_16816(sp[nt][ks & 1], af, qf[nt][ks].x, qf[nt][ks].y);
+                }
             }
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) s[nt][j] = sp[nt][0][j] + sp[nt][1][j];
         }
+        // lane: keys g (s[.][0..1]) and g + 8 (s[.][2..3]) of query columns 2 cq and 2 cq + 1
         const float* ksc = ssc + (st * 2 + 0) * BN + warp * 16;
         const float* vsc = ssc + (st * 2 + 1) * BN + warp * 16;
-        float mx0 = -INFINITY, mx1 = -INFINITY;
-        float vs[2][2];
+        const bool v0 = (okmask >> g) & 1u, v1 = (okmask >> (g + 8)) & 1u;
+        const float f0 = sl2 * ksc[g], f1 = sl2 * ksc[g + 8];
+        const float vs0 = v0 ? vsc[g] : 0.f, vs1 = v1 ? vsc[g + 8] : 0.f;
+        float mx[NT][2];
+        bool grow = false;
 #pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
-            const int kk = nt * 8 + 2 * cq;   // key index within the warp's 16
-            const bool v0 = (okmask >> kk) & 1u, v1 = (okmask >> (kk + 1)) & 1u;
-            const float f0 = sl2 * ksc[kk], f1 = sl2 * ksc[kk + 1];
-            vs[nt][0] = v0 ? vsc[kk] : 0.f;
-            vs[nt][1] = v1 ? vsc[kk + 1] : 0.f;
+        for (int nt = 0; nt < NT; ++nt) {
             s[nt][0] = v0 ? s[nt][0] * f0 : -INFINITY;
-            s[nt][1] = v1 ? s[nt][1] * f1 : -INFINITY;
-            s[nt][2] = v0 ? s[nt][2] * f0 : -INFINITY;
+            s[nt][1] = v0 ? s[nt][1] * f0 : -INFINITY;
+            s[nt][2] = v1 ? s[nt][2] * f1 : -INFINITY;
             s[nt][3] = v1 ? s[nt][3] * f1 : -INFINITY;
-            mx0 = fmaxf(mx0, fmaxf(s[nt][0], s[nt][1]));
-            mx1 = fmaxf(mx1, fmaxf(s[nt][2], s[nt][3]));
-        }
+            mx[nt][0] = fmaxf(s[nt][0], s[nt][2]);
+            mx[nt][1] = fmaxf(s[nt][1], s[nt][3]);
 #pragma unroll
-        for (int o = 1; o <= 2; o <<= 1) {
-            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
-            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
+            for (int o = 4; o <= 16; o <<= 1) {
+                mx[nt][0] = fmaxf(mx[nt][0], __shfl_xor_sync(0xffffffffu, mx[nt][0], o));
+                mx[nt][1] = fmaxf(mx[nt][1], __shfl_xor_sync(0xffffffffu, mx[nt][1], o));
+            }
+            grow = grow || mx[nt][0] > m[nt][0] + 8.f || mx[nt][1] > m[nt][1] + 8.f;
         }
-        // The exponent base of a row moves only when its max grows by more than 2^8 (P then
+        // The exponent base of a column moves only when its max grows by more than 2^8 (P then
         // stays below 256); otherwise the running sums need no rescaling this tile.
-        if (__any_sync(0xffffffffu, mx0 > m0 + 8.f || mx1 > m1 + 8.f)) {
-            const float mn0 = mx0 > m0 + 8.f ? mx0 : m0, mn1 = mx1 > m1 + 8.f ? mx1 : m1;
-            const float al0 = mn0 == m0 ? 1.f : ex2_approx(m0 - mn0);
-            const float al1 = mn1 == m1 ? 1.f : ex2_approx(m1 - mn1);
-            l0 *= al0;
-            l1 *= al1;
+        if (__any_sync(0xffffffffu, grow)) {
 #pragma unroll
-            for (int i = 0; i < D / 8; ++i) {
-                acc[i][0] *= al0;
-                acc[i][1] *= al0;
-                acc[i][2] *= al1;
-                acc[i][3] *= al1;
-            }
-            m0 = mn0;
-            m1 = mn1;
-        }
-        const float base0 = (m0 == -INFINITY) ? 0.f : m0;
-        const float base1 = (m1 == -INFINITY) ? 0.f : m1;
-        uint32_t pf[4];
-        float rs0 = 0.f, rs1 = 0.f;
-        {
-            float p[2][4];
+            for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-            for (int nt = 0; nt < 2; ++nt) {
-                p[nt][0] = ex2_approx(s[nt][0] - base0);
-                p[nt][1] = ex2_approx(s[nt][1] - base0);
-                p[nt][2] = ex2_approx(s[nt][2] - base1);
-                p[nt][3] = ex2_approx(s[nt][3] - base1);
-                rs0 += p[nt][0] + p[nt][1];
-                rs1 += p[nt][2] + p[nt][3];
-            }
-            // each key's V scale rides on its probability
-            pf[0] = pack_f16x2(p[0][0] * vs[0][0], p[0][1] * vs[0][1]);
-            pf[1] = pack_f16x2(p[0][2] * vs[0][0], p[0][3] * vs[0][1]);
-            pf[2] = pack_f16x2(p[1][0] * vs[1][0], p[1][1] * vs[1][1]);
-            pf[3] = pack_f16x2(p[1][2] * vs[1][0], p[1][3] * vs[1][1]);
+                for (int e = 0; e < 2; ++e) {
+                    const float mn = mx[nt][e] > m[nt][e] + 8.f ? mx[nt][e] : m[nt][e];
+                    const float al = mn == m[nt][e] ? 1.f : ex2_approx(m[nt][e] - mn);
+                    l[nt][e] *= al;
+#pragma unroll
+                    for (int t = 0; t < D / 16; ++t) {
+                        acc[nt][t][e] *= al;
+                        acc[nt][t][e + 2] *= al;
+                    }
+                    m[nt][e] = mn;
+                }
         }
-        l0 += rs0;
-        l1 += rs1;
-        // O += P V, the codes converted straight into MMA fragments with the output columns
-        // permuted: column n of step t is dim 16 n + t, so lane g reads one 16-byte chunk (dims
-        // 16 g .. 16 g + 15) of each of its key rows 2 cq, 2 cq + 1, 2 cq + 8, 2 cq + 9, and
-        // byte-interleaves the rows of a key pair into FP16 pairs.
+        // P^T (each key's V scale riding on its probability) as the B fragments of O^T = V^T P^T
+        uint32_t pb[NT][2];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            const float b0 = (m[nt][0] == -INFINITY) ? 0.f : m[nt][0];
+            const float b1 = (m[nt][1] == -INFINITY) ? 0.f : m[nt][1];
+            const float p00 = ex2_approx(s[nt][0] - b0), p01 = ex2_approx(s[nt][1] - b1);
+            const float p10 = ex2_approx(s[nt][2] - b0), p11 = ex2_approx(s[nt][3] - b1);
+            l[nt][0] += p00 + p10;
+            l[nt][1] += p01 + p11;
+            pb[nt][0] = movmatrix_trans(pack_f16x2(p00 * vs0, p01 * vs0));   // keys 0-7
+            pb[nt][1] = movmatrix_trans(pack_f16x2(p10 * vs1, p11 * vs1));   // keys 8-15
+        }
+        // O^T += V^T P^T: lane g reads one 16-byte chunk (dims 16 g .. 16 g + 15) of each of its
+        // key rows 2 cq, 2 cq + 1, 2 cq + 8, 2 cq + 9 and byte-interleaves the rows of a key pair
+        // into FP16 pairs: word i gives tile 2 i (dims 16 g + 4 i, + 1) and tile 2 i + 1 (+ 2, + 3).
         uint32_t vw[4][4];
 #pragma unroll
         for (int q4 = 0; q4 < 4; ++q4) {
@@ -586,41 +605,46 @@ __global__ void __launch_bounds__(160, 3)
             asm("prmt.b32 %0, %1, %2, 0x7362;" : "=r"(y01) : "r"(vw[0][i]), "r"(vw[1][i]));
             asm("prmt.b32 %0, %1, %2, 0x5140;" : "=r"(x23) : "r"(vw[2][i]), "r"(vw[3][i]));
             asm("prmt.b32 %0, %1, %2, 0x7362;" : "=r"(y23) : "r"(vw[2][i]), "r"(vw[3][i]));
-            uint32_t b0[4], b1[4];
-            i8x4_to_f16x4(x01, b0[0], b0[1]);        // steps 4 i, 4 i + 1
-            i8x4_to_f16x4(y01, b0[2], b0[3]);        // steps 4 i + 2, 4 i + 3
-            i8x4_to_f16x4(x23, b1[0], b1[1]);
-            i8x4_to_f16x4(y23, b1[2], b1[3]);
+            uint32_t at0[4], at1[4];
+            i8x4_to_f16x4(x01, at0[0], at0[1]);      // keys 2 cq, 2 cq + 1: dims 16 g + 4 i, + 1
+            i8x4_to_f16x4(x23, at0[2], at0[3]);      // keys 2 cq + 8, 2 cq + 9
+            i8x4_to_f16x4(y01, at1[0], at1[1]);      // dims 16 g + 4 i + 2, + 3
+            i8x4_to_f16x4(y23, at1[2], at1[3]);
 #pragma unroll
-            for (int u = 0; u < 4; ++u) mma_f16_16816(acc[4 * i + u], pf, b0[u], b1[u]);
+            for (int nt = 0; nt < NT; ++nt) {
+                mma_f16_16816(acc[nt][2 * i], at0, pb[nt][0], pb[nt][1]);
+                mma_f16_16816(acc[nt][2 * i + 1], at1, pb[nt][0], pb[nt][1]);
+            }
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty_bar[st]);
     }
 #pragma unroll
-    for (int o = 1; o <= 2; o <<= 1) {
-        l0 += __shfl_xor_sync(0xffffffffu, l0, o);
-        l1 += __shfl_xor_sync(0xffffffffu, l1, o);
-    }
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int e = 0; e < 2; ++e)
+#pragma unroll
+            for (int o = 4; o <= 16; o <<= 1) l[nt][e] += __shfl_xor_sync(0xffffffffu, l[nt][e], o);
 
     // merge the 4 consumer warps: [4][16] (m, l) and [4][16][D] acc, over the code rings
     asm volatile("bar.sync 1, 128;" ::: "memory");
     float* s_ml = reinterpret_cast<float*>(sk);            // [4][16][2]
     float* s_acc = s_ml + 4 * 16 * 2;                      // [4][16][D]
-    if (cq == 0) {
-        s_ml[(warp * 16 + g) * 2 + 0] = m0;
-        s_ml[(warp * 16 + g) * 2 + 1] = l0;
-        s_ml[(warp * 16 + g + 8) * 2 + 0] = m1;
-        s_ml[(warp * 16 + g + 8) * 2 + 1] = l1;
-    }
 #pragma unroll
-    for (int t = 0; t < D / 8; ++t) {
-        // step t's columns 2 cq and 2 cq + 1 are dims 32 cq + t and 32 cq + 16 + t
-        const int col = 32 * cq + t;
-        s_acc[(warp * 16 + g) * D + col] = acc[t][0];
-        s_acc[(warp * 16 + g) * D + col + 16] = acc[t][1];
-        s_acc[(warp * 16 + g + 8) * D + col] = acc[t][2];
-        s_acc[(warp * 16 + g + 8) * D + col + 16] = acc[t][3];
+    for (int nt = 0; nt < NT; ++nt) {
+        if (g == 0) {
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const int r = warp * 16 + 8 * nt + 2 * cq + e;
+                s_ml[r * 2 + 0] = m[nt][e];
+                s_ml[r * 2 + 1] = l[nt][e];
+            }
+        }
+#pragma unroll
+        for (int t = 0; t < D / 16; ++t)
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                s_acc[(warp * 16 + 8 * nt + 2 * cq + (j & 1)) * D + 16 * g + 2 * t + (j >> 1)] = acc[nt][t][j];
     }
     asm volatile("bar.sync 1, 128;" ::: "memory");
     for (int i = threadIdx.x; i < G * D; i += NCONS) {
@@ -701,15 +725,20 @@ cudaError_t decode_for(const AttnDecodeArgs& a, cudaStream_t stream) {
     return record(cudaGetLastError(), "attn_decode_combine_kernel launch");
 }
 
-cudaError_t decode_q8(const AttnDecodeArgs& a, cudaStream_t stream) {
+template <int NT>
+cudaError_t decode_q8_for(const AttnDecodeArgs& a, cudaStream_t stream) {
     constexpr int D = 128, BN = 64, STAGES = 3;
     const int max_splits = attn_decode_max_splits(a.max_blocks, a.block_size);
     const size_t smem = (size_t)STAGES * 2 * BN * D + STAGES * 2 * BN * 4 + 16 * D * 2 + 1024;
     static bool configured = false;
     if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(attn_decode_split_q8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)smem);
+        cudaError_t e = cudaFuncSetAttribute(attn_decode_split_q8_kernel<NT>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return record(e, "cudaFuncSetAttribute(attn_decode_split_q8_kernel)");
+        // four CTAs of 56 KB per SM need the whole shared-memory carveout
+        e = cudaFuncSetAttribute(attn_decode_split_q8_kernel<NT>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                 (int)cudaSharedmemCarveoutMaxShared);
+        if (e != cudaSuccess) return record(e, "cudaFuncSetAttribute(attn_decode_split_q8_kernel carveout)");
         configured = true;
     }
     CUtensorMap tmK, tmV;
@@ -719,7 +748,7 @@ cudaError_t decode_q8(const AttnDecodeArgs& a, cudaStream_t stream) {
         return cudaErrorInvalidValue;
     dim3 grid(max_splits, a.n_kv_heads, a.batch);
     trace_before("attn_decode_split", stream);
-    cudaError_t e = launch_pdl(attn_decode_split_q8_kernel, grid, dim3(160), smem, stream, 1, tmK, tmV, a,
+    cudaError_t e = launch_pdl(attn_decode_split_q8_kernel<NT>, grid, dim3(160), smem, stream, 1, tmK, tmV, a,
                                max_splits);
     trace_after(stream);
     if (e == cudaSuccess) e = cudaGetLastError();
@@ -746,8 +775,11 @@ size_t attn_decode_scratch_bytes(int batch, int n_heads, int head_dim, int max_b
 
 cudaError_t launch_attn_decode_q8(const AttnDecodeArgs& a, cudaStream_t stream) {
     if (a.batch <= 0) return cudaSuccess;
-    if (a.head_dim != 128) return cudaErrorInvalidValue;
-    return decode_q8(a, stream);
+    if (a.head_dim != 128 || a.n_kv_heads <= 0 || a.n_heads % a.n_kv_heads != 0) return cudaErrorInvalidValue;
+    const int G = a.n_heads / a.n_kv_heads;
+    if (G <= 8) return decode_q8_for<1>(a, stream);
+    if (G <= 16) return decode_q8_for<2>(a, stream);
+    return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_attn_decode(const AttnDecodeArgs& a, cudaStream_t stream) {

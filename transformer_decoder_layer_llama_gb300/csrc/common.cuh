@@ -435,6 +435,15 @@ LL_DEVINL uint32_t pack_f16x2(float lo, float hi) {
     return *reinterpret_cast<uint32_t*>(&v);
 }
 
+// Transpose of an 8x8 FP16 matrix held one pair per lane (lane 4 r + c holds row
+// r, columns 2 c and 2 c + 1): afterwards every lane holds the same positions of
+// the transpose.
+LL_DEVINL uint32_t movmatrix_trans(uint32_t x) {
+    uint32_t y;
+    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+    return y;
+}
+
 // Four INT8 codes (one 32-bit word, lowest address first) as two FP16 pairs,
 // exactly: bias each byte to x + 128, place it under the FP16 exponent of 1024
 // (the pair 1024 + x + 128), and subtract 1152.
