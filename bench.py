@@ -52,14 +52,14 @@ NCU_TRAFFIC = {
                      "sha256": "5e2cc4e2c5027a67959e1359d1f5371ec4912d05d033db45fb4ad7f06660a2c3", "bytes_per_launch": 168.4e6},
     # attn_decode_split_kernel, 7B decode (batch 64)
     "llama2_7b_decode_attn": {"file": "transformer_decoder_layer_llama_gb300/csrc/attn.cu",
-                              "sha256": "5a66b67687131c863374f04ddd6aaef49e6cd4ee61d55657f10114d57625f324", "bytes_per_launch": 2245.9e6},
+                              "sha256": "2fd2e5678af2d403d070c7a044407b883d53c52455899be0c0dbc5dea3340504", "bytes_per_launch": 2246.1e6},
     # one weight-form GEMM (gemm_weight_kernel + gemm_weight_fixup_kernel), 70B decode:
     # mean over the layer's 4 GEMMs
     "llama70b_gqa_decode_gemm": {"file": "transformer_decoder_layer_llama_gb300/csrc/gemm_tc.cu",
                                  "sha256": "5e2cc4e2c5027a67959e1359d1f5371ec4912d05d033db45fb4ad7f06660a2c3", "bytes_per_launch": 433.1e6},
     # attn_decode_split_q8_kernel, 7B decode over an INT8 cache (batch 64)
     "llama2_7b_decode_int8kv_attn": {"file": "transformer_decoder_layer_llama_gb300/csrc/attn.cu",
-                                     "sha256": "5a66b67687131c863374f04ddd6aaef49e6cd4ee61d55657f10114d57625f324", "bytes_per_launch": 1168.9e6},
+                                     "sha256": "2fd2e5678af2d403d070c7a044407b883d53c52455899be0c0dbc5dea3340504", "bytes_per_launch": 1159.8e6},
     # one weight-form GEMM, 70B decode over an INT8 cache: mean over the layer's 4 GEMMs
     "llama70b_gqa_decode_int8kv_gemm": {"file": "transformer_decoder_layer_llama_gb300/csrc/gemm_tc.cu",
                                         "sha256": "5e2cc4e2c5027a67959e1359d1f5371ec4912d05d033db45fb4ad7f06660a2c3", "bytes_per_launch": 433.2e6},
