@@ -218,9 +218,9 @@ size_t ll_attention_workspace_size(int32_t batch, int32_t n_heads, int32_t head_
  * the operators", flash_attention_decode; paging page PagedAttentionOperation):
  * q BF16 [batch, n_heads, head_dim]; sequence b's query head h attends over
  * positions 0..context_lens[b]-1 of KV head h / (n_heads / n_kv_heads) with
- * softmax(q k^T * scale).  out BF16 [batch, n_heads, head_dim].
- * head_dim 64 or 128, n_heads / n_kv_heads <= 16, block_size a power of two
- * in [16, 256]. */
+ * softmax(q k^T * scale).  out BF16 [batch, n_heads, head_dim]; a sequence
+ * with context length 0 gets zero rows.  head_dim 64 or 128, n_heads /
+ * n_kv_heads <= 16, block_size a power of two in [16, 256]. */
 int ll_paged_attention_decode(const void* q, const ll_kv_pool* pool, const int32_t* block_table,
                               int32_t max_blocks, const int32_t* context_lens, int32_t batch,
                               int32_t n_heads, int32_t n_kv_heads, int32_t head_dim,

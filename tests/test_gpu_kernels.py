@@ -24,7 +24,8 @@ DEV = "cuda"
     (64, 4096, 11008),                                   # weight form, split K
     (64, 128, 4096), (48, 256, 8192),                    # 16-32 CTAs share one tile
     (200, 1376, 688), (256, 4096, 4096),                 # weight form up to 256 tokens
-    (129, 12288, 512),                                   # few tokens, wide output: CTA pairs
+    (129, 12288, 512),                                   # weight form, wide output
+    (232, 12288, 512),                                   # few tokens, wide output: CTA pairs, ragged
     (65, 256, 128), (128, 512, 256), (300, 1376, 688), (2048, 4096, 4096), (257, 12288, 4096),
 ])
 def test_linear_matches_float64_matmul(m, n, k):
@@ -100,6 +101,33 @@ def test_paged_attention_decode(B, Hq, Hkv, d, bs, ctx_lo, ctx_hi):
     torch.cuda.synchronize()
     ref = O.paged_attention_decode(f64(q), bits(kp), bits(vp), table.numpy(), ctx.numpy(), scale)
     assert_close(f64(out), ref, "paged_attention_decode")
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,d,bs,ctx_hi", [
+    (40, 8, 2, 64, 16, 3100),           # full splits first, then the partial ones by length
+    (520, 2, 1, 64, 32, 60),            # beyond the sorted batch: partial splits in sequence order
+])
+def test_paged_attention_decode_dispatch_order(B, Hq, Hkv, d, bs, ctx_hi):
+    """Many sequences with contexts on, next to and away from the 1024-key split
+    boundaries, empty ones (their output rows are zero) and two of 9 splits (long enough
+    for the split grid to run in its dispatch order)."""
+    dims = synth.LayerDims(Hq * d, Hq, Hkv, d, 64, bs)
+    ctx = synth.make_context_lens(B, 1, ctx_hi, seed=B * 31)
+    ctx[:9] = torch.tensor([0, 1024, 2048, 1023, 1025, 0, 1, 8200, 9216], dtype=torch.int32)
+    table, nb = synth.make_block_table(ctx.tolist(), bs, seed=B * 37, extra_blocks=3)
+    kp, vp = synth.make_pool(nb, dims, seed=B * 41)
+    q = synth.normal_bf16((B, Hq, d), 1.0, seed=B + 3, tag="q")
+    scale = 1 / math.sqrt(d)
+    status = api.new_status()
+    out = api.paged_attention_decode(q.to(DEV), kp.to(DEV), vp.to(DEV), table.to(DEV), ctx.to(DEV), scale,
+                                     status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    got = f64(out)
+    live = ctx.numpy() > 0
+    assert (got[~live] == 0).all()
+    ref = O.paged_attention_decode(f64(q)[live], bits(kp), bits(vp), table.numpy()[live], ctx.numpy()[live], scale)
+    assert_close(got[live], ref, "paged_attention_decode, many sequences")
 
 
 # ---------------------------------------------------------------- whole layer, tiny GQA workload
@@ -320,6 +348,7 @@ def _random_q8_pool(nb, Hkv, bs, d, seed):
     (2, 8, 1, 16, 1, 90),               # 16-row blocks, one KV head
     (3, 12, 3, 128, 1, 700),            # GQA 4: half the query columns padding
     (2, 16, 1, 64, 500, 2100),          # GQA 16: two query column tiles
+    (40, 8, 1, 16, 1, 2100),            # many sequences: the sorted dispatch order
 ])
 def test_paged_attention_decode_q8(B, Hq, Hkv, bs, ctx_lo, ctx_hi):
     d = 128

@@ -45,6 +45,142 @@ LL_DEVINL uint32_t swz(int r, int c) {
     return (uint32_t)(r * (D * 2) + ((c ^ (r & 7)) << 4));
 }
 
+// ---------------------------------------------------------------- decode dispatch order
+// Entry L of the order table is the work of the split kernel's CTA with linear index L
+// (x fastest): {sequence, KV head, split, context length}, or sequence -1 for none.
+// Every full 1024-key split comes first (they all take the same time), then each
+// sequence's partial last split, longest first (in sequence order for batches above
+// kOrderSortMax), so that the CTAs still running at the end of the grid are short ones.
+constexpr int kOrderThreads = 1024;
+constexpr int kOrderSortMax = 512;
+constexpr int kOrderMaxBatch = 8192;    // shared memory: three ints per sequence
+
+// exclusive prefix sum over the block (one value per thread) and the block total
+LL_DEVINL long long block_exclusive_scan(long long v, long long* s_warp, long long& total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    long long x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const long long y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) s_warp[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+        long long w = lane < nw ? s_warp[lane] : 0;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const long long y = __shfl_up_sync(0xffffffffu, w, o);
+            if (lane >= o) w += y;
+        }
+        if (lane < nw) s_warp[lane] = w;         // inclusive prefix of the warp totals
+    }
+    __syncthreads();
+    total = s_warp[nw - 1];
+    return (warp ? s_warp[warp - 1] : 0) + x - v;
+}
+
+__global__ void __launch_bounds__(kOrderThreads) attn_decode_order_kernel(const AttnDecodeArgs a, int max_splits) {
+    extern __shared__ int s_ord[];             // [batch] context, [batch] full-split prefix, [batch] partial slot -> sequence
+    __shared__ long long s_warp[32];
+    pdl_trigger();
+    const int B = a.batch, Hkv = a.n_kv_heads;
+    const int max_ctx = a.max_blocks * a.block_size;
+    int* s_c = s_ord;
+    int* s_f = s_ord + B;
+    int* s_inv = s_ord + 2 * B;
+    for (int b = threadIdx.x; b < B; b += blockDim.x) {
+        int c = a.context_lens[b];
+        if (c < 0 || c > max_ctx) {
+            flag_status(a.status, LL_DEV_BAD_POSITION);
+            c = min(max(c, 0), max_ctx);
+        }
+        s_c[b] = c;
+    }
+    __syncthreads();
+    // per sequence: full splits (high 32 bits) and whether a partial split follows (low 32 bits),
+    // summed over a contiguous chunk of sequences per thread, then scanned over the block
+    const int per = (B + (int)blockDim.x - 1) / (int)blockDim.x;
+    const int b0 = min(B, (int)threadIdx.x * per), b1 = min(B, b0 + per);
+    long long mine = 0;
+    for (int b = b0; b < b1; ++b)
+        mine += ((long long)(s_c[b] / kDecodeChunk) << 32) + (s_c[b] % kDecodeChunk != 0);
+    long long total;
+    long long run = block_exclusive_scan(mine, s_warp, total);
+    const bool sorted = B <= kOrderSortMax;
+    for (int b = b0; b < b1; ++b) {
+        s_f[b] = (int)(run >> 32);
+        if (!sorted && s_c[b] % kDecodeChunk != 0) s_inv[(int)(run & 0xffffffffll)] = b;
+        run += ((long long)(s_c[b] / kDecodeChunk) << 32) + (s_c[b] % kDecodeChunk != 0);
+    }
+    const int F = (int)(total >> 32), P = (int)(total & 0xffffffffll);
+    if (sorted) {
+        // slot of a partial split: its rank by decreasing length (ties by sequence)
+        for (int b = threadIdx.x; b < B; b += blockDim.x) {
+            const int pk = s_c[b] % kDecodeChunk;
+            if (pk == 0) continue;
+            int r = 0;
+            for (int j = 0; j < B; ++j) {
+                const int pj = s_c[j] % kDecodeChunk;
+                r += (pj > pk) || (pj == pk && j < b);
+            }
+            s_inv[r] = b;
+        }
+    }
+    __syncthreads();
+    // one entry per thread and step, consecutive threads on consecutive entries: full split
+    // f (in sequence order) of KV head hk at f * Hkv + hk, then the partial splits by slot
+    const long long full_end = (long long)Hkv * F, used = (long long)Hkv * ((long long)F + P);
+    const long long all = (long long)max_splits * Hkv * B;
+    for (long long L = threadIdx.x; L < all; L += blockDim.x) {
+        int4 e = make_int4(-1, 0, 0, 0);
+        if (L < full_end) {
+            const int f = (int)(L / Hkv), hk = (int)(L - (long long)f * Hkv);
+            int lo = 0, hi = B - 1;                  // last sequence whose full splits start at or before f
+            while (lo < hi) {
+                const int mid = (lo + hi + 1) >> 1;
+                if (s_f[mid] <= f) lo = mid; else hi = mid - 1;
+            }
+            e = make_int4(lo, hk, f - s_f[lo], s_c[lo]);
+        } else if (L < used) {
+            const long long q = L - full_end;
+            const int r = (int)(q / Hkv), hk = (int)(q - (long long)r * Hkv);
+            const int b = s_inv[r];
+            e = make_int4(b, hk, s_c[b] / kDecodeChunk, s_c[b]);
+        }
+        a.order[L] = e;
+    }
+    // the split kernel waits for this grid only: keep it ordered after the kernel before
+    pdl_wait();
+}
+
+// The work of this CTA of the split grid: from the dispatch order when there is one, else
+// the grid position (split, KV head, sequence).  False: nothing to do.
+struct DecodeWork {
+    int b, hk, split, ctx;
+};
+
+LL_DEVINL bool decode_work(const AttnDecodeArgs& a, DecodeWork& w) {
+    if (a.order) {
+        const int4 e = a.order[blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z)];
+        w.b = e.x;
+        w.hk = e.y;
+        w.split = e.z;
+        w.ctx = e.w;
+        return e.x >= 0;
+    }
+    w.split = blockIdx.x;
+    w.hk = blockIdx.y;
+    w.b = blockIdx.z;
+    int ctx = a.context_lens[w.b];
+    if (ctx > a.max_blocks * a.block_size || ctx < 0) {
+        if (threadIdx.x == 0 && w.split == 0 && w.hk == 0) flag_status(a.status, LL_DEV_BAD_POSITION);
+        ctx = min(max(ctx, 0), a.max_blocks * a.block_size);
+    }
+    w.ctx = ctx;
+    return true;
+}
+
 // ---------------------------------------------------------------- decode
 
 // Byte offset of 16-byte chunk c of row r in a K/V tile that TMA wrote with the
@@ -77,16 +213,13 @@ __global__ void __launch_bounds__(160, 2)
     __shared__ uint64_t full_bar[STAGES], empty_bar[STAGES];
     __shared__ int abort_s;
 
-    const int split = blockIdx.x, hk = blockIdx.y, b = blockIdx.z;
     const int G = a.n_heads / a.n_kv_heads;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     pdl_wait();
     pdl_trigger();
-    int ctx = a.context_lens[b];
-    if (ctx > a.max_blocks * a.block_size || ctx < 0) {
-        if (threadIdx.x == 0 && split == 0 && hk == 0) flag_status(a.status, LL_DEV_BAD_POSITION);
-        ctx = min(max(ctx, 0), a.max_blocks * a.block_size);
-    }
+    DecodeWork wk;
+    if (!decode_work(a, wk)) return;
+    const int split = wk.split, hk = wk.hk, b = wk.b, ctx = wk.ctx;
     const int k_begin = split * kDecodeChunk;
     const int k_end = min(ctx, k_begin + kDecodeChunk);
     const size_t part_row = ((size_t)b * a.n_heads + (size_t)hk * G) * max_splits + split;
@@ -366,16 +499,13 @@ __global__ void __launch_bounds__(160, NT == 1 ? 4 : 2)
     __shared__ unsigned long long valid_s[STAGES];     // per stage: bit k = key k of the tile is cached
     __shared__ int abort_s;
 
-    const int split = blockIdx.x, hk = blockIdx.y, b = blockIdx.z;
     const int G = a.n_heads / a.n_kv_heads;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     pdl_wait();
     pdl_trigger();
-    int ctx = a.context_lens[b];
-    if (ctx > a.max_blocks * a.block_size || ctx < 0) {
-        if (threadIdx.x == 0 && split == 0 && hk == 0) flag_status(a.status, LL_DEV_BAD_POSITION);
-        ctx = min(max(ctx, 0), a.max_blocks * a.block_size);
-    }
+    DecodeWork wk;
+    if (!decode_work(a, wk)) return;
+    const int split = wk.split, hk = wk.hk, b = wk.b, ctx = wk.ctx;
     const int k_begin = split * kDecodeChunk;
     const int k_end = min(ctx, k_begin + kDecodeChunk);
     const size_t part_row = ((size_t)b * a.n_heads + (size_t)hk * G) * max_splits + split;
@@ -693,9 +823,51 @@ __global__ void attn_decode_combine_kernel(const AttnDecodeArgs a, int max_split
     }
 }
 
+// The dispatch order table sits in the scratch after the split partials (16-byte entries).
+int4* order_table(const AttnDecodeArgs& a, int max_splits) {
+    const size_t rows = (size_t)a.batch * a.n_heads * max_splits;
+    const uintptr_t p = reinterpret_cast<uintptr_t>(a.part_ml + 2 * rows);
+    return reinterpret_cast<int4*>((p + 15) & ~uintptr_t(15));
+}
+
+// Launches the order kernel and points a.order at its table.  The table pays where the
+// grid's tail is long next to the one more kernel it puts between the QKV epilogue and the
+// split kernel: INT8 caches (short CTAs, four per SM) and BF16 contexts of 8 or more splits
+// (measured on GB300: 70B decode step 1.5-2% faster; with at most 4-5 splits per sequence,
+// the 7B decode and the 32-layer continuous batching, 2-4% slower).  Otherwise, and for
+// batches beyond what it sorts in shared memory, a.order is null and the split CTAs work in
+// grid order.
+constexpr int kOrderMinSplitsBf16 = 8;
+
+cudaError_t launch_order(AttnDecodeArgs& a, int max_splits, bool int8_cache, cudaStream_t stream) {
+    if (a.batch > kOrderMaxBatch || (!int8_cache && max_splits < kOrderMinSplitsBf16)) {
+        a.order = nullptr;
+        return cudaSuccess;
+    }
+    static bool configured = false;
+    if (!configured) {
+        cudaError_t e = cudaFuncSetAttribute(attn_decode_order_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)(3 * kOrderMaxBatch * sizeof(int)));
+        if (e != cudaSuccess) return record(e, "cudaFuncSetAttribute(attn_decode_order_kernel)");
+        configured = true;
+    }
+    a.order = order_table(a, max_splits);
+    trace_before("attn_decode_order", stream);
+    cudaError_t e = launch_pdl(attn_decode_order_kernel, dim3(1), dim3(kOrderThreads), 3 * (size_t)a.batch * sizeof(int),
+                               stream, 1, a, max_splits);
+    trace_after(stream);
+    if (e == cudaSuccess) e = cudaGetLastError();
+    return e == cudaSuccess ? cudaSuccess : record(e, "attn_decode_order_kernel launch");
+}
+
 template <int D>
-cudaError_t decode_for(const AttnDecodeArgs& a, cudaStream_t stream) {
+cudaError_t decode_for(const AttnDecodeArgs& args, cudaStream_t stream) {
+    AttnDecodeArgs a = args;
     const int max_splits = attn_decode_max_splits(a.max_blocks, a.block_size);
+    {
+        const cudaError_t eo = launch_order(a, max_splits, false, stream);
+        if (eo != cudaSuccess) return eo;
+    }
     const size_t smem = (size_t)2 * 3 * (64 * D * 2) + 16 * D * 2 + 1024;
     static bool configured = false;
     if (!configured) {
@@ -726,9 +898,14 @@ cudaError_t decode_for(const AttnDecodeArgs& a, cudaStream_t stream) {
 }
 
 template <int NT>
-cudaError_t decode_q8_for(const AttnDecodeArgs& a, cudaStream_t stream) {
+cudaError_t decode_q8_for(const AttnDecodeArgs& args, cudaStream_t stream) {
+    AttnDecodeArgs a = args;
     constexpr int D = 128, BN = 64, STAGES = 3;
     const int max_splits = attn_decode_max_splits(a.max_blocks, a.block_size);
+    {
+        const cudaError_t eo = launch_order(a, max_splits, true, stream);
+        if (eo != cudaSuccess) return eo;
+    }
     const size_t smem = (size_t)STAGES * 2 * BN * D + STAGES * 2 * BN * 4 + 16 * D * 2 + 1024;
     static bool configured = false;
     if (!configured) {
@@ -769,8 +946,10 @@ int attn_decode_max_splits(int max_blocks, int block_size) {
 
 size_t attn_decode_scratch_bytes(int batch, int n_heads, int head_dim, int max_blocks,
                                  int block_size) {
+    // per split row: the partial output and (m, l); then the dispatch order (one 16-byte entry
+    // per CTA of the split grid, at most one per row) behind a 16-byte alignment pad
     const size_t rows = (size_t)batch * n_heads * attn_decode_max_splits(max_blocks, block_size);
-    return rows * head_dim * sizeof(float) + rows * 2 * sizeof(float);
+    return rows * head_dim * sizeof(float) + rows * 2 * sizeof(float) + 16 + rows * sizeof(int4);
 }
 
 cudaError_t launch_attn_decode_q8(const AttnDecodeArgs& a, cudaStream_t stream) {

@@ -169,6 +169,7 @@ struct AttnDecodeArgs {
     const int8_t* v_q8;
     const float* k_scale;          // ... and their scales [num_blocks, n_kv_heads, block_size]
     const float* v_scale;
+    int4* order;                   // dispatch order of the split grid, in the scratch (set by the launcher)
 };
 int attn_decode_max_splits(int max_blocks, int block_size);
 size_t attn_decode_scratch_bytes(int batch, int n_heads, int head_dim, int max_blocks,
