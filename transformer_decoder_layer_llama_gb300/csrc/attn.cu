@@ -250,7 +250,7 @@ __global__ void __launch_bounds__(160, 2)
         if (lane == 0) {
             tma_prefetch_desc(&tmK);
             tma_prefetch_desc(&tmV);
-            uint32_t issued[STAGES] = {0, 0, 0};
+            uint32_t issued = 0, parity = 0;    // per stage: a load was issued; parity of the loads issued
             for (int kt = 0; kt < n_kt; ++kt) {
                 const int st = kt % STAGES;
                 const uint32_t ph = (uint32_t)(kt / STAGES) & 1u;
@@ -276,12 +276,13 @@ __global__ void __launch_bounds__(160, 2)
                         tma_load_2d(sv + off, &tmV, h * 64, row, &full_bar[st]);
                     }
                 }
-                ++issued[st];
+                issued |= 1u << st;
+                parity ^= 1u << st;
             }
             if (abort_s) {
                 volatile int never = 0;
                 for (int st = 0; st < STAGES; ++st)
-                    if (issued[st]) mbar_wait_bounded(&full_bar[st], (issued[st] - 1) & 1u, &never, nullptr);
+                    if ((issued >> st) & 1u) mbar_wait_bounded(&full_bar[st], ((parity >> st) & 1u) ^ 1u, &never, nullptr);
             }
         }
         __syncwarp();
@@ -465,6 +466,14 @@ __global__ void __launch_bounds__(160, 2)
     }
 }
 
+// Column of the INT8 kernel's merge buffer [4 warps][16 rows][128] that holds head dim `col`
+// of row r: XOR-swizzled within each 32-column group, so that a warp's accumulator stores
+// (8 dims 16 apart in 4 row pairs) hit 32 distinct banks and a warp's row reads stay
+// conflict-free.
+LL_DEVINL int q8_merge_col(int r, int col) {
+    return col ^ (((col >> 5) & 3) << 1) ^ ((r >> 1) & 1) ^ (((r >> 2) & 1) << 3);
+}
+
 // ---------------------------------------------------------------- decode over an INT8 cache
 // The same split / warp structure over an INT8 pool (head_dim 128; paging page,
 // section "KV Cache quantisation": the cache block is dequantised as it is
@@ -536,7 +545,7 @@ __global__ void __launch_bounds__(160, NT == 1 ? 4 : 2)
         if (lane == 0) {
             tma_prefetch_desc(&tmK);
             tma_prefetch_desc(&tmV);
-            uint32_t issued[STAGES] = {0, 0, 0};
+            uint32_t issued = 0, parity = 0;    // per stage: a load was issued; parity of the loads issued
             for (int kt = 0; kt < n_kt; ++kt) {
                 const int st = kt % STAGES;
                 const uint32_t ph = (uint32_t)(kt / STAGES) & 1u;
@@ -569,12 +578,13 @@ __global__ void __launch_bounds__(160, NT == 1 ? 4 : 2)
                     bulk_load(ssc + (st * 2 + 1) * BN + sb * kt_rows, a.v_scale + row, (uint32_t)kt_rows * 4u,
                               &full_bar[st]);
                 }
-                ++issued[st];
+                issued |= 1u << st;
+                parity ^= 1u << st;
             }
             if (abort_s) {
                 volatile int never = 0;
                 for (int st = 0; st < STAGES; ++st)
-                    if (issued[st]) mbar_wait_bounded(&full_bar[st], (issued[st] - 1) & 1u, &never, nullptr);
+                    if ((issued >> st) & 1u) mbar_wait_bounded(&full_bar[st], ((parity >> st) & 1u) ^ 1u, &never, nullptr);
             }
         }
         __syncwarp();
@@ -773,8 +783,10 @@ __global__ void __launch_bounds__(160, NT == 1 ? 4 : 2)
 #pragma unroll
         for (int t = 0; t < D / 16; ++t)
 #pragma unroll
-            for (int j = 0; j < 4; ++j)
-                s_acc[(warp * 16 + 8 * nt + 2 * cq + (j & 1)) * D + 16 * g + 2 * t + (j >> 1)] = acc[nt][t][j];
+            for (int j = 0; j < 4; ++j) {
+                const int r = 8 * nt + 2 * cq + (j & 1);
+                s_acc[(warp * 16 + r) * D + q8_merge_col(r, 16 * g + 2 * t + (j >> 1))] = acc[nt][t][j];
+            }
     }
     asm volatile("bar.sync 1, 128;" ::: "memory");
     for (int i = threadIdx.x; i < G * D; i += NCONS) {
@@ -787,7 +799,7 @@ __global__ void __launch_bounds__(160, NT == 1 ? 4 : 2)
 #pragma unroll
         for (int w = 0; w < 4; ++w) {
             const float e = exp2f(s_ml[(w * 16 + r) * 2] - base);
-            num += e * s_acc[(w * 16 + r) * D + col];
+            num += e * s_acc[(w * 16 + r) * D + q8_merge_col(r, col)];
             den += e * s_ml[(w * 16 + r) * 2 + 1];
         }
         const size_t pr = part_row + (size_t)r * max_splits;
