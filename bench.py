@@ -80,6 +80,25 @@ def ncu_traffic(key):
     return e["bytes_per_launch"]
 
 
+# ---------------------------------------------------------------- ranks
+
+def slowest_rank_ms(ms, world, device):
+    """The largest of the ranks' times (all-reduce MAX, then a barrier); a single rank's
+    own time when world == 1."""
+    if world <= 1:
+        return ms
+    import torch.distributed as dist
+    t = torch.tensor([ms], device=device, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.barrier()
+    return float(t.item())
+
+
+def job_throughput(world, units_per_rank_step, ms_step):
+    """Whole-job rate: every rank's units of one step over the slowest rank's step time."""
+    return world * units_per_rank_step / (ms_step * 1e-3)
+
+
 # ---------------------------------------------------------------- work accounting
 
 def gemm_flops(d, T):
@@ -291,7 +310,7 @@ class DecodeQ8(Decode):
                                       workspace=self.ws, status=self.status, stream=stream)
 
 
-def continuous_batching(api, wl, steps, warmup, stream, peaks, seed=4321):
+def continuous_batching(api, wl, steps, warmup, stream, peaks, seed=4321, world=1):
     """The 32-layer stack under continuous batching: 64 slots with resident contexts
     ~U[ctx_lo, ctx_hi] (pre-filled cache), per-request decode budgets ~U[1, 256]; a finished
     request's blocks go back to the free list and a new request is admitted with a 256-token
@@ -391,7 +410,7 @@ def continuous_batching(api, wl, steps, warmup, stream, peaks, seed=4321):
     t_ev[1].record(stream)
     stream.synchronize()
     wall = time.perf_counter() - t0
-    ms = t_ev[0].elapsed_time(t_ev[1])
+    ms = slowest_rank_ms(t_ev[0].elapsed_time(t_ev[1]), world, "cuda")
     status = int(eng.status.item())
     # minimum bytes of the decode steps: every layer's weights + the KV each step reads
     decode_bytes = steps * L * weight_bytes(d) + L * kv_bytes_read(d, [stats["kv_tokens_read"]])
@@ -400,10 +419,10 @@ def continuous_batching(api, wl, steps, warmup, stream, peaks, seed=4321):
     decode_roof_s = decode_bytes / (peaks["hbm_gbs"] * 1e9)
     out = {
         "layers": L, "slots": n_slots, "steps": steps, "ms_total": ms, "wall_s": wall,
-        "decode_tok_per_s": stats["decode_tokens"] / (ms * 1e-3),
-        "total_tok_per_s": (stats["decode_tokens"] + stats["prefill_tokens"]) / (ms * 1e-3),
+        "decode_tok_per_s": job_throughput(world, stats["decode_tokens"], ms),
+        "total_tok_per_s": job_throughput(world, stats["decode_tokens"] + stats["prefill_tokens"], ms),
         "admitted_requests": stats["admitted"],
-        "hbm_gbs_decode_min_bytes": decode_bytes / (ms * 1e-3) / 1e9,
+        "hbm_gbs_decode_min_bytes": job_throughput(world, decode_bytes, ms) / 1e9,
         "roofline_frac": roof_s / (ms * 1e-3),
         # the same run split by phase: the decode CUDA graphs alone against the decode
         # bytes, the batched prefills alone, and what is left (host scheduling, copies)
@@ -602,13 +621,9 @@ def main():
     with ClockSampler(dev_index) as clocks:
         ms = timed_steps(work, args.steps, stream, flush)
     torch.cuda.synchronize()
-    if world > 1:
-        t = torch.tensor([ms], device="cuda", dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
-        dist.barrier()
+    ms = slowest_rank_ms(ms, world, "cuda")
     ms_step = ms / args.steps
-    value = world * work.flops / (ms_step * 1e-3) / 1e12
+    value = job_throughput(world, work.flops, ms_step) / 1e12
     st = int(work.status.item())
 
     per, launches_per_step = traced_breakdown(api, work, min(args.steps, 50), stream, flush)
@@ -640,7 +655,7 @@ def main():
             y_h.copy_(work.y, non_blocking=True)
             b.record(stream)
     stream.synchronize()
-    e2e_ms = sum(a.elapsed_time(b) for a, b in evs) / e2e_steps
+    e2e_ms = slowest_rank_ms(sum(a.elapsed_time(b) for a, b in evs) / e2e_steps, world, "cuda")
     h2d = x_h.numel() * 2 + pos_h.numel() * 4 + tab_h.numel() * 4
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
@@ -649,7 +664,7 @@ def main():
         "data": "synthetic", "config": cfg_json,
         "layer_roofline_frac": work.roofline_s(peaks) / (ms_step * 1e-3),
         "roofline": roof,
-        "e2e": {"value": world * work.flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+        "e2e": {"value": job_throughput(world, work.flops, e2e_ms) / 1e12, "unit": "TFLOP/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": y_h.numel() * 2},
         "gpu_launches": launches_per_step * args.steps,
         "kernels": {k: {"launches_per_step": v["launches"] // n_tr, "ms_per_step": v["ms"] / n_tr,
@@ -674,7 +689,7 @@ def main():
             stream.synchronize()
             k2 = max(args.steps // 2, 10)
             with ClockSampler(dev_index) as ck2:
-                ms2 = timed_steps(dw, k2, stream, flush) / k2
+                ms2 = slowest_rank_ms(timed_steps(dw, k2, stream, flush) / k2, world, "cuda")
             per2, lps2 = traced_breakdown(api, dw, min(k2, 30), stream, flush)
             n2 = min(k2, 30)
             att_ms = (per2.get("attn_decode_split", {"ms": 0})["ms"]
@@ -684,8 +699,8 @@ def main():
             dom_bytes = dw.kv_read if dom == "attn_decode" else weight_bytes(dw.d)
             dom_ms = att_ms if dom == "attn_decode" else gem_ms
             extras[name] = {
-                "tok_per_s": world * dw.B / (ms2 * 1e-3),
-                "hbm_gbs": dw.min_bytes / (ms2 * 1e-3) / 1e9,
+                "tok_per_s": job_throughput(world, dw.B, ms2),
+                "hbm_gbs": job_throughput(world, dw.min_bytes, ms2) / 1e9,
                 "ms_per_step": ms2,
                 "layer_roofline_frac": dw.roofline_s(peaks) / (ms2 * 1e-3),
                 "min_bytes_per_step": dw.min_bytes,
@@ -706,7 +721,7 @@ def main():
         if not args.no_stack:
             line["continuous_batching"] = continuous_batching(
                 api, synth.WORKLOADS["llama2_7b_stack_cb"], synth.WORKLOADS["llama2_7b_stack_cb"].steps,
-                3, stream, peaks)
+                3, stream, peaks, world=world)
 
     if rank == 0 and world == 1 and not args.no_cpu:
         v, n, desc = OracleSample(wl).run(64, budget_s=12.0)
