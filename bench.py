@@ -52,14 +52,14 @@ NCU_TRAFFIC = {
                      "sha256": "9e702575ebb3cd4534ca3821d5aa30f491fe9685ebf4c5eff2f7374e8b5fec5f", "bytes_per_launch": 168.2e6},
     # attn_decode_split_kernel, 7B decode (batch 64)
     "llama2_7b_decode_attn": {"file": "transformer_decoder_layer_llama_gb300/csrc/attn.cu",
-                              "sha256": "2046ad427fc10acb5fdf1716e39e1b9c86992bb7eb60380d23ee3d352144d9f6", "bytes_per_launch": 2245.3e6},
+                              "sha256": "a43aeff2b5f54595a8119e2904dbc0a7e3bba36fe8d4591225fcd4cfe70edb26", "bytes_per_launch": 2245.3e6},
     # one weight-form GEMM (gemm_weight_kernel + gemm_weight_fixup_kernel), 70B decode:
     # mean over the layer's 4 GEMMs
     "llama70b_gqa_decode_gemm": {"file": "transformer_decoder_layer_llama_gb300/csrc/gemm_tc.cu",
                                  "sha256": "9e702575ebb3cd4534ca3821d5aa30f491fe9685ebf4c5eff2f7374e8b5fec5f", "bytes_per_launch": 433.3e6},
     # attn_decode_split_q8_kernel, 7B decode over an INT8 cache (batch 64)
     "llama2_7b_decode_int8kv_attn": {"file": "transformer_decoder_layer_llama_gb300/csrc/attn.cu",
-                                     "sha256": "2046ad427fc10acb5fdf1716e39e1b9c86992bb7eb60380d23ee3d352144d9f6", "bytes_per_launch": 1159.4e6},
+                                     "sha256": "a43aeff2b5f54595a8119e2904dbc0a7e3bba36fe8d4591225fcd4cfe70edb26", "bytes_per_launch": 1159.4e6},
     # one weight-form GEMM, 70B decode over an INT8 cache: mean over the layer's 4 GEMMs
     "llama70b_gqa_decode_int8kv_gemm": {"file": "transformer_decoder_layer_llama_gb300/csrc/gemm_tc.cu",
                                         "sha256": "9e702575ebb3cd4534ca3821d5aa30f491fe9685ebf4c5eff2f7374e8b5fec5f", "bytes_per_launch": 433.1e6},

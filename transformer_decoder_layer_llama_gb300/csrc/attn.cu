@@ -183,6 +183,14 @@ LL_DEVINL bool decode_work(const AttnDecodeArgs& a, DecodeWork& w) {
 
 // ---------------------------------------------------------------- decode
 
+// Column of the BF16 kernel's merge buffer [4 warps][16 rows][D] that holds head dim `col`
+// of row r: bits 0, 3 and 4 XORed with the three low bits of r, so that a warp's
+// accumulator stores (rows g and g + 8, columns 8 i + 2 cq + e) hit 32 distinct banks and
+// a warp's row reads stay conflict-free.
+LL_DEVINL int bf16_merge_col(int r, int col) {
+    return col ^ (r & 1) ^ (((r >> 1) & 1) << 3) ^ (((r >> 2) & 1) << 4);
+}
+
 // Byte offset of 16-byte chunk c of row r in a K/V tile that TMA wrote with the
 // 128-byte swizzle: the tile is [D/64 column halves][ROWS rows][128 bytes] and
 // chunk (c & 7) of a row sits at position (c & 7) ^ (r & 7).
@@ -438,10 +446,10 @@ __global__ void __launch_bounds__(160, 2)
 #pragma unroll
     for (int i = 0; i < D / 8; ++i) {
         const int col = i * 8 + 2 * cq;
-        s_acc[(warp * 16 + g) * D + col] = acc[i][0];
-        s_acc[(warp * 16 + g) * D + col + 1] = acc[i][1];
-        s_acc[(warp * 16 + g + 8) * D + col] = acc[i][2];
-        s_acc[(warp * 16 + g + 8) * D + col + 1] = acc[i][3];
+        s_acc[(warp * 16 + g) * D + bf16_merge_col(g, col)] = acc[i][0];
+        s_acc[(warp * 16 + g) * D + bf16_merge_col(g, col + 1)] = acc[i][1];
+        s_acc[(warp * 16 + g + 8) * D + bf16_merge_col(g, col)] = acc[i][2];
+        s_acc[(warp * 16 + g + 8) * D + bf16_merge_col(g, col + 1)] = acc[i][3];
     }
     asm volatile("bar.sync 1, 128;" ::: "memory");
     for (int i = threadIdx.x; i < G * D; i += NCONS) {
@@ -454,7 +462,7 @@ __global__ void __launch_bounds__(160, 2)
 #pragma unroll
         for (int w = 0; w < 4; ++w) {
             const float e = exp2f(s_ml[(w * 16 + r) * 2] - base);
-            num += e * s_acc[(w * 16 + r) * D + col];
+            num += e * s_acc[(w * 16 + r) * D + bf16_merge_col(r, col)];
             den += e * s_ml[(w * 16 + r) * 2 + 1];
         }
         const size_t pr = part_row + (size_t)r * max_splits;
