@@ -31,7 +31,7 @@ Sources (web pages on Ascend Transformer Boost; cited by page and section):
             fusion graph of a decoder layer": QKV projection as one MatMul,
             then RoPE, then attention, softmax, times V, O projection.
 
-Readings where the pages are silent (each is listed in the design doc):
+Readings where the pages are silent (the same in the CUDA path):
 * RMSNorm: y = x / sqrt(mean(x^2) + eps) * g (g fp32, eps 1e-5).
 * RoPE: half-split pairing (element i with i + d/2), angle pos * theta^(-2i/d).
 * GQA: query head h uses KV head floor(h / (Hq / Hkv)).
