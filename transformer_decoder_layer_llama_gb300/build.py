@@ -1,7 +1,7 @@
 """Builds the C-ABI library libllamalayer.so from csrc/*.cu for sm_103a.
 
 Each translation unit is compiled in parallel with nvcc, then linked with the
-CUDA runtime statically, so the library loads without a GPU (only the driver
+CUDA runtime statically, so the library loads without a GPU (only the CUDA driver
 is needed once a call runs).  Output: <package>/_build/libllamalayer.so.
 """
 from __future__ import annotations
