@@ -40,25 +40,52 @@ struct RowIO<float> {
     }
 };
 
-template <typename In>
+// One row per CTA.  With NV > 0 each thread keeps its NV 8-element vectors of the row
+// (and of the gains) in registers between the sum of squares and the scaling, so the
+// row is read once; NV = 0 reads it twice (any width).  The gains live in the packed
+// weights, which no kernel still running can be writing (packing synchronises its
+// stream), so they load before the grid-dependency wait.
+template <typename In, int NV>
 __global__ void __launch_bounds__(kNormThreads) rmsnorm_kernel(const In* __restrict__ x,
                                                                const float* __restrict__ g,
                                                                __nv_bfloat16* __restrict__ out,
                                                                int hidden, float eps,
                                                                int32_t* zero_ptr, int zero_words) {
+    const int t = blockIdx.x;
+    const int nv = hidden >> 3;
+    const float4* g4 = reinterpret_cast<const float4*>(g);
+    float4 ga[NV > 0 ? NV : 1], gb[NV > 0 ? NV : 1];
+#pragma unroll
+    for (int k = 0; k < NV; ++k) {
+        const int i = threadIdx.x + k * blockDim.x;
+        if (i < nv) {
+            ga[k] = g4[2 * i];
+            gb[k] = g4[2 * i + 1];
+        }
+    }
     pdl_wait();
     pdl_trigger();
-    const int t = blockIdx.x;
     if (zero_ptr && t == 0)
         for (int i = threadIdx.x; i < zero_words; i += blockDim.x) zero_ptr[i] = 0;
     const In* xr = x + (size_t)t * hidden;
-    const int nv = hidden >> 3;
+    float f[NV > 0 ? NV : 1][8];
     float ss = 0.f;
-    for (int i = threadIdx.x; i < nv; i += blockDim.x) {
-        float f[8];
-        RowIO<In>::load(xr, i, f);
+    if (NV > 0) {
 #pragma unroll
-        for (int j = 0; j < 8; ++j) ss += f[j] * f[j];
+        for (int k = 0; k < NV; ++k) {
+            const int i = threadIdx.x + k * blockDim.x;
+            if (i < nv) {
+                RowIO<In>::load(xr, i, f[k]);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) ss += f[k][j] * f[k][j];
+            }
+        }
+    } else {
+        for (int i = threadIdx.x; i < nv; i += blockDim.x) {
+            RowIO<In>::load(xr, i, f[0]);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) ss += f[0][j] * f[0][j];
+        }
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
@@ -74,17 +101,50 @@ __global__ void __launch_bounds__(kNormThreads) rmsnorm_kernel(const In* __restr
     __syncthreads();
     const float r = r_s;
     uint4* orow = reinterpret_cast<uint4*>(out + (size_t)t * hidden);
-    const float4* g4 = reinterpret_cast<const float4*>(g);
-    for (int i = threadIdx.x; i < nv; i += blockDim.x) {
-        float f[8];
-        RowIO<In>::load(xr, i, f);
-        float4 ga = g4[2 * i], gb = g4[2 * i + 1];
+    auto emit = [&](int i, const float (&v)[8], float4 a, float4 b) {
         uint4 o;
-        o.x = pack_bf16x2(f[0] * r * ga.x, f[1] * r * ga.y);
-        o.y = pack_bf16x2(f[2] * r * ga.z, f[3] * r * ga.w);
-        o.z = pack_bf16x2(f[4] * r * gb.x, f[5] * r * gb.y);
-        o.w = pack_bf16x2(f[6] * r * gb.z, f[7] * r * gb.w);
+        o.x = pack_bf16x2(v[0] * r * a.x, v[1] * r * a.y);
+        o.y = pack_bf16x2(v[2] * r * a.z, v[3] * r * a.w);
+        o.z = pack_bf16x2(v[4] * r * b.x, v[5] * r * b.y);
+        o.w = pack_bf16x2(v[6] * r * b.z, v[7] * r * b.w);
         orow[i] = o;
+    };
+    if (NV > 0) {
+#pragma unroll
+        for (int k = 0; k < NV; ++k) {
+            const int i = threadIdx.x + k * blockDim.x;
+            if (i < nv) emit(i, f[k], ga[k], gb[k]);
+        }
+    } else {
+        for (int i = threadIdx.x; i < nv; i += blockDim.x) {
+            RowIO<In>::load(xr, i, f[0]);
+            emit(i, f[0], g4[2 * i], g4[2 * i + 1]);
+        }
+    }
+}
+
+// Launches rmsnorm_kernel with the register-resident row when each thread holds at most
+// four vectors (hidden <= 8192 at 256 threads).
+template <typename In>
+cudaError_t launch_rmsnorm_any(const In* x, const float* g, __nv_bfloat16* out, int tokens, int hidden,
+                               float eps, int32_t* zero_ptr, int zero_words, cudaStream_t stream) {
+    const int nv = hidden / 8;
+    const int threads = std::min(kNormThreads, std::max(32, ((nv + 31) / 32) * 32));
+    const int per = (nv + threads - 1) / threads;
+    switch (per) {
+        case 1:
+            return launch_pdl(rmsnorm_kernel<In, 1>, dim3(tokens), dim3(threads), 0, stream, 1, x, g, out, hidden, eps,
+                              zero_ptr, zero_words);
+        case 2:
+            return launch_pdl(rmsnorm_kernel<In, 2>, dim3(tokens), dim3(threads), 0, stream, 1, x, g, out, hidden, eps,
+                              zero_ptr, zero_words);
+        case 3:
+        case 4:
+            return launch_pdl(rmsnorm_kernel<In, 4>, dim3(tokens), dim3(threads), 0, stream, 1, x, g, out, hidden, eps,
+                              zero_ptr, zero_words);
+        default:
+            return launch_pdl(rmsnorm_kernel<In, 0>, dim3(tokens), dim3(threads), 0, stream, 1, x, g, out, hidden, eps,
+                              zero_ptr, zero_words);
     }
 }
 
@@ -251,10 +311,8 @@ cudaError_t launch_rmsnorm(const __nv_bfloat16* x, const float* g, __nv_bfloat16
                            int hidden, float eps, int32_t* zero_ptr, int zero_words,
                            cudaStream_t stream) {
     if (tokens <= 0) return cudaSuccess;
-    const int threads = std::min(kNormThreads, std::max(32, ((hidden / 8 + 31) / 32) * 32));
     trace_before("rmsnorm", stream);
-    cudaError_t e = launch_pdl(rmsnorm_kernel<__nv_bfloat16>, dim3(tokens), dim3(threads), 0, stream, 1, x,
-                               g, out, hidden, eps, zero_ptr, zero_words);
+    cudaError_t e = launch_rmsnorm_any(x, g, out, tokens, hidden, eps, zero_ptr, zero_words, stream);
     trace_after(stream);
     if (e != cudaSuccess) return record(e, "rmsnorm launch");
     return record(cudaGetLastError(), "rmsnorm launch");
@@ -263,10 +321,8 @@ cudaError_t launch_rmsnorm(const __nv_bfloat16* x, const float* g, __nv_bfloat16
 cudaError_t launch_rmsnorm_f32(const float* x, const float* g, __nv_bfloat16* out, int tokens,
                                int hidden, float eps, cudaStream_t stream) {
     if (tokens <= 0) return cudaSuccess;
-    const int threads = std::min(kNormThreads, std::max(32, ((hidden / 8 + 31) / 32) * 32));
     trace_before("rmsnorm", stream);
-    cudaError_t e = launch_pdl(rmsnorm_kernel<float>, dim3(tokens), dim3(threads), 0, stream, 1, x, g, out,
-                               hidden, eps, (int32_t*)nullptr, 0);
+    cudaError_t e = launch_rmsnorm_any(x, g, out, tokens, hidden, eps, (int32_t*)nullptr, 0, stream);
     trace_after(stream);
     if (e != cudaSuccess) return record(e, "rmsnorm_f32 launch");
     return record(cudaGetLastError(), "rmsnorm_f32 launch");
