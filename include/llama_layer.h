@@ -246,9 +246,14 @@ int ll_paged_attention_decode_q8(const void* q, const ll_kv_pool_q8* pool, const
  * and keeps the per-split partial results in a fixed device array inside the
  * library (32 MiB; every GPU that loads the library holds it until the
  * process exits).  It allocates nothing and calls no allocator.
- *  - Limit: batch * n_heads * ceil(max_blocks * block_size / 1024) *
- *    (head_dim + 2) * 4 bytes must not exceed 32 MiB, else it returns
- *    LL_ERR_UNSUPPORTED (ll_last_error gives the sizes) and launches nothing.
+ *  - Limit: with rows = batch * n_heads * ceil(max_blocks * block_size / 1024)
+ *    (one per 1024-key split of every query head), the call needs
+ *    rows * ((head_dim + 2) * 4 + 16) + 16 bytes of the array (per row the
+ *    float32 partial output, its running max and sum, and a 16-byte entry of
+ *    the splits' dispatch order; then a 16-byte pad);
+ *    ll_attention_workspace_size gives the same figure rounded up to a
+ *    multiple of 256.  Beyond 32 MiB it returns LL_ERR_UNSUPPORTED
+ *    (ll_last_error gives the sizes) and launches nothing.
  *  - The first call on a device resolves the array's device address (this may
  *    load the library's device code); make that first call before any stream
  *    capture on the device.

@@ -31,28 +31,25 @@ def assert_close(got, ref, name="", atol=ATOL, rtol=RTOL):
     assert np.isfinite(got).all(), name
 
 
-# Full-size workloads: the per-element bound above must hold on all but a small
-# fraction of elements, and every element must stay within a hard bound derived
-# from the BF16 operand-rounding cascade.  tests/tolerance_model.py models a
-# correct float32-accumulating BF16 implementation on the CPU: against the
-# float64 oracle it leaves 1.0e-3 of the 7B prefill outputs outside the
-# per-element bound (rms error 5.8e-3, worst 0.044, 2.4x the bound), 1.5e-5 of
-# the 7B decode outputs and none of the 70B decode outputs.  The tensor cores'
-# float32 accumulation adds a little more spread (2.6e-3 measured on GB300).
-FULL_MAX_FRAC_OUTSIDE = 5e-3
-FULL_HARD_ATOL = 6e-2
-
-
-def assert_close_fullsize(got, ref, name=""):
+def outside_stats(got, ref, atol=ATOL, rtol=RTOL):
+    """(fraction of elements outside atol + rtol*|ref|, worst |got - ref| / (atol + rtol*|ref|),
+    rms error) of got against ref."""
     got = np.asarray(got, np.float64)
     ref = np.asarray(ref, np.float64)
-    assert got.shape == ref.shape, (name, got.shape, ref.shape)
-    assert np.isfinite(got).all(), name
+    assert got.shape == ref.shape, (got.shape, ref.shape)
     err = np.abs(got - ref)
-    frac = float((err > ATOL + RTOL * np.abs(ref)).mean())
-    print(f"{name}: {frac:.2e} outside {ATOL}+{RTOL}|ref|, rms error {float(np.sqrt((err ** 2).mean())):.2e}, "
-          f"worst {float((err / (FULL_HARD_ATOL + RTOL * np.abs(ref))).max()):.2f} of the hard bound")
-    assert frac <= FULL_MAX_FRAC_OUTSIDE, (
-        f"{name}: {frac:.2e} of elements outside {ATOL}+{RTOL}|ref| (allowed {FULL_MAX_FRAC_OUTSIDE})")
-    assert_close(got, ref, name + " [hard bound]", atol=FULL_HARD_ATOL, rtol=RTOL)
-    return frac
+    ratio = err / (atol + rtol * np.abs(ref))
+    return float((ratio > 1).mean()), float(ratio.max()), float(np.sqrt((err ** 2).mean()))
+
+
+def assert_within(got, ref, name, max_frac=0.0, max_ratio=1.0):
+    """The per-element bound on all but `max_frac` of the elements, and no element beyond
+    `max_ratio` times the bound.  With the defaults: the bound on every element."""
+    got = np.asarray(got, np.float64)
+    assert np.isfinite(got).all(), name
+    frac, worst, rms = outside_stats(got, ref)
+    print(f"{name}: {frac:.2e} outside {ATOL}+{RTOL}|ref| (limit {max_frac:.1e}), worst {worst:.2f}x "
+          f"(limit {max_ratio:.2f}x), rms error {rms:.2e}")
+    assert frac <= max_frac, f"{name}: {frac:.2e} of elements outside {ATOL}+{RTOL}|ref| (allowed {max_frac:.1e})"
+    assert worst <= max_ratio, f"{name}: worst element at {worst:.2f}x the bound (allowed {max_ratio:.2f}x)"
+    return frac, worst

@@ -366,6 +366,54 @@ def test_bf16_storage_mode_rounds_the_cache():
     np.testing.assert_allclose(y, ye, rtol=0.02, atol=0.02 * np.abs(ye).max())
 
 
+def _on_bf16_grid(a):
+    """Elementwise: is the value a BF16 number (round-tripping through torch's BF16 keeps it)?"""
+    a = np.asarray(a, np.float64)
+    back = torch.from_numpy(a).to(torch.bfloat16).to(torch.float64).numpy()
+    return back == a
+
+
+@pytest.mark.parametrize("mode", ["prefill", "decode"])
+def test_bf16_storage_mode_rounding_points(mode):
+    """Which intermediates the BF16 storage mode rounds, pinned by value: every MatMul
+    operand (x_hat, q, k, v, o, h_hat, a) comes back as BF16 numbers, the float32 residual
+    stream h and the output y do not (their exact values are off the BF16 grid), and each
+    rounded stage is the nearest BF16 of the exact stage value computed from the stage
+    before it (so no tensor is rounded twice, or rounded and then moved).  Adding or
+    dropping one rounding in the layer fails here."""
+    dm = dims(hidden=32, n_heads=4, n_kv_heads=2, head_dim=8, intermediate=40, block_size=4, rms_eps=1e-5)
+    W, rng = _rand_layer(dm, 15)
+    W = {k: (O.bf16_round(v) if k.startswith("w_") else v) for k, v in W.items()}
+    x = O.bf16_round(rng.standard_normal((7, 32)))
+    table = np.array([[1, 0]])
+    kp, vp = _pools(dm, 2, exact=False)
+    want = {}
+    if mode == "prefill":
+        y = O.layer_prefill(dm, W, x, np.arange(7), 1, 7, kp, vp, table, want=want)
+    else:
+        O.layer_prefill(dm, W, x[:6], np.arange(6), 1, 6, kp, vp, table)
+        y = O.layer_decode_step(dm, W, x[6:], kp, vp, table, [7], want=want)
+    for name in ("xh", "q", "k", "v", "o", "hh", "a"):
+        assert _on_bf16_grid(want[name]).all(), f"{name} is not a BF16 tensor"
+    for name, t in (("h", want["h"]), ("y", y)):
+        assert _on_bf16_grid(t).mean() < 0.2, f"{name} looks rounded to BF16"
+    # each rounded stage against torch's BF16 rounding of the exact value from the stage before
+    nearest = lambda t: torch.from_numpy(np.ascontiguousarray(t, np.float64)).to(torch.bfloat16).double().numpy()
+    T = want["xh"].shape[0]
+    xr = x[6:] if mode == "decode" else x
+    ms = np.mean(xr * xr, axis=1, keepdims=True)
+    np.testing.assert_array_equal(want["xh"], nearest(xr / np.sqrt(ms + dm.rms_eps) * W["g_attn"]))
+    qkv = want["xh"] @ W["w_qkv"].T
+    np.testing.assert_array_equal(want["v"], nearest(qkv[:, 48:].reshape(T, 2, 8)))
+    h = xr + want["o"].reshape(T, -1) @ W["w_o"].T
+    np.testing.assert_array_equal(want["h"], h)
+    ms2 = np.mean(h * h, axis=1, keepdims=True)
+    np.testing.assert_array_equal(want["hh"], nearest(h / np.sqrt(ms2 + dm.rms_eps) * W["g_ffn"]))
+    g, u = want["hh"] @ W["w_gate"].T, want["hh"] @ W["w_up"].T
+    np.testing.assert_array_equal(want["a"], nearest(g / (1 + np.exp(-g)) * u))
+    np.testing.assert_array_equal(y, h + want["a"] @ W["w_down"].T)
+
+
 def test_layer_two_token_attention_by_hand():
     # H = Hq*d = 8 (2 heads of d=4, one KV head), W_o = I, FFN zero: y = x + o.  Token 1
     # (position 1) attends to keys 0 and 1 with weight logistic(s0 - s1) on key 0, where

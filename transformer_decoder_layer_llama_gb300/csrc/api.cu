@@ -16,9 +16,12 @@
 
 #include <algorithm>
 #include <cmath>
-#include <vector>
 #include <cstdio>
 #include <cstring>
+#include <map>
+#include <mutex>
+#include <tuple>
+#include <vector>
 
 #include "../../include/llama_layer.h"
 #include "kernels.h"
@@ -321,6 +324,27 @@ int run_layer(const ll_config* cfg, const void* packed, const void* x, const int
 }  // namespace
 
 namespace ll {
+namespace {
+std::mutex g_attr_mu;
+std::map<std::tuple<int, const void*, int>, int> g_attr_set;   // (device, kernel, attribute) -> value
+}  // namespace
+
+cudaError_t ensure_func_attr(const void* kernel, cudaFuncAttribute attr, int value, const char* what) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return record(e, "cudaGetDevice");
+    std::lock_guard<std::mutex> lock(g_attr_mu);
+    const auto key = std::make_tuple(dev, kernel, (int)attr);
+    auto it = g_attr_set.find(key);
+    if (it != g_attr_set.end() &&
+        (it->second == value || (attr == cudaFuncAttributeMaxDynamicSharedMemorySize && it->second >= value)))
+        return cudaSuccess;
+    e = cudaFuncSetAttribute(kernel, attr, value);
+    if (e != cudaSuccess) return record(e, what);
+    g_attr_set[key] = value;
+    return cudaSuccess;
+}
+
 void set_last_error(const char* where, const char* what) {
     snprintf(g_last_error, sizeof(g_last_error), "%s: %s", where, what);
 }

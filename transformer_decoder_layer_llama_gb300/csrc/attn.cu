@@ -497,7 +497,12 @@ LL_DEVINL int q8_merge_col(int r, int col) {
 // scale multiplies its score and its V scale its probability before P V, so
 // dequantised values are never formed; the row sum stays the sum of the
 // unscaled probabilities.  Q enters as FP16 (exact for BF16 values of FP16's
-// range), P as one FP16 operand (the cache's INT8 rounding dominates its error).
+// range).  P times the V scale enters P V as two FP16 parts (hi + lo), with the
+// exponent base set by the largest such weight so that the parts stay in FP16's
+// normal range: one FP16 operand under the score's own base left 7e-3 of the 7B
+// decode layer's outputs outside the per-element bound against the oracle (which
+// reads the same codes exactly), and a CPU model of the layer puts this form at
+// 6e-4, the same as exact probabilities.
 // One column tile runs four CTAs per SM (94 registers); two run two (their
 // accumulators take 64 registers).
 template <int NT>
@@ -688,6 +693,11 @@ __global__ void __launch_bounds__(160, NT == 1 ? 4 : 2)
         const bool v0 = (okmask >> g) & 1u, v1 = (okmask >> (g + 8)) & 1u;
         const float f0 = sl2 * ksc[g], f1 = sl2 * ksc[g + 8];
         const float vs0 = v0 ? vsc[g] : 0.f, vs1 = v1 ? vsc[g + 8] : 0.f;
+        // A key's weight in P V is its probability times its V scale, so the exponent base
+        // follows the largest log2 weight: P times the V scale then stays below 2^8 and in FP16's
+        // normal range down to 2^-14 of the largest weight (keys below that no longer matter).
+        // Scales under 2^-40 count as 2^-40, which keeps P itself below 2^48.
+        const float lv0 = fmaxf(lg2_approx(vs0), -40.f), lv1 = fmaxf(lg2_approx(vs1), -40.f);
         float mx[NT][2];
         bool grow = false;
 #pragma unroll
@@ -696,8 +706,8 @@ __global__ void __launch_bounds__(160, NT == 1 ? 4 : 2)
             s[nt][1] = v0 ? s[nt][1] * f0 : -INFINITY;
             s[nt][2] = v1 ? s[nt][2] * f1 : -INFINITY;
             s[nt][3] = v1 ? s[nt][3] * f1 : -INFINITY;
-            mx[nt][0] = fmaxf(s[nt][0], s[nt][2]);
-            mx[nt][1] = fmaxf(s[nt][1], s[nt][3]);
+            mx[nt][0] = fmaxf(s[nt][0] + lv0, s[nt][2] + lv1);
+            mx[nt][1] = fmaxf(s[nt][1] + lv0, s[nt][3] + lv1);
 #pragma unroll
             for (int o = 4; o <= 16; o <<= 1) {
                 mx[nt][0] = fmaxf(mx[nt][0], __shfl_xor_sync(0xffffffffu, mx[nt][0], o));
@@ -705,8 +715,8 @@ __global__ void __launch_bounds__(160, NT == 1 ? 4 : 2)
             }
             grow = grow || mx[nt][0] > m[nt][0] + 8.f || mx[nt][1] > m[nt][1] + 8.f;
         }
-        // The exponent base of a column moves only when its max grows by more than 2^8 (P then
-        // stays below 256); otherwise the running sums need no rescaling this tile.
+        // The exponent base of a column moves only when its max grows by more than 2^8 (P times
+        // the V scale then stays below 256); otherwise the running sums need no rescaling.
         if (__any_sync(0xffffffffu, grow)) {
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt)
@@ -723,8 +733,9 @@ __global__ void __launch_bounds__(160, NT == 1 ? 4 : 2)
                     m[nt][e] = mn;
                 }
         }
-        // P^T (each key's V scale riding on its probability) as the B fragments of O^T = V^T P^T
-        uint32_t pb[NT][2];
+        // P^T (each key's V scale riding on its probability) as the B fragments of O^T = V^T P^T,
+        // in two FP16 parts (hi + lo, about 22 significant bits together)
+        uint32_t pb[NT][2], pl[NT][2];
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
             const float b0 = (m[nt][0] == -INFINITY) ? 0.f : m[nt][0];
@@ -733,8 +744,13 @@ __global__ void __launch_bounds__(160, NT == 1 ? 4 : 2)
             const float p10 = ex2_approx(s[nt][2] - b0), p11 = ex2_approx(s[nt][3] - b1);
             l[nt][0] += p00 + p10;
             l[nt][1] += p01 + p11;
-            pb[nt][0] = movmatrix_trans(pack_f16x2(p00 * vs0, p01 * vs0));   // keys 0-7
-            pb[nt][1] = movmatrix_trans(pack_f16x2(p10 * vs1, p11 * vs1));   // keys 8-15
+            uint32_t h0, l0, h1, l1;
+            split_f16x2(p00 * vs0, p01 * vs0, h0, l0);     // keys 0-7
+            split_f16x2(p10 * vs1, p11 * vs1, h1, l1);     // keys 8-15
+            pb[nt][0] = movmatrix_trans(h0);
+            pb[nt][1] = movmatrix_trans(h1);
+            pl[nt][0] = movmatrix_trans(l0);
+            pl[nt][1] = movmatrix_trans(l1);
         }
         // O^T += V^T P^T: lane g reads one 16-byte chunk (dims 16 g .. 16 g + 15) of each of its
         // key rows 2 cq, 2 cq + 1, 2 cq + 8, 2 cq + 9 and byte-interleaves the rows of a key pair
@@ -762,6 +778,8 @@ __global__ void __launch_bounds__(160, NT == 1 ? 4 : 2)
             for (int nt = 0; nt < NT; ++nt) {
                 mma_f16_16816(acc[nt][2 * i], at0, pb[nt][0], pb[nt][1]);
                 mma_f16_16816(acc[nt][2 * i + 1], at1, pb[nt][0], pb[nt][1]);
+                mma_f16_16816(acc[nt][2 * i], at0, pl[nt][0], pl[nt][1]);
+                mma_f16_16816(acc[nt][2 * i + 1], at1, pl[nt][0], pl[nt][1]);
             }
         }
         __syncwarp();
@@ -864,12 +882,12 @@ cudaError_t launch_order(AttnDecodeArgs& a, int max_splits, bool int8_cache, cud
         a.order = nullptr;
         return cudaSuccess;
     }
-    static bool configured = false;
-    if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(attn_decode_order_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)(3 * kOrderMaxBatch * sizeof(int)));
-        if (e != cudaSuccess) return record(e, "cudaFuncSetAttribute(attn_decode_order_kernel)");
-        configured = true;
+    {
+        const cudaError_t e = ensure_func_attr((const void*)attn_decode_order_kernel,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               (int)(3 * kOrderMaxBatch * sizeof(int)),
+                                               "cudaFuncSetAttribute(attn_decode_order_kernel)");
+        if (e != cudaSuccess) return e;
     }
     a.order = order_table(a, max_splits);
     trace_before("attn_decode_order", stream);
@@ -889,12 +907,11 @@ cudaError_t decode_for(const AttnDecodeArgs& args, cudaStream_t stream) {
         if (eo != cudaSuccess) return eo;
     }
     const size_t smem = (size_t)2 * 3 * (64 * D * 2) + 16 * D * 2 + 1024;
-    static bool configured = false;
-    if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(attn_decode_split_kernel<D>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return record(e, "cudaFuncSetAttribute(attn_decode_split_kernel)");
-        configured = true;
+    {
+        const cudaError_t e = ensure_func_attr((const void*)attn_decode_split_kernel<D>,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem,
+                                               "cudaFuncSetAttribute(attn_decode_split_kernel)");
+        if (e != cudaSuccess) return e;
     }
     CUtensorMap tmK, tmV;
     const uint64_t rows = (uint64_t)a.num_blocks * a.n_kv_heads * a.block_size;
@@ -927,16 +944,16 @@ cudaError_t decode_q8_for(const AttnDecodeArgs& args, cudaStream_t stream) {
         if (eo != cudaSuccess) return eo;
     }
     const size_t smem = (size_t)STAGES * 2 * BN * D + STAGES * 2 * BN * 4 + 16 * D * 2 + 1024;
-    static bool configured = false;
-    if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(attn_decode_split_q8_kernel<NT>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return record(e, "cudaFuncSetAttribute(attn_decode_split_q8_kernel)");
+    {
+        cudaError_t e = ensure_func_attr((const void*)attn_decode_split_q8_kernel<NT>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem,
+                                         "cudaFuncSetAttribute(attn_decode_split_q8_kernel)");
+        if (e != cudaSuccess) return e;
         // four CTAs of 56 KB per SM need the whole shared-memory carveout
-        e = cudaFuncSetAttribute(attn_decode_split_q8_kernel<NT>, cudaFuncAttributePreferredSharedMemoryCarveout,
-                                 (int)cudaSharedmemCarveoutMaxShared);
-        if (e != cudaSuccess) return record(e, "cudaFuncSetAttribute(attn_decode_split_q8_kernel carveout)");
-        configured = true;
+        e = ensure_func_attr((const void*)attn_decode_split_q8_kernel<NT>,
+                             cudaFuncAttributePreferredSharedMemoryCarveout, (int)cudaSharedmemCarveoutMaxShared,
+                             "cudaFuncSetAttribute(attn_decode_split_q8_kernel carveout)");
+        if (e != cudaSuccess) return e;
     }
     CUtensorMap tmK, tmV;
     const uint64_t rows = (uint64_t)a.num_blocks * a.n_kv_heads * a.block_size;

@@ -445,12 +445,11 @@ template <int D>
 cudaError_t prefill_tc_for(const AttnPrefillArgs& a, cudaStream_t stream) {
     using L = TcLayout<D>;
     const size_t smem = L::TOTAL + 1024;
-    static bool configured = false;
-    if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(attn_prefill_tc_kernel<D>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return record(e, "cudaFuncSetAttribute(attn_prefill_tc_kernel)");
-        configured = true;
+    {
+        const cudaError_t e = ensure_func_attr((const void*)attn_prefill_tc_kernel<D>,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem,
+                                               "cudaFuncSetAttribute(attn_prefill_tc_kernel)");
+        if (e != cudaSuccess) return e;
     }
     TcArgs args{a, std::min(a.block_size, kKT)};
     CUtensorMap tmQ, tmK, tmV;

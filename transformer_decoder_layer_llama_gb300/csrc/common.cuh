@@ -39,6 +39,13 @@ LL_DEVINL float ex2_approx(float x) {
     return y;
 }
 
+// log2(x) by the SFU instruction (approximate; lg2(0) = -inf).
+LL_DEVINL float lg2_approx(float x) {
+    float y;
+    asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 LL_DEVINL void flag_status(int32_t* status, int32_t bits) {
     if (status) atomicOr(status, bits);
 }
@@ -433,6 +440,14 @@ LL_DEVINL void mma_f16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
 LL_DEVINL uint32_t pack_f16x2(float lo, float hi) {
     __half2 v = __floats2half2_rn(lo, hi);
     return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// Two FP16 pairs whose sum carries (a, b) to about 22 significant bits:
+// hi = fp16(a, b), lo = fp16(a - hi.a, b - hi.b).
+LL_DEVINL void split_f16x2(float a, float b, uint32_t& hi, uint32_t& lo) {
+    hi = pack_f16x2(a, b);
+    const float2 h = __half22float2(*reinterpret_cast<const __half2*>(&hi));
+    lo = pack_f16x2(a - h.x, b - h.y);
 }
 
 // Transpose of an 8x8 FP16 matrix held one pair per lane (lane 4 r + c holds row

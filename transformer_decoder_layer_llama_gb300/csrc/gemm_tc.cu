@@ -538,8 +538,6 @@ LL_DEVINL bool epi_all(bool v) {
     return r != 0;
 }
 
-LL_DEVINL void epi_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
-
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_weight_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                        const GemmArgs a) {
@@ -1033,12 +1031,11 @@ cudaError_t launch_gemm(const GemmProblem& pr, cudaStream_t stream) {
         if (!make_tmap(&tA2, pr.act, pr.k, pr.tokens, BM) || !make_tmap(&tB2, pr.w, pr.k, pr.n, BM))
             return cudaErrorInvalidValue;
         const size_t smem = (size_t)a.stages * a.stage_bytes + 1024;
-        static int configured_smem2 = 0;
-        if ((int)smem > configured_smem2) {
-            cudaError_t e = cudaFuncSetAttribute(gemm_token2_kernel,
-                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-            if (e != cudaSuccess) return record(e, "cudaFuncSetAttribute(gemm_token2_kernel)");
-            configured_smem2 = (int)smem;
+        {
+            const cudaError_t e = ensure_func_attr((const void*)gemm_token2_kernel,
+                                                   cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem,
+                                                   "cudaFuncSetAttribute(gemm_token2_kernel)");
+            if (e != cudaSuccess) return e;
         }
         const int pairs = std::min(a.units, sms / 2);
         trace_before("gemm_tc", stream);
@@ -1048,13 +1045,11 @@ cudaError_t launch_gemm(const GemmProblem& pr, cudaStream_t stream) {
         if (e != cudaSuccess) return record(e, "gemm_token2_kernel launch");
         return record(cudaGetLastError(), "gemm_token2_kernel launch");
     }
-    static int configured_smem_w = 0;
-    if ((int)p.smem_bytes > configured_smem_w) {
-        cudaError_t e = cudaFuncSetAttribute(gemm_weight_kernel,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)p.smem_bytes);
-        if (e != cudaSuccess) return record(e, "cudaFuncSetAttribute(gemm_weight_kernel)");
-        configured_smem_w = (int)p.smem_bytes;
+    {
+        const cudaError_t e = ensure_func_attr((const void*)gemm_weight_kernel,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.smem_bytes,
+                                               "cudaFuncSetAttribute(gemm_weight_kernel)");
+        if (e != cudaSuccess) return e;
     }
     if (!pr.partials || pr.partial_bytes < (size_t)p.units * 2 * pr.tokens * BM * sizeof(float)) {
         set_last_error("launch_gemm", "weight form needs split-K scratch");

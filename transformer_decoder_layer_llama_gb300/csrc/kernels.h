@@ -105,6 +105,12 @@ bool make_tmap_u8_sw128(CUtensorMap* m, const void* ptr, uint64_t rows, uint32_t
 
 int device_sm_count();
 
+// Sets function attribute `attr` of `kernel` to `value` on the current device, once per
+// (device, kernel, attribute): function attributes belong to each device's context, so a
+// process driving several GPUs configures each.  For the dynamic shared-memory size the
+// largest value asked for so far stays set.  Thread-safe; records the failing step.
+cudaError_t ensure_func_attr(const void* kernel, cudaFuncAttribute attr, int value, const char* what);
+
 // Records why the current call failed (thread-local; read by ll_last_error).
 void set_last_error(const char* where, const char* what);
 void clear_last_error();

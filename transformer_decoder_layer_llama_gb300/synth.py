@@ -153,6 +153,17 @@ def make_pool(num_blocks: int, d: LayerDims, seed: int, fill: str = "normal"):
     raise ValueError(fill)
 
 
+def make_pool_q8(num_blocks: int, d: LayerDims, seed: int):
+    """A pre-filled INT8 pool: (k_codes, v_codes, k_scales, v_scales); codes int8
+    `[num_blocks, n_kv_heads, block_size, head_dim]` uniform on -127..127, scales float32
+    `[num_blocks, n_kv_heads, block_size]` uniform on [0.001, 0.031) (dequantised cache
+    values of order 1, like the BF16 pools' N(0, 1))."""
+    shape = (num_blocks, d.n_kv_heads, d.block_size, d.head_dim)
+    codes = lambda tag: torch.randint(-127, 128, shape, generator=_gen(seed, tag), dtype=torch.int8)
+    scales = lambda tag: torch.rand(shape[:3], generator=_gen(seed, tag), dtype=torch.float32) * 0.03 + 0.001
+    return codes("k_codes"), codes("v_codes"), scales("k_scales"), scales("v_scales")
+
+
 def prefill_positions(batch: int, seq_len: int, start: int = 0) -> torch.Tensor:
     """Positions start..start+seq_len-1 for each of `batch` sequences, token-major [B*S]."""
     return (torch.arange(seq_len, dtype=torch.int32) + start).repeat(batch)
