@@ -156,6 +156,46 @@ typedef struct {
 int ll_workspace_checkpoints(const ll_config* cfg, int32_t max_tokens, int32_t max_blocks,
                              ll_checkpoints* out);
 
+/* Execution modes of a layer call (page "ATB fused-operator matrix and KV-cache
+ * management", section on the engineering limits of fusion granularity, which
+ * names a step-by-step mode, a fused mode and a fused mode with verification
+ * checkpoints).  LL_MODE_FUSED is the fused chain of ll_layer_prefill and
+ * ll_layer_decode_step, whose kernel outputs stay readable through
+ * ll_workspace_checkpoints (the checkpointed mode needs nothing more).
+ * LL_MODE_STEP_BY_STEP runs every operator of the chain as its own kernel and
+ * keeps every intermediate: RMSNorm, the merged QKV Linear (float32 output),
+ * RotaryEmbedding, the slot mapping, ReshapeAndCache, attention, the O Linear,
+ * the residual add, RMSNorm, the merged gate/up Linear, SiLU * up, the down
+ * Linear and the residual add.  Its element-wise arithmetic is the fused
+ * epilogues', so the two modes compute the same values; it exists to locate a
+ * wrong result by comparing one operator at a time.  It takes BF16 pools. */
+#define LL_MODE_FUSED 0
+#define LL_MODE_STEP_BY_STEP 1
+
+/* Workspace bytes for calls in `mode` (LL_MODE_FUSED: ll_workspace_size). */
+size_t ll_workspace_size_mode(const ll_config* cfg, int32_t max_tokens, int32_t max_blocks, int32_t mode);
+
+/* The step-by-step mode's extra intermediates, as byte offsets from the start of a
+ * workspace sized by ll_workspace_size_mode(cfg, max_tokens, max_blocks,
+ * LL_MODE_STEP_BY_STEP); the offsets of ll_workspace_checkpoints hold in that
+ * workspace too.  After a step-by-step call over T tokens, row t < T of:
+ *   qkv      float32 [T][(n_heads + 2 n_kv_heads) head_dim]  x_hat W_qkv^T before RoPE, in the
+ *            packed column order: within each Q and K head column 2i holds element i and
+ *            2i + 1 element i + head_dim/2; V heads in element order
+ *   k, v     BF16    [T][n_kv_heads head_dim]   K after RoPE and V, element order
+ *   slots    int32   [T]                        cache slot of each token (-1 if invalid)
+ *   o_proj   float32 [T][hidden]                o W_o^T
+ *   gate_up  float32 [T][2 intermediate]        h_hat W_gate^T and h_hat W_up^T, interleaved
+ *                                               (column 2j gate j, 2j + 1 up j)
+ *   down     float32 [T][hidden]                a W_down^T
+ * Host-only; no GPU work. */
+typedef struct {
+    size_t qkv, k, v, slots, o_proj, gate_up, down;
+} ll_step_checkpoints;
+
+int ll_workspace_step_checkpoints(const ll_config* cfg, int32_t max_tokens, int32_t max_blocks,
+                                  ll_step_checkpoints* out);
+
 /* Prefill: x BF16 [batch*seq_len, hidden], token-major; token t belongs to
  * sequence t / seq_len and sits at positions[t] (int32 [batch*seq_len]).
  * Writes every token's K and V (after RoPE on K) into the pool at
@@ -179,6 +219,18 @@ int ll_layer_decode_step(const ll_config* cfg, const void* packed, const void* x
                          const ll_kv_pool* pool, const int32_t* block_table, int32_t max_blocks,
                          const int32_t* context_lens, int32_t batch, void* y, void* workspace,
                          size_t workspace_bytes, int32_t* status, void* stream);
+
+/* ll_layer_prefill and ll_layer_decode_step with an execution mode (LL_MODE_FUSED or
+ * LL_MODE_STEP_BY_STEP; anything else is LL_ERR_INVALID_ARG).  Arguments as there; the
+ * workspace comes from ll_workspace_size_mode for the same mode. */
+int ll_layer_prefill_mode(const ll_config* cfg, const void* packed, const void* x, const int32_t* positions,
+                          int32_t batch, int32_t seq_len, const ll_kv_pool* pool, const int32_t* block_table,
+                          int32_t max_blocks, void* y, void* workspace, size_t workspace_bytes, int32_t* status,
+                          int32_t mode, void* stream);
+int ll_layer_decode_step_mode(const ll_config* cfg, const void* packed, const void* x, const ll_kv_pool* pool,
+                              const int32_t* block_table, int32_t max_blocks, const int32_t* context_lens,
+                              int32_t batch, void* y, void* workspace, size_t workspace_bytes, int32_t* status,
+                              int32_t mode, void* stream);
 
 /* ll_layer_decode_step over an INT8 pool: the new tokens' K and V (after RoPE,
  * BF16) are quantised into the pool as ll_reshape_and_cache_q8 does, and the

@@ -345,7 +345,9 @@ def layer_forward(dims, W, x, positions, seq_of_token, k_pool, v_pool, block_tab
     x [T, H]; positions[T]; seq_of_token[T] (the sequence each token belongs to).
     Every token's K/V is written to the cache at its position first; then each
     query at position p attends over cache positions 0..p of its sequence.
-    want: optional dict that receives the intermediates by name.
+    want: optional dict that receives the intermediates by name: xh, qkv (before RoPE), q, k,
+      v (after RoPE; v as cached), o, o_proj (o W_o^T), h, hh, gate, up, a, down (a W_down^T),
+      slots.
     """
     rnd = _rounder(storage)
     H, Hq, Hkv, d = dims.hidden, dims.n_heads, dims.n_kv_heads, dims.head_dim
@@ -400,7 +402,8 @@ def layer_forward(dims, W, x, positions, seq_of_token, k_pool, v_pool, block_tab
     o = rnd(o)
 
     # 6. O projection + residual (the residual stream is not a MatMul operand: not rounded)
-    h1 = x + o.reshape(T, Hq * d) @ w["w_o"].T
+    o_proj = o.reshape(T, Hq * d) @ w["w_o"].T
+    h1 = x + o_proj
 
     # 7-8. RMSNorm, merged gate/up projection, SwiGLU
     if form == "opbyop":
@@ -418,10 +421,12 @@ def layer_forward(dims, W, x, positions, seq_of_token, k_pool, v_pool, block_tab
     a = rnd(silu(gate) * up)
 
     # 9. down projection + residual
-    y = h1 + a @ w["w_down"].T
+    down = a @ w["w_down"].T
+    y = h1 + down
     if want is not None:
-        want.update(xh=xh, q=q, k=k, v=v, o=o, h=h1, hh=hh if form == "opbyop" or storage == "bf16" else None,
-                    a=a, slots=np.asarray(slots))
+        want.update(xh=xh, qkv=qkv, q=q, k=k, v=v, o=o, o_proj=o_proj, h=h1,
+                    hh=hh if form == "opbyop" or storage == "bf16" else None,
+                    gate=gate, up=up, a=a, down=down, slots=np.asarray(slots))
     return y
 
 

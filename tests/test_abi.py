@@ -42,6 +42,23 @@ def test_sizes_are_host_arithmetic():
     assert api.workspace_size(c, 0, 16) == 0
 
 
+def test_step_by_step_workspace_is_the_fused_one_plus_its_intermediates():
+    c = api.make_config(synth.DIMS_7B, 4096)
+    T, mb = 64, 32
+    fused = api.workspace_size(c, T, mb)
+    assert api.lib.ll_workspace_size_mode(ctypes.byref(c), T, mb, api.LL_MODE_FUSED) == fused
+    step = api.workspace_size(c, T, mb, api.LL_MODE_STEP_BY_STEP)
+    nqkv, H, I = 12288, 4096, 11008
+    extra = T * (nqkv + 1 + H + 2 * I + H) * 4
+    assert extra <= step - fused < extra + 6 * 256
+    assert api.lib.ll_workspace_size_mode(ctypes.byref(c), T, mb, 2) == 0
+    cp, sp = api.ll_checkpoints(), api.ll_step_checkpoints()
+    assert api.lib.ll_workspace_checkpoints(ctypes.byref(c), T, mb, ctypes.byref(cp)) == 0
+    assert api.lib.ll_workspace_step_checkpoints(ctypes.byref(c), T, mb, ctypes.byref(sp)) == 0
+    assert fused <= sp.qkv < sp.slots < sp.o_proj < sp.gate_up < sp.down < step
+    assert sp.down + T * H * 4 <= step and cp.a < fused
+
+
 def test_host_validation_returns_codes_without_launching():
     c = api.make_config(synth.DIMS_TINY, 128)
     pool = api.ll_kv_pool(0, 0, 0)

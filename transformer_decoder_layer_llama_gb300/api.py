@@ -20,6 +20,9 @@ LL_ERR_UNSUPPORTED = 2
 LL_ERR_WORKSPACE = 3
 LL_ERR_CUDA = 4
 
+LL_MODE_FUSED = 0
+LL_MODE_STEP_BY_STEP = 1
+
 LL_DEV_BAD_BLOCK = 1
 LL_DEV_BAD_SLOT = 2
 LL_DEV_BAD_POSITION = 4
@@ -32,7 +35,8 @@ EXPORTED = [
     "ll_linear", "ll_device_sm_count", "ll_trace_begin", "ll_trace_end", "ll_trace_elapsed_ms",
     "ll_trace_name", "ll_paged_attention_decode_noalloc", "ll_selftest_bounded_wait",
     "ll_workspace_checkpoints", "ll_reshape_and_cache_q8", "ll_paged_attention_decode_q8",
-    "ll_layer_decode_step_q8",
+    "ll_layer_decode_step_q8", "ll_workspace_size_mode", "ll_workspace_step_checkpoints",
+    "ll_layer_prefill_mode", "ll_layer_decode_step_mode",
 ]
 
 
@@ -62,6 +66,10 @@ class ll_kv_pool_q8(ctypes.Structure):
 class ll_checkpoints(ctypes.Structure):
     _fields_ = [("x_hat", ctypes.c_size_t), ("q", ctypes.c_size_t), ("o", ctypes.c_size_t),
                 ("h", ctypes.c_size_t), ("h_hat", ctypes.c_size_t), ("a", ctypes.c_size_t)]
+
+
+class ll_step_checkpoints(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_size_t) for n in ("qkv", "k", "v", "slots", "o_proj", "gate_up", "down")]
 
 
 def _load():
@@ -101,6 +109,10 @@ def _load():
                                                         I32, I32, ctypes.c_float, P, P, S, P, P]),
         "ll_layer_decode_step_q8": (ctypes.c_int, [cfgp, P, P, ctypes.POINTER(ll_kv_pool_q8), P, I32, P, I32, P, P,
                                                    S, P, P]),
+        "ll_workspace_size_mode": (S, [cfgp, I32, I32, I32]),
+        "ll_workspace_step_checkpoints": (ctypes.c_int, [cfgp, I32, I32, ctypes.POINTER(ll_step_checkpoints)]),
+        "ll_layer_prefill_mode": (ctypes.c_int, [cfgp, P, P, P, I32, I32, poolp, P, I32, P, P, S, P, I32, P]),
+        "ll_layer_decode_step_mode": (ctypes.c_int, [cfgp, P, P, poolp, P, I32, P, I32, P, P, S, P, I32, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -184,12 +196,14 @@ def pack_weights(cfg: ll_config, W: dict, stream=None) -> torch.Tensor:
     return packed
 
 
-def workspace_size(cfg: ll_config, max_tokens: int, max_blocks: int) -> int:
-    return lib.ll_workspace_size(ctypes.byref(cfg), int(max_tokens), int(max_blocks))
+def workspace_size(cfg: ll_config, max_tokens: int, max_blocks: int, mode: int = LL_MODE_FUSED) -> int:
+    if mode == LL_MODE_FUSED:
+        return lib.ll_workspace_size(ctypes.byref(cfg), int(max_tokens), int(max_blocks))
+    return lib.ll_workspace_size_mode(ctypes.byref(cfg), int(max_tokens), int(max_blocks), int(mode))
 
 
-def new_workspace(cfg, max_tokens, max_blocks, device=None):
-    n = workspace_size(cfg, max_tokens, max_blocks)
+def new_workspace(cfg, max_tokens, max_blocks, device=None, mode=LL_MODE_FUSED):
+    n = workspace_size(cfg, max_tokens, max_blocks, mode)
     if n == 0:
         raise LayerError("ll_workspace_size", LL_ERR_INVALID_ARG)
     return torch.empty(n, dtype=torch.uint8, device=device or "cuda")
@@ -218,6 +232,31 @@ def checkpoints(cfg: ll_config, workspace: torch.Tensor, max_tokens: int, max_bl
     return views
 
 
+def step_checkpoints(cfg: ll_config, workspace: torch.Tensor, max_tokens: int, max_blocks: int,
+                     tokens: int) -> dict:
+    """Views into a step-by-step workspace (new_workspace(..., mode=LL_MODE_STEP_BY_STEP)) of
+    the intermediates that mode adds, after a call over `tokens` tokens: qkv (float32, packed
+    column order), k, v (BF16), slots (int32), o_proj, gate_up (interleaved), down (float32)."""
+    out = ll_step_checkpoints()
+    rc = lib.ll_workspace_step_checkpoints(ctypes.byref(cfg), int(max_tokens), int(max_blocks), ctypes.byref(out))
+    if rc != 0:
+        raise LayerError("ll_workspace_step_checkpoints", rc)
+    if not 0 < tokens <= max_tokens:
+        raise ValueError("tokens must be in 1..max_tokens")
+    nqkv = (cfg.n_heads + 2 * cfg.n_kv_heads) * cfg.head_dim
+    nkv = cfg.n_kv_heads * cfg.head_dim
+    shapes = {"qkv": ((nqkv,), torch.float32), "k": ((nkv,), torch.bfloat16), "v": ((nkv,), torch.bfloat16),
+              "slots": ((), torch.int32), "o_proj": ((cfg.hidden,), torch.float32),
+              "gate_up": ((2 * cfg.intermediate,), torch.float32), "down": ((cfg.hidden,), torch.float32)}
+    views = {}
+    for name, (width, dt) in shapes.items():
+        off = getattr(out, name)
+        count = tokens * (width[0] if width else 1)
+        nbytes = count * (torch.finfo(dt).bits if dt.is_floating_point else torch.iinfo(dt).bits) // 8
+        views[name] = workspace[off:off + nbytes].view(dt).view(tokens, *width)
+    return views
+
+
 def _pool(k_pool, v_pool):
     _need(k_pool, "k_pool", torch.bfloat16)
     _need(v_pool, "v_pool", torch.bfloat16)
@@ -227,8 +266,9 @@ def _pool(k_pool, v_pool):
 
 
 def layer_prefill(cfg, packed, x, positions, batch, seq_len, k_pool, v_pool, block_table,
-                  y=None, workspace=None, status=None, stream=None):
-    """ll_layer_prefill.  Returns y (BF16 [batch*seq_len, hidden])."""
+                  y=None, workspace=None, status=None, stream=None, mode=LL_MODE_FUSED):
+    """ll_layer_prefill (ll_layer_prefill_mode for another mode).  Returns y (BF16
+    [batch*seq_len, hidden])."""
     T = int(batch) * int(seq_len)
     _need(x, "x", torch.bfloat16, shape=(T, cfg.hidden))
     _need(positions, "positions", torch.int32, shape=(T,))
@@ -239,19 +279,23 @@ def layer_prefill(cfg, packed, x, positions, batch, seq_len, k_pool, v_pool, blo
     if y is None:
         y = torch.empty_like(x)
     if workspace is None:
-        workspace = new_workspace(cfg, T, block_table.shape[1], x.device)
+        workspace = new_workspace(cfg, T, block_table.shape[1], x.device, mode)
     if status is None:
         status = new_status(x.device)
-    _check("ll_layer_prefill", lib.ll_layer_prefill(
-        ctypes.byref(cfg), _ptr(packed), _ptr(x), _ptr(positions), int(batch), int(seq_len),
-        ctypes.byref(pool), _ptr(block_table), block_table.shape[1], _ptr(y), _ptr(workspace),
-        workspace.numel(), _ptr(status), _stream(stream)))
+    args = (ctypes.byref(cfg), _ptr(packed), _ptr(x), _ptr(positions), int(batch), int(seq_len),
+            ctypes.byref(pool), _ptr(block_table), block_table.shape[1], _ptr(y), _ptr(workspace),
+            workspace.numel(), _ptr(status))
+    if mode == LL_MODE_FUSED:
+        _check("ll_layer_prefill", lib.ll_layer_prefill(*args, _stream(stream)))
+    else:
+        _check("ll_layer_prefill_mode", lib.ll_layer_prefill_mode(*args, int(mode), _stream(stream)))
     return y
 
 
 def layer_decode_step(cfg, packed, x, k_pool, v_pool, block_table, context_lens, y=None,
-                      workspace=None, status=None, stream=None):
-    """ll_layer_decode_step.  Returns y (BF16 [batch, hidden])."""
+                      workspace=None, status=None, stream=None, mode=LL_MODE_FUSED):
+    """ll_layer_decode_step (ll_layer_decode_step_mode for another mode).  Returns y (BF16
+    [batch, hidden])."""
     B = x.shape[0]
     _need(x, "x", torch.bfloat16, shape=(B, cfg.hidden))
     _need(context_lens, "context_lens", torch.int32, shape=(B,))
@@ -262,13 +306,16 @@ def layer_decode_step(cfg, packed, x, k_pool, v_pool, block_table, context_lens,
     if y is None:
         y = torch.empty_like(x)
     if workspace is None:
-        workspace = new_workspace(cfg, B, block_table.shape[1], x.device)
+        workspace = new_workspace(cfg, B, block_table.shape[1], x.device, mode)
     if status is None:
         status = new_status(x.device)
-    _check("ll_layer_decode_step", lib.ll_layer_decode_step(
-        ctypes.byref(cfg), _ptr(packed), _ptr(x), ctypes.byref(pool), _ptr(block_table),
-        block_table.shape[1], _ptr(context_lens), B, _ptr(y), _ptr(workspace), workspace.numel(),
-        _ptr(status), _stream(stream)))
+    args = (ctypes.byref(cfg), _ptr(packed), _ptr(x), ctypes.byref(pool), _ptr(block_table),
+            block_table.shape[1], _ptr(context_lens), B, _ptr(y), _ptr(workspace), workspace.numel(),
+            _ptr(status))
+    if mode == LL_MODE_FUSED:
+        _check("ll_layer_decode_step", lib.ll_layer_decode_step(*args, _stream(stream)))
+    else:
+        _check("ll_layer_decode_step_mode", lib.ll_layer_decode_step_mode(*args, int(mode), _stream(stream)))
     return y
 
 

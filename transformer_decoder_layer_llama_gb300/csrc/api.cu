@@ -101,14 +101,17 @@ Packed packed_view(const ll_config* c, const void* base) {
     return p;
 }
 
-// Workspace of a layer call over T tokens with block tables max_blocks wide.
+// Workspace of a layer call over T tokens with block tables max_blocks wide.  The
+// step-by-step mode appends its float32 Linear outputs and the slot mapping; its K and V
+// after RoPE take the INT8 staging rows.
 struct WsLayout {
     size_t xh, q, o, h, hh, a, kst, vst, partials, counters, attn, total;
+    size_t qkv, slots, o_proj, gate_up, down;   // step-by-step only (0 otherwise)
     size_t partial_bytes;
     int counter_words;       // per GEMM
 };
 
-WsLayout ws_layout(const ll_config* c, int T, int max_blocks) {
+WsLayout ws_layout(const ll_config* c, int T, int max_blocks, int mode = LL_MODE_FUSED) {
     WsLayout L{};
     const size_t H = c->hidden, I = c->intermediate;
     const size_t nq = (size_t)c->n_heads * c->head_dim;
@@ -132,9 +135,18 @@ WsLayout ws_layout(const ll_config* c, int T, int max_blocks) {
     L.attn = at;
     at = align_up(at + ll::attn_decode_scratch_bytes(T, c->n_heads, c->head_dim, max_blocks,
                                                      c->block_size));
+    if (mode == LL_MODE_STEP_BY_STEP) {
+        L.qkv = at;     at = align_up(at + (size_t)T * nqkv * 4);
+        L.slots = at;   at = align_up(at + (size_t)T * 4);
+        L.o_proj = at;  at = align_up(at + (size_t)T * H * 4);
+        L.gate_up = at; at = align_up(at + (size_t)T * 2 * I * 4);
+        L.down = at;    at = align_up(at + (size_t)T * H * 4);
+    }
     L.total = at;
     return L;
 }
+
+bool mode_ok(int mode) { return mode == LL_MODE_FUSED || mode == LL_MODE_STEP_BY_STEP; }
 
 int cuda_rc(cudaError_t e) { return e == cudaSuccess ? LL_OK : LL_ERR_CUDA; }
 
@@ -318,6 +330,125 @@ int run_layer(const ll_config* cfg, const void* packed, const void* x, const int
     gd.ep.resid_f32 = h;
     gd.ep.status = status;
     if ((e = ll::launch_gemm(gd, stream)) != cudaSuccess) return LL_ERR_CUDA;
+    return LL_OK;
+}
+
+// The same chain with every operator its own kernel and every intermediate kept in the
+// workspace: RMSNorm -> QKV Linear (float32 out) -> RotaryEmbedding -> slot mapping ->
+// ReshapeAndCache -> attention -> O Linear -> residual add -> RMSNorm -> gate/up Linear ->
+// SiLU * up -> down Linear -> residual add.
+int run_layer_step_by_step(const ll_config* cfg, const void* packed, const void* x, const int32_t* positions,
+                           const int32_t* context_lens, int T, int seq_len, int batch, const ll_kv_pool* pool,
+                           const int32_t* block_table, int max_blocks, void* y, void* workspace,
+                           size_t workspace_bytes, int32_t* status, cudaStream_t stream, bool decode) {
+    WsLayout L = ws_layout(cfg, T, max_blocks, LL_MODE_STEP_BY_STEP);
+    if (!workspace || workspace_bytes < L.total || !aligned16(workspace)) return LL_ERR_WORKSPACE;
+    Packed P = packed_view(cfg, packed);
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    auto* xh = reinterpret_cast<__nv_bfloat16*>(ws + L.xh);
+    auto* q = reinterpret_cast<__nv_bfloat16*>(ws + L.q);
+    auto* o = reinterpret_cast<__nv_bfloat16*>(ws + L.o);
+    auto* h = reinterpret_cast<float*>(ws + L.h);
+    auto* hh = reinterpret_cast<__nv_bfloat16*>(ws + L.hh);
+    auto* a = reinterpret_cast<__nv_bfloat16*>(ws + L.a);
+    auto* k_rot = reinterpret_cast<__nv_bfloat16*>(ws + L.kst);
+    auto* v_new = reinterpret_cast<__nv_bfloat16*>(ws + L.vst);
+    auto* qkv = reinterpret_cast<float*>(ws + L.qkv);
+    auto* slots = reinterpret_cast<int32_t*>(ws + L.slots);
+    auto* o_proj = reinterpret_cast<float*>(ws + L.o_proj);
+    auto* gate_up = reinterpret_cast<float*>(ws + L.gate_up);
+    auto* down = reinterpret_cast<float*>(ws + L.down);
+    auto* counters = reinterpret_cast<int32_t*>(ws + L.counters);
+    const auto* xb = static_cast<const __nv_bfloat16*>(x);
+    const int H = cfg->hidden, I = cfg->intermediate, d = cfg->head_dim;
+    const int nq = cfg->n_heads * d;
+    const int nqkv = (cfg->n_heads + 2 * cfg->n_kv_heads) * d;
+    const int32_t* pos = decode ? nullptr : positions;
+    const int32_t* ctx = decode ? context_lens : nullptr;
+
+    if (ll::launch_rmsnorm(xb, P.g_attn, xh, T, H, cfg->rms_eps, counters, 4 * L.counter_words, stream) !=
+        cudaSuccess)
+        return LL_ERR_CUDA;
+    // a plain Linear: float32 output [T][n]
+    auto linear = [&](const __nv_bfloat16* act, const __nv_bfloat16* w, int n, int k, float* out, int slot) {
+        GemmProblem g{};
+        g.w_static = true;
+        g.partials = reinterpret_cast<float*>(ws + L.partials);
+        g.partial_bytes = L.partial_bytes;
+        g.counters = counters + slot * L.counter_words;
+        g.counter_cap = L.counter_words;
+        g.act = act;
+        g.w = w;
+        g.tokens = T;
+        g.n = n;
+        g.k = k;
+        g.ep.kind = ll::EPI_STORE;
+        g.ep.out_f32 = out;
+        g.ep.ld_out = n;
+        g.ep.status = status;
+        return ll::launch_gemm(g, stream);
+    };
+    if (linear(xh, P.qkv, nqkv, H, qkv, 0) != cudaSuccess) return LL_ERR_CUDA;
+    if (ll::launch_rope_split(qkv, pos, ctx, seq_len, T, cfg->n_heads, cfg->n_kv_heads, d, cfg->max_position,
+                              P.rope, q, k_rot, v_new, status, stream) != cudaSuccess)
+        return LL_ERR_CUDA;
+    if (ll::launch_slot_mapping(pos, ctx, seq_len, T, block_table, max_blocks, cfg->block_size, pool->num_blocks,
+                                cfg->max_position, slots, status, stream) != cudaSuccess)
+        return LL_ERR_CUDA;
+    if (ll::launch_reshape_and_cache(k_rot, v_new, slots, T, cfg->n_kv_heads, d, cfg->block_size,
+                                     static_cast<__nv_bfloat16*>(pool->k), static_cast<__nv_bfloat16*>(pool->v),
+                                     pool->num_blocks, status, stream) != cudaSuccess)
+        return LL_ERR_CUDA;
+    const float scale = 1.0f / std::sqrt((float)d);
+    if (!decode) {
+        ll::AttnPrefillArgs at{};
+        at.q = q;
+        at.k_pool = static_cast<const __nv_bfloat16*>(pool->k);
+        at.v_pool = static_cast<const __nv_bfloat16*>(pool->v);
+        at.positions = positions;
+        at.block_table = block_table;
+        at.max_blocks = max_blocks;
+        at.num_blocks = pool->num_blocks;
+        at.block_size = cfg->block_size;
+        at.batch = batch;
+        at.seq_len = seq_len;
+        at.n_heads = cfg->n_heads;
+        at.n_kv_heads = cfg->n_kv_heads;
+        at.head_dim = d;
+        at.scale = scale;
+        at.out = o;
+        at.status = status;
+        if (ll::launch_attn_prefill_tc(at, stream) != cudaSuccess) return LL_ERR_CUDA;
+    } else {
+        ll::AttnDecodeArgs at{};
+        at.q = q;
+        at.k_pool = static_cast<const __nv_bfloat16*>(pool->k);
+        at.v_pool = static_cast<const __nv_bfloat16*>(pool->v);
+        at.context_lens = context_lens;
+        at.block_table = block_table;
+        at.max_blocks = max_blocks;
+        at.num_blocks = pool->num_blocks;
+        at.block_size = cfg->block_size;
+        at.batch = batch;
+        at.n_heads = cfg->n_heads;
+        at.n_kv_heads = cfg->n_kv_heads;
+        at.head_dim = d;
+        at.scale = scale;
+        at.out = o;
+        const size_t rows = (size_t)batch * cfg->n_heads * ll::attn_decode_max_splits(max_blocks, cfg->block_size);
+        at.part_o = reinterpret_cast<float*>(ws + L.attn);
+        at.part_ml = at.part_o + rows * d;
+        at.status = status;
+        if (ll::launch_attn_decode(at, stream) != cudaSuccess) return LL_ERR_CUDA;
+    }
+    if (linear(o, P.o, H, nq, o_proj, 1) != cudaSuccess) return LL_ERR_CUDA;
+    if (ll::launch_residual_add(xb, o_proj, h, (long long)T * H, stream) != cudaSuccess) return LL_ERR_CUDA;
+    if (ll::launch_rmsnorm_f32(h, P.g_ffn, hh, T, H, cfg->rms_eps, stream) != cudaSuccess) return LL_ERR_CUDA;
+    if (linear(hh, P.gu, 2 * I, H, gate_up, 2) != cudaSuccess) return LL_ERR_CUDA;
+    if (ll::launch_swiglu(gate_up, a, T, I, stream) != cudaSuccess) return LL_ERR_CUDA;
+    if (linear(a, P.down, H, I, down, 3) != cudaSuccess) return LL_ERR_CUDA;
+    if (ll::launch_residual_add(h, down, static_cast<__nv_bfloat16*>(y), (long long)T * H, stream) != cudaSuccess)
+        return LL_ERR_CUDA;
     return LL_OK;
 }
 
@@ -690,6 +821,68 @@ int ll_workspace_checkpoints(const ll_config* cfg, int32_t max_tokens, int32_t m
     out->h_hat = L.hh;
     out->a = L.a;
     return LL_OK;
+}
+
+size_t ll_workspace_size_mode(const ll_config* cfg, int32_t max_tokens, int32_t max_blocks, int32_t mode) {
+    if (config_supported(cfg) != LL_OK || max_tokens <= 0 || max_blocks <= 0 || !mode_ok(mode)) return 0;
+    return ws_layout(cfg, max_tokens, max_blocks, mode).total;
+}
+
+int ll_workspace_step_checkpoints(const ll_config* cfg, int32_t max_tokens, int32_t max_blocks,
+                                  ll_step_checkpoints* out) {
+    ll::clear_last_error();
+    if (!out || max_tokens <= 0 || max_blocks <= 0) return LL_ERR_INVALID_ARG;
+    const int rc = config_supported(cfg);
+    if (rc != LL_OK) return rc;
+    const WsLayout L = ws_layout(cfg, max_tokens, max_blocks, LL_MODE_STEP_BY_STEP);
+    out->qkv = L.qkv;
+    out->k = L.kst;
+    out->v = L.vst;
+    out->slots = L.slots;
+    out->o_proj = L.o_proj;
+    out->gate_up = L.gate_up;
+    out->down = L.down;
+    return LL_OK;
+}
+
+int ll_layer_prefill_mode(const ll_config* cfg, const void* packed, const void* x, const int32_t* positions,
+                          int32_t batch, int32_t seq_len, const ll_kv_pool* pool, const int32_t* block_table,
+                          int32_t max_blocks, void* y, void* workspace, size_t workspace_bytes, int32_t* status,
+                          int32_t mode, void* stream) {
+    if (!mode_ok(mode)) return LL_ERR_INVALID_ARG;
+    if (mode == LL_MODE_FUSED)
+        return ll_layer_prefill(cfg, packed, x, positions, batch, seq_len, pool, block_table, max_blocks, y,
+                                workspace, workspace_bytes, status, stream);
+    ll::clear_last_error();
+    int rc = config_supported(cfg);
+    if (rc != LL_OK) return rc;
+    if (!packed || !x || !positions || !block_table || !y || !status || !pool_ok(pool)) return LL_ERR_INVALID_ARG;
+    if (batch <= 0 || seq_len <= 0 || max_blocks <= 0 || x == y) return LL_ERR_INVALID_ARG;
+    if (!aligned16(packed) || !aligned16(x) || !aligned16(y)) return LL_ERR_INVALID_ARG;
+    if ((long long)batch * seq_len > (1 << 24)) return LL_ERR_UNSUPPORTED;
+    return run_layer_step_by_step(cfg, packed, x, positions, nullptr, batch * seq_len, seq_len, batch, pool,
+                                  block_table, max_blocks, y, workspace, workspace_bytes, status,
+                                  static_cast<cudaStream_t>(stream), false);
+}
+
+int ll_layer_decode_step_mode(const ll_config* cfg, const void* packed, const void* x, const ll_kv_pool* pool,
+                              const int32_t* block_table, int32_t max_blocks, const int32_t* context_lens,
+                              int32_t batch, void* y, void* workspace, size_t workspace_bytes, int32_t* status,
+                              int32_t mode, void* stream) {
+    if (!mode_ok(mode)) return LL_ERR_INVALID_ARG;
+    if (mode == LL_MODE_FUSED)
+        return ll_layer_decode_step(cfg, packed, x, pool, block_table, max_blocks, context_lens, batch, y, workspace,
+                                    workspace_bytes, status, stream);
+    ll::clear_last_error();
+    int rc = config_supported(cfg);
+    if (rc != LL_OK) return rc;
+    if (!packed || !x || !context_lens || !block_table || !y || !status || !pool_ok(pool))
+        return LL_ERR_INVALID_ARG;
+    if (batch <= 0 || max_blocks <= 0 || x == y) return LL_ERR_INVALID_ARG;
+    if (!aligned16(packed) || !aligned16(x) || !aligned16(y)) return LL_ERR_INVALID_ARG;
+    return run_layer_step_by_step(cfg, packed, x, nullptr, context_lens, batch, 1, batch, pool, block_table,
+                                  max_blocks, y, workspace, workspace_bytes, status, static_cast<cudaStream_t>(stream),
+                                  true);
 }
 
 size_t ll_linear_workspace_size(int32_t m, int32_t n, int32_t k) {

@@ -39,6 +39,19 @@ LL_DEVINL float ex2_approx(float x) {
     return y;
 }
 
+// The element-wise steps of the chain, written once so that the fused epilogues and the
+// step-by-step kernels compute bit-identical values from the same inputs.
+// RoPE of one half-split pair: (x, y) = head elements (i, i + d/2), (c, s) = (cos, sin)
+// of its angle; returns the rotated (i, i + d/2).
+LL_DEVINL float2 rope_rotate(float x, float y, float c, float s) {
+    return make_float2(__fmaf_rn(x, c, -__fmul_rn(y, s)), __fmaf_rn(y, c, __fmul_rn(x, s)));
+}
+
+// SiLU(gate) * up, silu(z) = z / (1 + e^-z).
+LL_DEVINL float silu_mul(float gate, float up) {
+    return __fmul_rn(__fdiv_rn(gate, 1.0f + expf(-gate)), up);
+}
+
 // log2(x) by the SFU instruction (approximate; lg2(0) = -inf).
 LL_DEVINL float lg2_approx(float x) {
     float y;

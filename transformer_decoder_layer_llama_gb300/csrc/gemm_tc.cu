@@ -63,8 +63,6 @@ struct GemmArgs {
     float* partials;         // weight form: [CTAs][2][tokens][128] float32 partial tiles
 };
 
-LL_DEVINL float silu_f(float z) { return z / (1.0f + expf(-z)); }
-
 struct TokenSlot {
     int pos;         // -1 if invalid
     long long kv_row;  // row index (blk * Hkv) * bs + off of head 0, or -1
@@ -104,6 +102,12 @@ LL_DEVINL void epi_token_chunk(const EpiParams& ep, int t, bool row_ok, int n0, 
     if (!row_ok) return;
     switch (ep.kind) {
         case EPI_STORE: {
+            if (ep.out_f32) {
+                float4* dst = reinterpret_cast<float4*>(ep.out_f32 + (size_t)t * ep.ld_out + n0);
+#pragma unroll
+                for (int j = 0; j < 4; ++j) dst[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+                break;
+            }
             uint4 o0, o1;
             o0.x = pack_bf16x2(v[0], v[1]);   o0.y = pack_bf16x2(v[2], v[3]);
             o0.z = pack_bf16x2(v[4], v[5]);   o0.w = pack_bf16x2(v[6], v[7]);
@@ -152,7 +156,7 @@ LL_DEVINL void epi_token_chunk(const EpiParams& ep, int t, bool row_ok, int n0, 
         case EPI_SWIGLU: {
             float a[8];
 #pragma unroll
-            for (int j = 0; j < 8; ++j) a[j] = silu_f(v[2 * j]) * v[2 * j + 1];
+            for (int j = 0; j < 8; ++j) a[j] = silu_mul(v[2 * j], v[2 * j + 1]);
             uint4 o;
             o.x = pack_bf16x2(a[0], a[1]); o.y = pack_bf16x2(a[2], a[3]);
             o.z = pack_bf16x2(a[4], a[5]); o.w = pack_bf16x2(a[6], a[7]);
@@ -194,10 +198,12 @@ LL_DEVINL void epi_token_chunk(const EpiParams& ep, int t, bool row_ok, int n0, 
                 for (int jj = 0; jj < 4; ++jj) {
                     float4 c = cs4[jj];   // (cos, sin) of pairs i0+2jj and i0+2jj+1
                     int j = 2 * jj;
-                    lo[j] = v[2 * j] * c.x - v[2 * j + 1] * c.y;
-                    hi[j] = v[2 * j + 1] * c.x + v[2 * j] * c.y;
-                    lo[j + 1] = v[2 * j + 2] * c.z - v[2 * j + 3] * c.w;
-                    hi[j + 1] = v[2 * j + 3] * c.z + v[2 * j + 2] * c.w;
+                    const float2 r0 = rope_rotate(v[2 * j], v[2 * j + 1], c.x, c.y);
+                    const float2 r1 = rope_rotate(v[2 * j + 2], v[2 * j + 3], c.z, c.w);
+                    lo[j] = r0.x;
+                    hi[j] = r0.y;
+                    lo[j + 1] = r1.x;
+                    hi[j + 1] = r1.y;
                 }
                 uint4 a, b;
                 a.x = pack_bf16x2(lo[0], lo[1]); a.y = pack_bf16x2(lo[2], lo[3]);
@@ -230,7 +236,12 @@ LL_DEVINL void epi_weight_chunk(const EpiParams& ep, int n, int N, int t0, int T
             if (n_ok)
 #pragma unroll
                 for (int j = 0; j < 16; ++j)
-                    if (t0 + j < T) ep.out[(size_t)(t0 + j) * ep.ld_out + n] = __float2bfloat16_rn(v[j]);
+                    if (t0 + j < T) {
+                        if (ep.out_f32)
+                            ep.out_f32[(size_t)(t0 + j) * ep.ld_out + n] = v[j];
+                        else
+                            ep.out[(size_t)(t0 + j) * ep.ld_out + n] = __float2bfloat16_rn(v[j]);
+                    }
             break;
         case EPI_RESID:
             if (n_ok) {
@@ -279,7 +290,7 @@ LL_DEVINL void epi_weight_chunk(const EpiParams& ep, int n, int N, int t0, int T
                 float other = __shfl_xor_sync(0xffffffffu, v[j], 1);
                 if (n_ok && (n & 1) == 0 && t0 + j < T)
                     ep.out[(size_t)(t0 + j) * ep.ld_out + (n >> 1)] =
-                        __float2bfloat16_rn(silu_f(v[j]) * other);
+                        __float2bfloat16_rn(silu_mul(v[j], other));
             }
             break;
         case EPI_QKV: {
@@ -319,8 +330,9 @@ LL_DEVINL void epi_weight_chunk(const EpiParams& ep, int n, int N, int t0, int T
                 if (pj[j] < 0) continue;
                 float val = v[j];
                 if (sec != 2) {
+                    // lane pair (even, odd) = head elements (i, i + d/2)
                     const float2 cs = csj[j];
-                    val = (e & 1) ? (v[j] * cs.x + other[j] * cs.y) : (v[j] * cs.x - other[j] * cs.y);
+                    val = (e & 1) ? rope_rotate(other[j], v[j], cs.x, cs.y).y : rope_rotate(v[j], other[j], cs.x, cs.y).x;
                 }
                 const __nv_bfloat16 bv = __float2bfloat16_rn(val);
                 if (sec == 0) {

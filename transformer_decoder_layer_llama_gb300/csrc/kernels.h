@@ -39,7 +39,7 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
 }
 
 enum EpiKind : int {
-    EPI_STORE = 0,   // out = acc
+    EPI_STORE = 0,   // out = acc (BF16 `out`, or float32 `out_f32`)
     EPI_RESID = 1,   // out = resid + acc (O projection, down projection); resid and out may be fp32
     EPI_SWIGLU = 2,  // out[j] = silu(acc[2j]) * acc[2j+1] (merged gate/up, rows interleaved)
     EPI_QKV = 3,     // RoPE on Q/K, Q -> q_out, K/V -> paged pool (merged QKV)
@@ -51,7 +51,7 @@ struct EpiParams {
     int ld_out;
     const __nv_bfloat16* resid;    // RESID: [tokens, n] BF16 residual, or
     const float* resid_f32;        //        [tokens, n] float32 residual (one of the two)
-    float* out_f32;                // RESID: float32 destination [tokens, n] instead of `out`
+    float* out_f32;                // STORE / RESID: float32 destination instead of `out`
     // EPI_QKV
     __nv_bfloat16* q_out;          // [tokens, n_heads * head_dim]
     __nv_bfloat16* k_pool;         // the paged pool, or with kv_stage a staging buffer
@@ -183,6 +183,25 @@ size_t attn_decode_scratch_bytes(int batch, int n_heads, int head_dim, int max_b
 cudaError_t launch_attn_decode(const AttnDecodeArgs& a, cudaStream_t stream);
 // Decode attention over an INT8 pool (k_q8/v_q8 + scales; head_dim 128).
 cudaError_t launch_attn_decode_q8(const AttnDecodeArgs& a, cudaStream_t stream);
+
+// Step-by-step operators (each one kernel; arithmetic as in the fused epilogues).
+// RotaryEmbedding of the merged QKV Linear output (float32, packed column order) into
+// q, k (rotated) and v, BF16 [tokens][heads * head_dim] in element order.
+cudaError_t launch_rope_split(const float* qkv, const int32_t* positions, const int32_t* context_lens, int seq_len,
+                              int tokens, int n_heads, int n_kv_heads, int head_dim, int max_position,
+                              const float2* rope_cs, __nv_bfloat16* q, __nv_bfloat16* k, __nv_bfloat16* v,
+                              int32_t* status, cudaStream_t stream);
+// Cache slot of each token from its position and the block table (-1 where invalid).
+cudaError_t launch_slot_mapping(const int32_t* positions, const int32_t* context_lens, int seq_len, int tokens,
+                                const int32_t* block_table, int max_blocks, int block_size, int num_blocks,
+                                int max_position, int32_t* slots, int32_t* status, cudaStream_t stream);
+// a = bf16(silu(gate) * up) from the merged gate/up Linear output (float32, interleaved).
+cudaError_t launch_swiglu(const float* gate_up, __nv_bfloat16* a, int tokens, int intermediate, cudaStream_t stream);
+// out = resid + acc (float32 add) over n elements.
+cudaError_t launch_residual_add(const __nv_bfloat16* resid, const float* acc, float* out, long long n,
+                                cudaStream_t stream);
+cudaError_t launch_residual_add(const float* resid, const float* acc, __nv_bfloat16* out, long long n,
+                                cudaStream_t stream);
 
 // Weight packing helpers.
 cudaError_t launch_pack_rows(const __nv_bfloat16* src, __nv_bfloat16* dst, int rows, int cols,

@@ -303,9 +303,159 @@ __global__ void bounded_wait_selftest_kernel(int32_t* status, int32_t* out, uint
     if (!done) atomicAdd(out, 1);
 }
 
+// ---------------------------------------------------------------- step-by-step operators
+// The element-wise operators of the chain as kernels of their own, for the step-by-step
+// execution mode (page "ATB fused-operator matrix and KV-cache management", section on
+// the engineering limits of fusion granularity).  Their arithmetic is the fused
+// epilogues' (rope_rotate, silu_mul, float32 residual adds), so both modes compute the
+// same values from the same Linear outputs.
+
+// A token's position: positions[t], or context_lens[t / seq_len] - 1 when positions is null.
+LL_DEVINL int token_position(const int32_t* positions, const int32_t* context_lens, int seq_len, int t) {
+    return positions ? positions[t] : context_lens[t / seq_len] - 1;
+}
+
+// RotaryEmbedding on the merged QKV Linear output (float32 [tokens][nqkv], the packed
+// column order: for Q and K heads column 2i holds element i and 2i + 1 element i + d/2,
+// V heads in element order).  One thread per (token, head, pair); writes q and k rotated
+// and v, each BF16 in element order ([tokens][heads * d]).  A token whose position is
+// outside the RoPE table is flagged and skipped, as in the fused epilogue.
+__global__ void rope_split_kernel(const float* __restrict__ qkv, const int32_t* __restrict__ positions,
+                                  const int32_t* __restrict__ context_lens, int seq_len, int tokens, int n_heads,
+                                  int n_kv_heads, int head_dim, int max_position, const float2* __restrict__ rope_cs,
+                                  __nv_bfloat16* __restrict__ q, __nv_bfloat16* __restrict__ k,
+                                  __nv_bfloat16* __restrict__ v, int32_t* status) {
+    const int half = head_dim >> 1;
+    const int heads = n_heads + 2 * n_kv_heads;
+    const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    if (idx >= (long long)tokens * heads * half) return;
+    const int t = (int)(idx / ((long long)heads * half));
+    const int rem = (int)(idx - (long long)t * heads * half);
+    const int head = rem / half, i = rem - head * half;
+    const int pos = token_position(positions, context_lens, seq_len, t);
+    if (pos < 0 || pos >= max_position) {
+        if (head == 0 && i == 0) flag_status(status, LL_DEV_BAD_POSITION);
+        return;
+    }
+    const float* row = qkv + (size_t)t * heads * head_dim + (size_t)head * head_dim;
+    if (head >= n_heads + n_kv_heads) {           // V: two elements, unrotated
+        const int hv = head - n_heads - n_kv_heads;
+        __nv_bfloat16* dst = v + ((size_t)t * n_kv_heads + hv) * head_dim;
+        dst[2 * i] = __float2bfloat16_rn(row[2 * i]);
+        dst[2 * i + 1] = __float2bfloat16_rn(row[2 * i + 1]);
+        return;
+    }
+    const float2 cs = rope_cs[(size_t)pos * half + i];
+    const float2 r = rope_rotate(row[2 * i], row[2 * i + 1], cs.x, cs.y);
+    __nv_bfloat16* dst = head < n_heads ? q + ((size_t)t * n_heads + head) * head_dim
+                                        : k + ((size_t)t * n_kv_heads + (head - n_heads)) * head_dim;
+    dst[i] = __float2bfloat16_rn(r.x);
+    dst[i + half] = __float2bfloat16_rn(r.y);
+}
+
+// The cache slot of each token: block_table[seq][pos / block_size] * block_size + pos %
+// block_size; -1 (and a status bit) where the position or its block is out of range.
+__global__ void slot_mapping_kernel(const int32_t* __restrict__ positions, const int32_t* __restrict__ context_lens,
+                                    int seq_len, int tokens, const int32_t* __restrict__ block_table, int max_blocks,
+                                    int block_size, int num_blocks, int max_position, int32_t* __restrict__ slots,
+                                    int32_t* status) {
+    const int t = blockIdx.x * blockDim.x + threadIdx.x;
+    if (t >= tokens) return;
+    const int pos = token_position(positions, context_lens, seq_len, t);
+    int slot = -1;
+    if (pos < 0 || pos >= max_position) {
+        flag_status(status, LL_DEV_BAD_POSITION);
+    } else if (pos / block_size >= max_blocks) {
+        flag_status(status, LL_DEV_BAD_BLOCK);
+    } else {
+        const int blk = block_table[(size_t)(t / seq_len) * max_blocks + pos / block_size];
+        if (blk < 0 || blk >= num_blocks)
+            flag_status(status, LL_DEV_BAD_BLOCK);
+        else
+            slot = blk * block_size + pos % block_size;
+    }
+    slots[t] = slot;
+}
+
+// a[t][j] = bf16(silu(gu[t][2j]) * gu[t][2j + 1]) from the merged gate/up Linear output
+// (float32, gate and up columns interleaved).
+__global__ void swiglu_kernel(const float2* __restrict__ gu, __nv_bfloat16* __restrict__ a, long long n) {
+    const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    if (idx >= n) return;
+    const float2 p = gu[idx];
+    a[idx] = __float2bfloat16_rn(silu_mul(p.x, p.y));
+}
+
+// out = resid + acc elementwise (float32 add), resid BF16 or float32, out float32 or BF16.
+template <typename In, typename Out>
+__global__ void residual_add_kernel(const In* __restrict__ resid, const float* __restrict__ acc,
+                                    Out* __restrict__ out, long long n) {
+    const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    if (idx >= n) return;
+    const float r = static_cast<float>(resid[idx]);
+    const float s = r + acc[idx];
+    if constexpr (sizeof(Out) == 4)
+        out[idx] = s;
+    else
+        out[idx] = __float2bfloat16_rn(s);
+}
+
 unsigned blocks_for(long long n, int threads) { return (unsigned)((n + threads - 1) / threads); }
 
 }  // namespace
+
+cudaError_t launch_rope_split(const float* qkv, const int32_t* positions, const int32_t* context_lens, int seq_len,
+                              int tokens, int n_heads, int n_kv_heads, int head_dim, int max_position,
+                              const float2* rope_cs, __nv_bfloat16* q, __nv_bfloat16* k, __nv_bfloat16* v,
+                              int32_t* status, cudaStream_t stream) {
+    if (tokens <= 0) return cudaSuccess;
+    const long long n = (long long)tokens * (n_heads + 2 * n_kv_heads) * (head_dim / 2);
+    trace_before("rope", stream);
+    rope_split_kernel<<<blocks_for(n, 256), 256, 0, stream>>>(qkv, positions, context_lens, seq_len, tokens, n_heads,
+                                                               n_kv_heads, head_dim, max_position, rope_cs, q, k, v,
+                                                               status);
+    trace_after(stream);
+    return record(cudaGetLastError(), "rope_split launch");
+}
+
+cudaError_t launch_slot_mapping(const int32_t* positions, const int32_t* context_lens, int seq_len, int tokens,
+                                const int32_t* block_table, int max_blocks, int block_size, int num_blocks,
+                                int max_position, int32_t* slots, int32_t* status, cudaStream_t stream) {
+    if (tokens <= 0) return cudaSuccess;
+    trace_before("slot_mapping", stream);
+    slot_mapping_kernel<<<blocks_for(tokens, 256), 256, 0, stream>>>(positions, context_lens, seq_len, tokens,
+                                                                      block_table, max_blocks, block_size, num_blocks,
+                                                                      max_position, slots, status);
+    trace_after(stream);
+    return record(cudaGetLastError(), "slot_mapping launch");
+}
+
+cudaError_t launch_swiglu(const float* gate_up, __nv_bfloat16* a, int tokens, int intermediate, cudaStream_t stream) {
+    const long long n = (long long)tokens * intermediate;
+    if (n <= 0) return cudaSuccess;
+    trace_before("swiglu", stream);
+    swiglu_kernel<<<blocks_for(n, 256), 256, 0, stream>>>(reinterpret_cast<const float2*>(gate_up), a, n);
+    trace_after(stream);
+    return record(cudaGetLastError(), "swiglu launch");
+}
+
+cudaError_t launch_residual_add(const __nv_bfloat16* resid, const float* acc, float* out, long long n,
+                                cudaStream_t stream) {
+    if (n <= 0) return cudaSuccess;
+    trace_before("residual_add", stream);
+    residual_add_kernel<__nv_bfloat16, float><<<blocks_for(n, 256), 256, 0, stream>>>(resid, acc, out, n);
+    trace_after(stream);
+    return record(cudaGetLastError(), "residual_add launch");
+}
+
+cudaError_t launch_residual_add(const float* resid, const float* acc, __nv_bfloat16* out, long long n,
+                                cudaStream_t stream) {
+    if (n <= 0) return cudaSuccess;
+    trace_before("residual_add", stream);
+    residual_add_kernel<float, __nv_bfloat16><<<blocks_for(n, 256), 256, 0, stream>>>(resid, acc, out, n);
+    trace_after(stream);
+    return record(cudaGetLastError(), "residual_add launch");
+}
 
 cudaError_t launch_rmsnorm(const __nv_bfloat16* x, const float* g, __nv_bfloat16* out, int tokens,
                            int hidden, float eps, int32_t* zero_ptr, int zero_words,
