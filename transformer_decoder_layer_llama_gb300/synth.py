@@ -71,38 +71,44 @@ WORKLOADS = {
 }
 
 
-def _gen(seed: int, tag: str) -> torch.Generator:
-    """CPU generator of stream `tag` for a user seed.  Different tags give independent
-    streams for the same seed (the seed is hashed with the tag), so two tensors can never
-    be drawn from one stream by accident (e.g. an input equal to a scaled weight row)."""
-    g = torch.Generator()
+def _gen(seed: int, tag: str, device=None) -> torch.Generator:
+    """Generator of stream `tag` for a user seed (on the CPU, or on `device`).  Different
+    tags give independent streams for the same seed (the seed is hashed with the tag), so
+    two tensors can never be drawn from one stream by accident (e.g. an input equal to a
+    scaled weight row).  A device generator draws other numbers than the CPU one for the
+    same seed; each is reproducible on its own."""
+    g = torch.Generator(device=device) if device is not None else torch.Generator()
     g.manual_seed(zlib.crc32(f"{tag}:{int(seed)}".encode()) * 2654435761 % (1 << 63))
     return g
 
 
-def normal_bf16(shape, std: float, seed: int, tag: str = "normal") -> torch.Tensor:
-    """BF16 tensor of N(0, std^2) draws (drawn in fp32, rounded to nearest BF16)."""
-    t = torch.randn(*shape, generator=_gen(seed, tag), dtype=torch.float32)
+def normal_bf16(shape, std: float, seed: int, tag: str = "normal", device=None) -> torch.Tensor:
+    """BF16 tensor of N(0, std^2) draws (drawn in fp32, rounded to nearest BF16), on the
+    CPU or, with `device`, drawn there by its own generator (for large inputs)."""
+    t = torch.randn(*shape, generator=_gen(seed, tag, device), dtype=torch.float32,
+                    device=device if device is not None else "cpu")
     if std != 1.0:
         t.mul_(std)
     return t.to(BF16)
 
 
-def make_weights(d: LayerDims, w_std: float, seed: int) -> dict:
-    """Canonical layer weights, all `[out, in]` row-major.
+def make_weights(d: LayerDims, w_std: float, seed: int, device=None) -> dict:
+    """Canonical layer weights, all `[out, in]` row-major (drawn on `device` if given).
 
     w_qkv rows are [Q heads; K heads; V heads], each head `head_dim` rows.
     Gate and up are separate `[I, H]` matrices; w_down is `[H, I]`.
     """
     H, I = d.hidden, d.intermediate
+    dev = device if device is not None else "cpu"
+    gain = lambda tag: 1.0 + 0.1 * torch.randn(H, generator=_gen(seed, tag, device), dtype=torch.float32, device=dev)
     return {
-        "w_qkv": normal_bf16((d.qkv_rows, H), w_std, seed, "w_qkv"),
-        "w_o": normal_bf16((H, d.n_heads * d.head_dim), w_std, seed, "w_o"),
-        "w_gate": normal_bf16((I, H), w_std, seed, "w_gate"),
-        "w_up": normal_bf16((I, H), w_std, seed, "w_up"),
-        "w_down": normal_bf16((H, I), w_std, seed, "w_down"),
-        "g_attn": 1.0 + 0.1 * torch.randn(H, generator=_gen(seed, "g_attn"), dtype=torch.float32),
-        "g_ffn": 1.0 + 0.1 * torch.randn(H, generator=_gen(seed, "g_ffn"), dtype=torch.float32),
+        "w_qkv": normal_bf16((d.qkv_rows, H), w_std, seed, "w_qkv", device),
+        "w_o": normal_bf16((H, d.n_heads * d.head_dim), w_std, seed, "w_o", device),
+        "w_gate": normal_bf16((I, H), w_std, seed, "w_gate", device),
+        "w_up": normal_bf16((I, H), w_std, seed, "w_up", device),
+        "w_down": normal_bf16((H, I), w_std, seed, "w_down", device),
+        "g_attn": gain("g_attn"),
+        "g_ffn": gain("g_ffn"),
     }
 
 
@@ -139,15 +145,16 @@ def make_block_table(seq_tokens, block_size: int, seed: int, extra_blocks: int =
     return table, num_blocks
 
 
-def make_pool(num_blocks: int, d: LayerDims, seed: int, fill: str = "normal"):
+def make_pool(num_blocks: int, d: LayerDims, seed: int, fill: str = "normal", device=None):
     """(k_pool, v_pool), each BF16 `[num_blocks, n_kv_heads, block_size, head_dim]`.
 
-    fill="normal": N(0,1) draws (a pre-filled cache).  fill="sentinel": every
-    element is the BF16 value -1024.0, so untouched slots can be recognised.
+    fill="normal": N(0,1) draws (a pre-filled cache; drawn on `device` if given).
+    fill="sentinel": every element is the BF16 value -1024.0, so untouched slots can be
+    recognised.
     """
     shape = (num_blocks, d.n_kv_heads, d.block_size, d.head_dim)
     if fill == "normal":
-        return normal_bf16(shape, 1.0, seed, "k_pool"), normal_bf16(shape, 1.0, seed, "v_pool")
+        return normal_bf16(shape, 1.0, seed, "k_pool", device), normal_bf16(shape, 1.0, seed, "v_pool", device)
     if fill == "sentinel":
         return (torch.full(shape, -1024.0, dtype=BF16), torch.full(shape, -1024.0, dtype=BF16))
     raise ValueError(fill)
