@@ -348,15 +348,16 @@ LL_DEVINL void epi_weight_chunk(const EpiParams& ep, int n, int N, int t0, int T
 }
 
 // ---------------------------------------------------------------- token form
-// A cluster of two CTAs computes 256 x 256 output tiles with tcgen05.mma.cta_group::2:
-// CTA r stages rows [128 r, 128 r + 128) of the tile's A block and rows
-// [128 r, 128 r + 128) of its B block (256 output columns), the even CTA issues the
-// pair's MMAs, and each CTA's TMEM receives its 128 output rows.  Per k-block each
-// CTA moves 32 KB (not 48 KB) for the same MMA work, which relieves shared memory.
-// Both CTAs' TMA loads complete the even CTA's full barrier; the MMA commits
-// arrive on both CTAs' barriers (multicast); both CTAs' epilogue threads release
-// the even CTA's accumulator barrier.
-constexpr int kPairBN = 256;
+// A cluster of two CTAs computes 256 x bn output tiles (bn in [128, 256], chosen per
+// shape so that the tiles fill the last wave of pairs; see pair_tile_n) with
+// tcgen05.mma.cta_group::2: CTA r stages rows [128 r, 128 r + 128) of the tile's A
+// block and rows [bn/2 r, bn/2 (r + 1)) of its B block, the even CTA issues the pair's
+// MMAs, and each CTA's TMEM receives its 128 output rows.  Per k-block each CTA moves
+// 16 KB + bn/2 x 128 bytes (32 KB, not 48 KB, at bn = 256) for the same MMA work,
+// which relieves shared memory.  Both CTAs' TMA loads complete the even CTA's full
+// barrier; the MMA commits arrive on both CTAs' barriers (multicast); both CTAs'
+// epilogue threads release the even CTA's accumulator barrier.
+constexpr int kPairBN = 256;      // the widest tile; each of the two TMEM accumulators starts a multiple of it apart
 
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_token2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -375,7 +376,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool leader = rank == 0;
     const int pair = blockIdx.x >> 1, num_pairs = gridDim.x >> 1;
     int32_t* status = a.ep.status;
-    // a.tiles_m counts 256-row tiles here, a.bn = 256
+    // a.tiles_m counts 256-row tiles here; a tile has a.bn output columns
     if (threadIdx.x == 0) {
         for (int s = 0; s < a.stages; ++s) {
             mbar_init(&full_bar[s], 1);
@@ -404,7 +405,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     pdl_wait();
     pdl_trigger();
     const uint32_t tmem = tmem_base_s;
-    const uint32_t half_bytes = (uint32_t)BM * BK * 2;     // 16 KB: A rows or B rows of one CTA
+    const uint32_t half_bytes = (uint32_t)BM * BK * 2;     // 16 KB: this CTA's A rows (its B rows follow)
 
     if (warp == 0) {
         if (lane == 0) {
@@ -426,7 +427,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (leader) mbar_arrive_expect_tx(&full_bar[stage], 2u * a.stage_bytes);
                     const uint32_t fb = cluster_map(smem_u32(&full_bar[stage]), 0);
                     tma_load_2d_pair(sa, &tmA, kb * BK, m2 * 256 + (int)rank * BM, fb);
-                    tma_load_2d_pair(sb, &tmB, kb * BK, nb * kPairBN + (int)rank * BM, fb);
+                    tma_load_2d_pair(sb, &tmB, kb * BK, nb * a.bn + (int)rank * (a.bn >> 1), fb);
                     for (int s = 0; s < MAX_STAGES; ++s) issued[s] += (s == stage);
                     if (++stage == a.stages) {
                         stage = 0;
@@ -443,12 +444,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
     } else if (warp == 1) {
         if (lane == 0 && leader) {
-            const uint32_t idesc = umma_idesc_bf16(2 * BM, kPairBN);
+            const uint32_t idesc = umma_idesc_bf16(2 * BM, a.bn);
             int stage = 0;
             uint32_t phase = 0;
             int local = 0;
             bool ok = true;
-            const int nbuf = (int)(a.tmem_cols / kPairBN);
+            const int nbuf = (int)(a.tmem_cols / kPairBN);   // two accumulators, at column 0 and 256
             for (int u = pair; u < a.units && ok; u += num_pairs, ++local) {
                 const int buf = local % nbuf;
                 const uint32_t accp = (uint32_t)(local / nbuf) & 1;
@@ -498,8 +499,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const bool row_ok = t < a.tokens;
             TokenSlot ts{-1, -1};
             if (a.ep.kind == EPI_QKV && row_ok) ts = token_slot(a.ep, t);
-            for (int c = 0; c < kPairBN; c += 16) {
-                const int n0 = nb * kPairBN + c;
+            for (int c = 0; c < a.bn; c += 16) {
+                const int n0 = nb * a.bn + c;
                 if (n0 >= a.n) break;
                 float v[16];
                 tmem_ld16(taddr + (uint32_t)c, v);
@@ -897,6 +898,31 @@ bool use_weight_form(int tokens, int n, int sms) {
     return ceil_div(tokens, 2 * BM) * ceil_div(n, kPairBN) * 4 < sms;
 }
 
+// Output columns of a CTA-pair tile: the width in [128, 256] (a multiple of 16) whose tiles
+// fill the pairs' waves best, by a model of the time (waves, rounded up) x (width + 16):
+// the width stands for the MMA time of a tile, the 16 for the fixed cost of its A block
+// and epilogue.  A 2048-token 7B layer then takes 224 (QKV, O, down: 5.8 and 2.0 waves
+// instead of 5.05 and 1.7 at 256) and 240 (gate/up: 9.7 waves instead of 9.05).
+// Measured on GB300 that layer's four GEMMs went only from 590 to 586 us: a pair streams
+// its operands from L2 at about 11 TB/s over the grid, and narrower tiles re-read the
+// token block more often, which takes back most of what the fuller waves give.  Small
+// shapes gain the most (a 300-token call spreads over twice the pairs).
+int pair_tile_n(int tokens, int n, int sms) {
+    const int pairs = std::max(1, sms / 2);
+    const long long mt = ceil_div(tokens, 2 * BM);
+    int best = kPairBN;
+    long long best_cost = -1;
+    for (int bn = kPairBN; bn >= 128; bn -= 16) {
+        const long long waves = (mt * ceil_div(n, bn) + pairs - 1) / pairs;
+        const long long cost = waves * (bn + 16);
+        if (best_cost < 0 || cost < best_cost) {
+            best_cost = cost;
+            best = bn;
+        }
+    }
+    return best;
+}
+
 Plan make_plan(int tokens, int n, int k, int sms) {
     Plan p{};
     p.swap = use_weight_form(tokens, n, sms);
@@ -1030,17 +1056,18 @@ cudaError_t launch_gemm(const GemmProblem& pr, cudaStream_t stream) {
     if (!p.swap) {
         // CTA pairs: 256 x 256 tiles, each CTA stages 128 rows of A and of B per stage
         a.tiles_m = ceil_div(pr.tokens, 2 * BM);
-        a.tiles_n = ceil_div(pr.n, kPairBN);
-        a.bn = kPairBN;
+        a.bn = pair_tile_n(pr.tokens, pr.n, sms);
+        a.tiles_n = ceil_div(pr.n, a.bn);
         a.units = a.tiles_m * a.tiles_n;
-        a.stage_bytes = 2u * BM * BK * 2;
+        a.stage_bytes = (uint32_t)(BM + a.bn / 2) * BK * 2;
         a.stages = std::min(MAX_STAGES, (int)((227 * 1024 - 2048) / a.stage_bytes));
         // two 256-column accumulators per CTA (the epilogue of one tile overlaps the main
         // loop of the next); tcgen05.alloc.cta_group::2 is one allocation made jointly by
         // the pair, at the same TMEM address in both CTAs
         a.tmem_cols = 512;
         CUtensorMap tA2, tB2;
-        if (!make_tmap(&tA2, pr.act, pr.k, pr.tokens, BM) || !make_tmap(&tB2, pr.w, pr.k, pr.n, BM))
+        if (!make_tmap(&tA2, pr.act, pr.k, pr.tokens, BM) ||
+            !make_tmap(&tB2, pr.w, pr.k, pr.n, (uint32_t)(a.bn / 2)))
             return cudaErrorInvalidValue;
         const size_t smem = (size_t)a.stages * a.stage_bytes + 1024;
         {
