@@ -49,20 +49,20 @@ L2_FLUSH_BYTES = 256 << 20
 NCU_TRAFFIC = {
     # gemm_token2_kernel (CTA pairs), 7B prefill layer: mean over its 4 launches (QKV, O, gate/up, down)
     "prefill_gemm": {"file": "transformer_decoder_layer_llama_gb300/csrc/gemm_tc.cu",
-                     "sha256": "9e702575ebb3cd4534ca3821d5aa30f491fe9685ebf4c5eff2f7374e8b5fec5f", "bytes_per_launch": 168.2e6},
+                     "sha256": "ca2eb5d891b88f200b2be7981feba0b9d8594ce7dc6654cf3e6eece5a26c217d", "bytes_per_launch": 169.3e6},
     # attn_decode_split_kernel, 7B decode (batch 64)
     "llama2_7b_decode_attn": {"file": "transformer_decoder_layer_llama_gb300/csrc/attn.cu",
-                              "sha256": "a43aeff2b5f54595a8119e2904dbc0a7e3bba36fe8d4591225fcd4cfe70edb26", "bytes_per_launch": 2245.3e6},
+                              "sha256": "a2726665bda63d9f93ea3a227a942f2436089903af09dc3aeb16d2a477b2a727", "bytes_per_launch": 2248.4e6},
     # one weight-form GEMM (gemm_weight_kernel + gemm_weight_fixup_kernel), 70B decode:
     # mean over the layer's 4 GEMMs
     "llama70b_gqa_decode_gemm": {"file": "transformer_decoder_layer_llama_gb300/csrc/gemm_tc.cu",
-                                 "sha256": "9e702575ebb3cd4534ca3821d5aa30f491fe9685ebf4c5eff2f7374e8b5fec5f", "bytes_per_launch": 433.3e6},
+                                 "sha256": "ca2eb5d891b88f200b2be7981feba0b9d8594ce7dc6654cf3e6eece5a26c217d", "bytes_per_launch": 433.8e6},
     # attn_decode_split_q8_kernel, 7B decode over an INT8 cache (batch 64)
     "llama2_7b_decode_int8kv_attn": {"file": "transformer_decoder_layer_llama_gb300/csrc/attn.cu",
-                                     "sha256": "a43aeff2b5f54595a8119e2904dbc0a7e3bba36fe8d4591225fcd4cfe70edb26", "bytes_per_launch": 1159.4e6},
+                                     "sha256": "a2726665bda63d9f93ea3a227a942f2436089903af09dc3aeb16d2a477b2a727", "bytes_per_launch": 1168.3e6},
     # one weight-form GEMM, 70B decode over an INT8 cache: mean over the layer's 4 GEMMs
     "llama70b_gqa_decode_int8kv_gemm": {"file": "transformer_decoder_layer_llama_gb300/csrc/gemm_tc.cu",
-                                        "sha256": "9e702575ebb3cd4534ca3821d5aa30f491fe9685ebf4c5eff2f7374e8b5fec5f", "bytes_per_launch": 433.1e6},
+                                        "sha256": "ca2eb5d891b88f200b2be7981feba0b9d8594ce7dc6654cf3e6eece5a26c217d", "bytes_per_launch": 433.8e6},
 }
 
 
@@ -440,6 +440,30 @@ def continuous_batching(api, wl, steps, warmup, stream, peaks, seed=4321, world=
     return out
 
 
+def rounded(xs, nd=4):
+    return None if xs is None else [round(x, nd) for x in xs]
+
+
+def compact_kernels(per, n):
+    """{kernel: [launches per step, ms per step]} from a traced breakdown over n steps."""
+    return {k: [v["launches"] // n, round(v["ms"] / n, 4)] for k, v in per.items() if isinstance(v, dict)}
+
+
+def summary_text(line):
+    """Every workload's time per step and roofline fraction in one short string."""
+    parts = [f"7B prefill {line['ms_per_step']:.3f} ms ({line['value']:.0f} TFLOP/s, "
+             f"{line['layer_roofline_frac']:.2f} of roofline)"]
+    for name, v in line.get("decode", {}).items():
+        parts.append(f"{name} {v['ms_per_step']:.3f} ms ({v['layer_roofline_frac']:.2f})")
+    cb = line.get("continuous_batching")
+    if cb:
+        parts.append(f"32-layer batching {cb['ms_total'] / cb['steps']:.2f} ms/step "
+                     f"({cb['decode_tok_per_s']:.0f} decode tok/s, {cb['roofline_frac']:.2f})")
+    if "cpu_baseline" in line:
+        parts.append(f"oracle {line['cpu_baseline']['value']:.3f} TFLOP/s on {line['cpu_baseline']['cores']} cores")
+    return "; ".join(parts)
+
+
 def timed_steps(work, steps, stream, flush):
     """Device time of `steps` steps, each bracketed by its own events, L2 flushed between."""
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
@@ -667,12 +691,11 @@ def main():
         "e2e": {"value": job_throughput(world, work.flops, e2e_ms) / 1e12, "unit": "TFLOP/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": y_h.numel() * 2},
         "gpu_launches": launches_per_step * args.steps,
-        "kernels": {k: {"launches_per_step": v["launches"] // n_tr, "ms_per_step": v["ms"] / n_tr,
-                        "share": v["share"]} for k, v in per.items() if isinstance(v, dict)},
-        "gemm_ms_qkv_o_gu_down": per.get("gemm_by_position_ms"),
+        "kernels": compact_kernels(per, n_tr),
+        "gemm_ms_qkv_o_gu_down": rounded(per.get("gemm_by_position_ms")),
         "clocks": clocks.summary(),
         "device_status": st,
-        "peaks": peaks,
+        "peaks": {k: peaks[k] for k in ("hbm_gbs", "bf16_tflops", "source") if k in peaks},
     }
     del work
     torch.cuda.empty_cache()
@@ -698,10 +721,11 @@ def main():
             dom = "attn_decode" if att_ms >= gem_ms else "gemm_tc"
             dom_bytes = dw.kv_read if dom == "attn_decode" else weight_bytes(dw.d)
             dom_ms = att_ms if dom == "attn_decode" else gem_ms
+            cs = ck2.summary()
             extras[name] = {
+                "ms_per_step": ms2,
                 "tok_per_s": job_throughput(world, dw.B, ms2),
                 "hbm_gbs": job_throughput(world, dw.min_bytes, ms2) / 1e9,
-                "ms_per_step": ms2,
                 "layer_roofline_frac": dw.roofline_s(peaks) / (ms2 * 1e-3),
                 "min_bytes_per_step": dw.min_bytes,
                 "roofline": {"bound": "hbm", "kernel": dom,
@@ -709,10 +733,9 @@ def main():
                              "peak": peaks["hbm_gbs"], "unit": "GB/s",
                              "frac": (dom_bytes / (dom_ms * 1e-3) / 1e9) / peaks["hbm_gbs"] if dom_ms else 0.0,
                              "traffic": ncu_traffic(f"{name}_{'attn' if dom == 'attn_decode' else 'gemm'}")},
-                "kernels": {k: {"launches_per_step": v["launches"] // n2, "ms_per_step": v["ms"] / n2,
-                                "share": v["share"]} for k, v in per2.items() if isinstance(v, dict)},
-                "gemm_ms_qkv_o_gu_down": per2.get("gemm_by_position_ms"),
-                "clocks": ck2.summary(),
+                "kernels": compact_kernels(per2, n2),
+                "gemm_ms_qkv_o_gu_down": rounded(per2.get("gemm_by_position_ms")),
+                "clocks": {"sm_mhz": cs.get("sm_mhz"), "reasons": cs.get("reasons")},
                 "device_status": int(dw.status.item()),
             }
             del dw
@@ -727,6 +750,7 @@ def main():
         v, n, desc = OracleSample(wl).run(64, budget_s=12.0)
         line["cpu_baseline"] = {"value": v, "unit": "TFLOP/s", "cores": host_cores(),
                                 "kind": "oracle", "sample": desc}
+    line["summary"] = summary_text(line)      # last, so that a cut-off copy of the line keeps it
     if rank == 0:
         print(json.dumps(line))
     if world > 1:
