@@ -59,6 +59,7 @@ struct GemmArgs {
     uint32_t stage_bytes;
     uint32_t a_bytes;
     uint32_t tmem_cols;
+    int kbs;                 // token form: 64-wide K blocks per stage
     int w_prefetch;          // weight form: weights may be loaded before the grid dependency wait
     float* partials;         // weight form: [CTAs][2][tokens][128] float32 partial tiles
 };
@@ -357,7 +358,17 @@ LL_DEVINL void epi_weight_chunk(const EpiParams& ep, int n, int N, int t0, int T
 // which relieves shared memory.  Both CTAs' TMA loads complete the even CTA's full
 // barrier; the MMA commits arrive on both CTAs' barriers (multicast); both CTAs'
 // epilogue threads release the even CTA's accumulator barrier.
+//
+// A stage holds two k-blocks (three stages of 60 KB instead of seven of 30 KB): the
+// one thread that issues the MMAs then waits on a barrier once per 8 MMAs instead of
+// once per 4, and the tensor pipe no longer idles behind those waits (measured on
+// GB300, the 7B prefill layer's four GEMMs: 585 -> 508 us; the same pipeline with no
+// operand loads at all ran 535 us with one k-block per stage, so the waits and not the
+// operand traffic were the limit; three k-blocks per stage leave two stages and are
+// slower).  The per-stage loops are unrolled: a rolled loop over one k-block per stage
+// put enough instructions between the MMAs to cost 20%.
 constexpr int kPairBN = 256;      // the widest tile; each of the two TMEM accumulators starts a multiple of it apart
+constexpr int kPairKbs = 2;       // 64-wide K blocks per stage
 
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_token2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -406,6 +417,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     pdl_trigger();
     const uint32_t tmem = tmem_base_s;
     const uint32_t half_bytes = (uint32_t)BM * BK * 2;     // 16 KB: this CTA's A rows (its B rows follow)
+    const uint32_t sub_bytes = half_bytes + (uint32_t)(a.bn >> 1) * BK * 2;   // one K block of A and B
 
     if (warp == 0) {
         if (lane == 0) {
@@ -416,18 +428,24 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool ok = true;
             for (int u = pair; u < a.units && ok; u += num_pairs) {
                 const int m2 = u % a.tiles_m, nb = u / a.tiles_m;
-                for (int kb = 0; kb < a.num_kb; ++kb) {
+                for (int kb0 = 0; kb0 < a.num_kb; kb0 += a.kbs) {
+                    const int cnt = min(a.kbs, a.num_kb - kb0);
                     if (!mbar_wait_bounded(&empty_bar[stage], phase ^ 1, &abort_s, status)) {
                         ok = false;
                         break;
                     }
-                    uint8_t* sa = smem + (size_t)stage * a.stage_bytes;
-                    uint8_t* sb = sa + half_bytes;
                     // both CTAs' loads of this stage complete the even CTA's full barrier
-                    if (leader) mbar_arrive_expect_tx(&full_bar[stage], 2u * a.stage_bytes);
+                    if (leader) mbar_arrive_expect_tx(&full_bar[stage], 2u * (uint32_t)cnt * sub_bytes);
                     const uint32_t fb = cluster_map(smem_u32(&full_bar[stage]), 0);
-                    tma_load_2d_pair(sa, &tmA, kb * BK, m2 * 256 + (int)rank * BM, fb);
-                    tma_load_2d_pair(sb, &tmB, kb * BK, nb * a.bn + (int)rank * (a.bn >> 1), fb);
+#pragma unroll
+                    for (int j = 0; j < kPairKbs; ++j) {
+                        if (j < cnt) {
+                            uint8_t* sa = smem + (size_t)stage * a.stage_bytes + (size_t)j * sub_bytes;
+                            tma_load_2d_pair(sa, &tmA, (kb0 + j) * BK, m2 * 256 + (int)rank * BM, fb);
+                            tma_load_2d_pair(sa + half_bytes, &tmB, (kb0 + j) * BK,
+                                             nb * a.bn + (int)rank * (a.bn >> 1), fb);
+                        }
+                    }
                     for (int s = 0; s < MAX_STAGES; ++s) issued[s] += (s == stage);
                     if (++stage == a.stages) {
                         stage = 0;
@@ -456,19 +474,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!mbar_wait_bounded(&tempty_bar[buf], accp ^ 1, &abort_s, status)) break;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem + (uint32_t)(buf * kPairBN);
-                for (int kb = 0; kb < a.num_kb; ++kb) {
+                for (int kb0 = 0; kb0 < a.num_kb; kb0 += a.kbs) {
+                    const int cnt = min(a.kbs, a.num_kb - kb0);
                     if (!mbar_wait_bounded(&full_bar[stage], phase, &abort_s, status)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t sa = smem_u32(smem + (size_t)stage * a.stage_bytes);
-                    const uint64_t da = umma_desc_sw128(sa);
-                    const uint64_t db = umma_desc_sw128(sa + half_bytes);
 #pragma unroll
-                    for (int kk = 0; kk < BK / UK; ++kk)
-                        tc_mma_bf16_pair(d_tmem, da + (uint64_t)(kk * 2), db + (uint64_t)(kk * 2), idesc,
-                                         (kb > 0 || kk > 0) ? 1u : 0u);
+                    for (int j = 0; j < kPairKbs; ++j) {
+                        if (j < cnt) {
+                            const uint32_t sa = smem_u32(smem + (size_t)stage * a.stage_bytes) + (uint32_t)j * sub_bytes;
+                            const uint64_t da = umma_desc_sw128(sa);
+                            const uint64_t db = umma_desc_sw128(sa + half_bytes);
+#pragma unroll
+                            for (int kk = 0; kk < BK / UK; ++kk)
+                                tc_mma_bf16_pair(d_tmem, da + (uint64_t)(kk * 2), db + (uint64_t)(kk * 2), idesc,
+                                                 (kb0 + j > 0 || kk > 0) ? 1u : 0u);
+                        }
+                    }
                     tc_commit_pair_mc(&empty_bar[stage], 0x3);
                     if (++stage == a.stages) {
                         stage = 0;
@@ -1059,7 +1083,8 @@ cudaError_t launch_gemm(const GemmProblem& pr, cudaStream_t stream) {
         a.bn = pair_tile_n(pr.tokens, pr.n, sms);
         a.tiles_n = ceil_div(pr.n, a.bn);
         a.units = a.tiles_m * a.tiles_n;
-        a.stage_bytes = (uint32_t)(BM + a.bn / 2) * BK * 2;
+        a.kbs = kPairKbs;   // the kernel's loops are unrolled for this many
+        a.stage_bytes = (uint32_t)a.kbs * (uint32_t)(BM + a.bn / 2) * BK * 2;
         a.stages = std::min(MAX_STAGES, (int)((227 * 1024 - 2048) / a.stage_bytes));
         // two 256-column accumulators per CTA (the epilogue of one tile overlaps the main
         // loop of the next); tcgen05.alloc.cta_group::2 is one allocation made jointly by
