@@ -358,6 +358,15 @@ LL_DEVINL void mbar_arrive_cluster(uint32_t cluster_addr) {
                  : "memory");
 }
 
+// Arrival that orders none of this thread's earlier memory accesses: for a thread whose
+// only hazard with the waiter is on data it has already consumed (an accumulator read
+// out of TMEM, its tcgen05.wait::ld done).  A release arrive at cluster scope would
+// first wait for the thread's outstanding global stores.
+LL_DEVINL void mbar_arrive_cluster_relaxed(uint32_t cluster_addr) {
+    asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+                 : "memory");
+}
+
 LL_DEVINL void tmem_alloc_pair(uint32_t* dst_smem, uint32_t ncols) {
     asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                      smem_u32(dst_smem)),

@@ -59,7 +59,6 @@ struct GemmArgs {
     uint32_t stage_bytes;
     uint32_t a_bytes;
     uint32_t tmem_cols;
-    int kbs;                 // token form: 64-wide K blocks per stage
     int w_prefetch;          // weight form: weights may be loaded before the grid dependency wait
     float* partials;         // weight form: [CTAs][2][tokens][128] float32 partial tiles
 };
@@ -428,8 +427,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool ok = true;
             for (int u = pair; u < a.units && ok; u += num_pairs) {
                 const int m2 = u % a.tiles_m, nb = u / a.tiles_m;
-                for (int kb0 = 0; kb0 < a.num_kb; kb0 += a.kbs) {
-                    const int cnt = min(a.kbs, a.num_kb - kb0);
+                for (int kb0 = 0; kb0 < a.num_kb; kb0 += kPairKbs) {
+                    const int cnt = min(kPairKbs, a.num_kb - kb0);
                     if (!mbar_wait_bounded(&empty_bar[stage], phase ^ 1, &abort_s, status)) {
                         ok = false;
                         break;
@@ -468,14 +467,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             int local = 0;
             bool ok = true;
             const int nbuf = (int)(a.tmem_cols / kPairBN);   // two accumulators, at column 0 and 256
+            // operand descriptors: stage 0's, advanced by the stage size (start address in
+            // 16-byte units; every address stays below 256 KB, so no carry leaves the field)
+            const uint64_t desc0 = umma_desc_sw128(smem_u32(smem));
+            const uint64_t stage_step = a.stage_bytes >> 4, sub_step = sub_bytes >> 4, half_step = half_bytes >> 4;
+            uint64_t dstage = desc0;
             for (int u = pair; u < a.units && ok; u += num_pairs, ++local) {
                 const int buf = local % nbuf;
                 const uint32_t accp = (uint32_t)(local / nbuf) & 1;
                 if (!mbar_wait_bounded(&tempty_bar[buf], accp ^ 1, &abort_s, status)) break;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem + (uint32_t)(buf * kPairBN);
-                for (int kb0 = 0; kb0 < a.num_kb; kb0 += a.kbs) {
-                    const int cnt = min(a.kbs, a.num_kb - kb0);
+                uint32_t acc0 = 0;                       // the tile's first MMA overwrites
+                for (int kb0 = 0; kb0 < a.num_kb; kb0 += kPairKbs) {
+                    const int cnt = min(kPairKbs, a.num_kb - kb0);
                     if (!mbar_wait_bounded(&full_bar[stage], phase, &abort_s, status)) {
                         ok = false;
                         break;
@@ -484,19 +489,21 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int j = 0; j < kPairKbs; ++j) {
                         if (j < cnt) {
-                            const uint32_t sa = smem_u32(smem + (size_t)stage * a.stage_bytes) + (uint32_t)j * sub_bytes;
-                            const uint64_t da = umma_desc_sw128(sa);
-                            const uint64_t db = umma_desc_sw128(sa + half_bytes);
+                            const uint64_t da = dstage + (uint64_t)j * sub_step;
+                            const uint64_t db = da + half_step;
 #pragma unroll
                             for (int kk = 0; kk < BK / UK; ++kk)
                                 tc_mma_bf16_pair(d_tmem, da + (uint64_t)(kk * 2), db + (uint64_t)(kk * 2), idesc,
-                                                 (kb0 + j > 0 || kk > 0) ? 1u : 0u);
+                                                 (j == 0 && kk == 0) ? acc0 : 1u);
                         }
                     }
+                    acc0 = 1;
                     tc_commit_pair_mc(&empty_bar[stage], 0x3);
+                    dstage += stage_step;
                     if (++stage == a.stages) {
                         stage = 0;
                         phase ^= 1;
+                        dstage = desc0;
                     }
                 }
                 if (ok) tc_commit_pair_mc(&tfull_bar[buf], 0x3);
@@ -531,7 +538,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 epi_token_chunk(a.ep, t, row_ok, n0, a.n, ts, v);
             }
             tc_fence_before();
-            mbar_arrive_cluster(cluster_map(smem_u32(&tempty_bar[buf]), 0));
+            // the accumulator is in registers (wait::ld done): release it without waiting
+            // for this tile's output stores
+            mbar_arrive_cluster_relaxed(cluster_map(smem_u32(&tempty_bar[buf]), 0));
         }
     }
 
@@ -1083,8 +1092,7 @@ cudaError_t launch_gemm(const GemmProblem& pr, cudaStream_t stream) {
         a.bn = pair_tile_n(pr.tokens, pr.n, sms);
         a.tiles_n = ceil_div(pr.n, a.bn);
         a.units = a.tiles_m * a.tiles_n;
-        a.kbs = kPairKbs;   // the kernel's loops are unrolled for this many
-        a.stage_bytes = (uint32_t)a.kbs * (uint32_t)(BM + a.bn / 2) * BK * 2;
+        a.stage_bytes = (uint32_t)kPairKbs * (uint32_t)(BM + a.bn / 2) * BK * 2;
         a.stages = std::min(MAX_STAGES, (int)((227 * 1024 - 2048) / a.stage_bytes));
         // two 256-column accumulators per CTA (the epilogue of one tile overlaps the main
         // loop of the next); tcgen05.alloc.cta_group::2 is one allocation made jointly by
