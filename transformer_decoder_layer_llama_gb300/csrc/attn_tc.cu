@@ -12,8 +12,9 @@
 //  * warp 0, one lane: TMA.  Q once (two 64-column boxes), then per key tile K
 //    and V as boxes of min(block_size, 128) rows x 64 columns at the physical
 //    block's rows, each double-buffered, K loaded one tile ahead of V.
-//  * warp 1, one lane: tcgen05.mma.  S_j = Q K_j^T (M 128, N 128, K = head_dim)
-//    into TMEM buffer j & 1; once the softmax has replaced S_j by P_j in that
+//  * warp 1, one lane: tcgen05.mma.  S_j = Q K_j^T (M 128, N 128, K = head_dim,
+//    Q as an A operand in TMEM: the softmax warps copy it there from the TMA tile
+//    once) into TMEM buffer j & 1; once the softmax has replaced S_j by P_j in that
 //    buffer, O += P_j V_j with P as the A operand read from TMEM (two BF16 parts
 //    hi + lo, two MMAs per 16 keys) and V an MN-major operand straight from the
 //    TMA tile.  O accumulates in TMEM over all key tiles.
@@ -51,6 +52,7 @@ struct TcLayout {
     static constexpr uint32_t OFF_V = OFF_K + 2 * KV_BYTES; // 2 stages
     static constexpr uint32_t TOTAL = OFF_V + 2 * KV_BYTES;
     static constexpr uint32_t TMEM_S0 = 0, TMEM_S1 = 128, TMEM_O = 256;
+    static constexpr uint32_t TMEM_Q = 384;   // Q as the A operand of S: D / 2 columns, two BF16 per column
     static constexpr uint32_t TMEM_COLS = 512;
 };
 
@@ -98,7 +100,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~uintptr_t(1023));
     __shared__ uint64_t q_full, k_full[2], k_empty[2], v_full[2], v_empty[2];
-    __shared__ uint64_t s_full[2], p_full, pv_done[2], drain;
+    __shared__ uint64_t s_full[2], p_full, pv_done[2], drain, q_tmem;
     __shared__ uint32_t tmem_base_s;
     __shared__ int abort_s;
     __shared__ int max_pos_s;
@@ -130,6 +132,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             mbar_init(&pv_done[i], 1);
         }
         mbar_init(&p_full, 256);
+        mbar_init(&q_tmem, 256);
         mbar_init(&drain, 1);
         abort_s = 0;
         max_pos_s = -1;
@@ -234,8 +237,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             // ------------------------------------------------ MMA issuer
             const uint32_t id_s = umma_idesc_bf16(kQT, kKT);
             const uint32_t id_o = idesc_bf16_bmn(kQT, D);
-            const uint32_t sq = smem_u32(smem + L::OFF_Q);
-            bool ok = mbar_wait_bounded(&q_full, 0, &abort_s, status);
+            // Q sits in TMEM once the softmax warps have copied it there (S from an A operand
+            // in TMEM: measured on GB300, M128 N128 MMAs with both operands in shared memory
+            // take up to twice as long as with A in TMEM)
+            bool ok = mbar_wait_bounded(&q_tmem, 0, &abort_s, status);
+            tc_fence_after();
             // S_j = Q K_j^T into TMEM buffer j & 1 (after P_{j-2} V_{j-2} has read it)
             auto issue_s = [&](int j) -> bool {
                 const int st = j & 1;
@@ -247,10 +253,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 const uint32_t d_s = tmem + (st ? L::TMEM_S1 : L::TMEM_S0);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (uint32_t)(kk >> 2) * (kQT * 128) + (uint32_t)(kk & 3) * 32;
                     const uint32_t offk = (uint32_t)(kk >> 2) * (kKT * 128) + (uint32_t)(kk & 3) * 32;
-                    tc_mma_bf16(d_s, umma_desc_sw128(sq + off), umma_desc_sw128(sk + offk), id_s,
-                                kk > 0 ? 1u : 0u);
+                    tc_mma_bf16_ts(d_s, tmem + L::TMEM_Q + (uint32_t)kk * 8u, umma_desc_sw128(sk + offk), id_s,
+                                   kk > 0 ? 1u : 0u);
                 }
                 tc_commit(&s_full[st]);
                 tc_commit(&k_empty[st]);
@@ -299,6 +304,30 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const float sl2 = a.scale * kLog2eTc;
         float m_used = -INFINITY, l = 0.f;
         bool ok = true;
+        if (n_kt > 0) {
+            // this thread's half of Q row r into TMEM (column c holds elements 2c, 2c + 1),
+            // read from the 128-byte-swizzled TMA tile [D / 64][128 rows][128 B]
+            const bool got_q = __all_sync(0xffffffffu, mbar_wait_bounded(&q_full, 0, &abort_s, status));
+#pragma unroll
+            for (int g = 0; g < HD / 32; ++g) {       // 32 elements (16 columns) at a time
+                uint32_t w[16];
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const int e = half * HD + g * 32 + c * 8;   // first element of the 16-byte chunk
+                    uint4 x = make_uint4(0u, 0u, 0u, 0u);
+                    if (got_q)
+                        x = *reinterpret_cast<const uint4*>(smem + L::OFF_Q + (e >> 6) * (kQT * 128) + r * 128 +
+                                                            ((((e & 63) >> 3) ^ (r & 7)) << 4));
+                    w[4 * c] = x.x;
+                    w[4 * c + 1] = x.y;
+                    w[4 * c + 2] = x.z;
+                    w[4 * c + 3] = x.w;
+                }
+                tmem_st16(tmem + lane_base + L::TMEM_Q + (uint32_t)(half * HD / 2 + g * 16), w);
+            }
+            tc_fence_before();
+            mbar_arrive(&q_tmem);
+        }
         for (int j = 0; j < n_kt && ok; ++j) {
             const int st = j & 1;
             const uint32_t ph = (uint32_t)(j >> 1) & 1u;
