@@ -29,6 +29,7 @@ DEV = "cuda"
     (65, 256, 128), (128, 512, 256), (300, 1376, 688), (2048, 4096, 4096), (257, 12288, 4096),
     (5, 12304, 512), (16, 38912, 256),                   # weight form, several tiles per CTA: split, whole
     (16, 40144, 256), (3, 24400, 320),                   # ... a ragged last tile (80 and 80 rows)
+    (520, 2048, 1040), (257, 640, 80),                   # CTA pairs: 17 K blocks (a half last stage), a ragged K block
 ])
 def test_linear_matches_float64_matmul(m, n, k):
     x = synth.normal_bf16((m, k), 1.0, seed=m * 7 + 1, tag="x")
