@@ -171,9 +171,6 @@ LL_DEVINL void prefetch_l2(const void* p) {
     asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<uint64_t>(p)));
 }
 
-// Orders this thread's generic-proxy global accesses with its async-proxy ones
-// (bulk copies) in both directions.
-LL_DEVINL void fence_proxy_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
 
 LL_DEVINL void tma_load_2d_hint(void* smem_dst, const void* tmap, int32_t c0, int32_t c1,
                                 uint64_t* bar, uint64_t policy) {
@@ -190,11 +187,6 @@ LL_DEVINL uint64_t l2_policy_evict_first() {
     return p;
 }
 
-LL_DEVINL uint64_t l2_policy_evict_last() {
-    uint64_t p;
-    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
-    return p;
-}
 
 // ---------------------------------------------------------------- tcgen05
 
@@ -353,11 +345,6 @@ LL_DEVINL uint32_t cluster_map(uint32_t smem_addr, uint32_t rank) {
     return r;
 }
 
-LL_DEVINL void mbar_arrive_cluster(uint32_t cluster_addr) {
-    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
-                 : "memory");
-}
-
 // Arrival that orders none of this thread's earlier memory accesses: for a thread whose
 // only hazard with the waiter is on data it has already consumed (an accumulator read
 // out of TMEM, its tcgen05.wait::ld done).  A release arrive at cluster scope would
@@ -402,7 +389,6 @@ LL_DEVINL void tc_commit_pair_mc(uint64_t* bar, uint16_t cta_mask) {
         : "memory");
 }
 
-LL_DEVINL void tc_fence_before_pair() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 
 // 2-D tiled TMA load into this CTA's shared memory whose completion is counted on
 // an mbarrier that may sit in the peer CTA (cluster address)
