@@ -178,7 +178,7 @@ def test_tiny_layer_prefill_then_decode_steps():
         assert_close(f64(yd), yd_ref, f"decode step {step}")
 
 
-@pytest.mark.parametrize("B,S", [(3, 17), (1, 130), (2, 1), (1, 200)])
+@pytest.mark.parametrize("B,S", [(3, 17), (1, 130), (2, 1), (1, 200), (2, 300)])
 def test_tiny_layer_ragged_prefill(B, S):
     wl, d, B, S, W, Wn, table, kp, vp, cfg, packed = _tiny_setup(seed=5, S=S, B=B, steps=0)
     x = synth.make_x(B * S, d.hidden, seed=31)
