@@ -355,6 +355,14 @@ int ll_selftest_bounded_wait(int32_t limit_us, int32_t* status, int32_t* out, vo
  * (queried once per device), or -1 without a device. */
 int ll_device_sm_count(void);
 
+/* Upper bound on the CTAs of the prefill attention, which is persistent: each
+ * CTA (one per SM by default) runs a fixed list of (sequence, query head,
+ * 128-query tile) items back to back.  n <= 0 restores one per SM.  A smaller
+ * bound leaves SMs to other work on the device, and lets small problems run
+ * several items per CTA.  Applies to launches made after the call, from any
+ * thread.  Always returns LL_OK. */
+int ll_set_prefill_attention_ctas(int32_t n);
+
 #ifdef __cplusplus
 }
 #endif

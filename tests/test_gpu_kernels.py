@@ -191,6 +191,51 @@ def test_tiny_layer_ragged_prefill(B, S):
     assert_close(f64(y), y_ref, f"prefill B{B} S{S}")
 
 
+@pytest.mark.parametrize("head_dim", [64, 128])
+@pytest.mark.parametrize("ctas", [1, 3, 7])
+def test_prefill_attention_several_items_per_cta(head_dim, ctas):
+    """The persistent prefill attention with its CTAs capped, so that each runs several
+    (sequence, head, query tile) items back to back: ragged last query tiles, a chunk
+    appended after a cached prefix (items of one and two key tiles with rows to mask).
+    Against the oracle, and bit for bit against the default one-CTA-per-SM launch."""
+    d = synth.DIMS_TINY if head_dim == 64 else synth.LayerDims(512, 4, 2, 128, 1024, 16)
+    B, S, extra = 3, 300, 70
+    W = synth.make_weights(d, 0.02, seed=131)
+    Wn = {k: f64(v) for k, v in W.items()}
+    table, nb = synth.make_block_table([S + extra] * B, d.block_size, seed=132, extra_blocks=3)
+    kp, vp = synth.make_pool(nb, d, seed=133, fill="sentinel")
+    cfg = api.make_config(d, max_position=S + extra + 1)
+    packed = api.pack_weights(cfg, {k: v.to(DEV) for k, v in W.items()})
+    td = table.to(DEV)
+
+    def run(cap):
+        kpd, vpd = kp.to(DEV), vp.to(DEV)
+        status = api.new_status()
+        api.set_prefill_attention_ctas(cap)
+        try:
+            ys = []
+            for start, n, seed in ((0, S, 134), (S, extra, 135)):
+                x = synth.make_x(B * n, d.hidden, seed=seed)
+                pos = synth.prefill_positions(B, n, start=start)
+                ys.append(api.layer_prefill(cfg, packed, x.to(DEV), pos.to(DEV), B, n, kpd, vpd, td,
+                                            status=status))
+            torch.cuda.synchronize()
+        finally:
+            api.set_prefill_attention_ctas(0)
+        assert int(status.item()) == 0
+        return ys
+
+    got, full = run(ctas), run(0)
+    for g_, f_ in zip(got, full):
+        assert torch.equal(g_, f_), "the result depends on how items are spread over CTAs"
+    ko, vo = bits(kp), bits(vp)
+    for (start, n, seed), y in zip(((0, S, 134), (S, extra, 135)), got):
+        x = synth.make_x(B * n, d.hidden, seed=seed)
+        pos = synth.prefill_positions(B, n, start=start)
+        y_ref = O.layer_prefill(d, Wn, f64(x), pos.numpy(), B, n, ko, vo, table.numpy())
+        assert_close(f64(y), y_ref, f"prefill from {start}, {n} tokens, {ctas} CTAs")
+
+
 def test_chunked_prefill_attends_to_cached_prefix():
     wl, d, B, S, W, Wn, table, kp, vp, cfg, packed = _tiny_setup(seed=7, S=64, B=2, steps=40)
     kpd, vpd, td = kp.to(DEV), vp.to(DEV), table.to(DEV)

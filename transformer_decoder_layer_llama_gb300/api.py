@@ -36,7 +36,7 @@ EXPORTED = [
     "ll_trace_name", "ll_paged_attention_decode_noalloc", "ll_selftest_bounded_wait",
     "ll_workspace_checkpoints", "ll_reshape_and_cache_q8", "ll_paged_attention_decode_q8",
     "ll_layer_decode_step_q8", "ll_workspace_size_mode", "ll_workspace_step_checkpoints",
-    "ll_layer_prefill_mode", "ll_layer_decode_step_mode",
+    "ll_layer_prefill_mode", "ll_layer_decode_step_mode", "ll_set_prefill_attention_ctas",
 ]
 
 
@@ -97,6 +97,7 @@ def _load():
         "ll_linear_workspace_size": (S, [I32, I32, I32]),
         "ll_linear": (ctypes.c_int, [P, P, P, I32, I32, I32, P, S, P, P]),
         "ll_device_sm_count": (ctypes.c_int, []),
+        "ll_set_prefill_attention_ctas": (ctypes.c_int, [I32]),
         "ll_trace_begin": (ctypes.c_int, [I32]),
         "ll_trace_end": (I32, []),
         "ll_trace_elapsed_ms": (ctypes.c_float, [I32]),
@@ -467,6 +468,12 @@ def paged_attention_decode_noalloc(q, k_pool, v_pool, block_table, context_lens,
         Hq, k_pool.shape[1], d, k_pool.shape[2], float(scale), _ptr(out), _ptr(status),
         _stream(stream)))
     return out
+
+
+def set_prefill_attention_ctas(n: int) -> None:
+    """ll_set_prefill_attention_ctas: bound on the persistent prefill attention's CTAs
+    (n <= 0: one per SM)."""
+    lib.ll_set_prefill_attention_ctas(int(n))
 
 
 def linear(x, w, y=None, workspace=None, status=None, stream=None):

@@ -570,6 +570,11 @@ const char* ll_strerror(int code) {
 
 int ll_device_sm_count(void) { return ll::device_sm_count(); }
 
+int ll_set_prefill_attention_ctas(int32_t n) {
+    ll::set_prefill_attention_ctas(n);
+    return LL_OK;
+}
+
 int ll_selftest_bounded_wait(int32_t limit_us, int32_t* status, int32_t* out, void* stream) {
     ll::clear_last_error();
     if (!status || !out || limit_us <= 0 || limit_us > 2000000) return LL_ERR_INVALID_ARG;

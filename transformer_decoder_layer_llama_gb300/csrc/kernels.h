@@ -157,6 +157,7 @@ struct AttnPrefillArgs {
     int32_t* status;
 };
 cudaError_t launch_attn_prefill_tc(const AttnPrefillArgs& a, cudaStream_t stream);
+void set_prefill_attention_ctas(int n);   // 0: one CTA per SM
 
 struct AttnDecodeArgs {
     const __nv_bfloat16* q;        // [batch, n_heads, d]
