@@ -236,6 +236,39 @@ def test_prefill_attention_several_items_per_cta(head_dim, ctas):
         assert_close(f64(y), y_ref, f"prefill from {start}, {n} tokens, {ctas} CTAs")
 
 
+@pytest.mark.parametrize("ctas", [1, 0])
+def test_prefill_attention_item_without_valid_positions(ctas):
+    """A sequence whose positions are all out of range gives work items with no key tile:
+    with one CTA they sit between the other sequences' items in its list.  The position
+    error is flagged, nothing waits out its limit, and the other sequences match the oracle."""
+    wl = synth.WORKLOADS["tiny_gqa"]
+    d = wl.dims
+    B, S = 3, 100
+    W = synth.make_weights(d, wl.w_std, seed=141)
+    Wn = {k: f64(v) for k, v in W.items()}
+    table, nb = synth.make_block_table([S] * B, d.block_size, seed=142, extra_blocks=3)
+    kp, vp = synth.make_pool(nb, d, seed=143, fill="sentinel")
+    cfg = api.make_config(d, max_position=S + 1)
+    packed = api.pack_weights(cfg, {k: v.to(DEV) for k, v in W.items()})
+    x = synth.make_x(B * S, d.hidden, seed=144)
+    pos = synth.prefill_positions(B, S)
+    pos[S:2 * S] = 10_000                      # sequence 1: beyond the cache and the RoPE table
+    status = api.new_status()
+    api.set_prefill_attention_ctas(ctas)
+    try:
+        y = api.layer_prefill(cfg, packed, x.to(DEV), pos.to(DEV), B, S, kp.to(DEV), vp.to(DEV),
+                              table.to(DEV), status=status)
+        torch.cuda.synchronize()
+    finally:
+        api.set_prefill_attention_ctas(0)
+    st = int(status.item())
+    assert st & api.LL_DEV_BAD_POSITION and not st & api.LL_DEV_TIMEOUT, st
+    keep = np.r_[0:S, 2 * S:3 * S]
+    ko, vo = bits(kp), bits(vp)
+    y_ref = O.layer_prefill(d, Wn, f64(x)[keep], pos.numpy()[keep], 2, S, ko, vo, table.numpy()[[0, 2]])
+    assert_close(f64(y)[keep], y_ref, "sequences 0 and 2")
+
+
 def test_chunked_prefill_attends_to_cached_prefix():
     wl, d, B, S, W, Wn, table, kp, vp, cfg, packed = _tiny_setup(seed=7, S=64, B=2, steps=40)
     kpd, vpd, td = kp.to(DEV), vp.to(DEV), table.to(DEV)
