@@ -269,6 +269,59 @@ def test_prefill_attention_item_without_valid_positions(ctas):
     assert_close(f64(y)[keep], y_ref, "sequences 0 and 2")
 
 
+@pytest.mark.parametrize("bs", [32, 64, 256])
+def test_prefill_attention_block_sizes(bs):
+    """Paged prefill attention with KV blocks of 32, 64 and 256 positions (a 256-position
+    block spans two 128-key tiles; smaller ones fill a tile from several boxes), with
+    the CTAs capped so that each runs several items.  Against the oracle."""
+    d = synth.LayerDims(256, 4, 2, 64, 688, bs)
+    B, S = 2, 300
+    W = synth.make_weights(d, 0.02, seed=151)
+    Wn = {k: f64(v) for k, v in W.items()}
+    table, nb = synth.make_block_table([S] * B, bs, seed=152, extra_blocks=2)
+    kp, vp = synth.make_pool(nb, d, seed=153, fill="sentinel")
+    cfg = api.make_config(d, max_position=S + 1)
+    packed = api.pack_weights(cfg, {k: v.to(DEV) for k, v in W.items()})
+    x = synth.make_x(B * S, d.hidden, seed=154)
+    pos = synth.prefill_positions(B, S)
+    status = api.new_status()
+    api.set_prefill_attention_ctas(5)
+    try:
+        y = api.layer_prefill(cfg, packed, x.to(DEV), pos.to(DEV), B, S, kp.to(DEV), vp.to(DEV),
+                              table.to(DEV), status=status)
+        torch.cuda.synchronize()
+    finally:
+        api.set_prefill_attention_ctas(0)
+    assert int(status.item()) == 0
+    ko, vo = bits(kp), bits(vp)
+    y_ref = O.layer_prefill(d, Wn, f64(x), pos.numpy(), B, S, ko, vo, table.numpy())
+    assert_close(f64(y), y_ref, f"prefill with {bs}-position blocks")
+
+
+def test_prefill_attention_long_cached_context():
+    """A 64-token chunk appended at positions 60000..60063 over a cached prefix of N(0, 1)
+    K/V: each work item runs 469 key tiles (the metadata warp marks 3752 valid 16-key
+    chunks per item).  Against the oracle."""
+    d = synth.DIMS_TINY
+    start, n = 60_000, 64
+    W = synth.make_weights(d, 0.02, seed=161)
+    Wn = {k: f64(v) for k, v in W.items()}
+    table, nb = synth.make_block_table([start + n], d.block_size, seed=162, extra_blocks=2)
+    kp, vp = synth.make_pool(nb, d, seed=163)
+    cfg = api.make_config(d, max_position=start + n + 1)
+    packed = api.pack_weights(cfg, {k: v.to(DEV) for k, v in W.items()})
+    x = synth.make_x(n, d.hidden, seed=164)
+    pos = synth.prefill_positions(1, n, start=start)
+    status = api.new_status()
+    y = api.layer_prefill(cfg, packed, x.to(DEV), pos.to(DEV), 1, n, kp.to(DEV), vp.to(DEV), table.to(DEV),
+                          status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    ko, vo = bits(kp), bits(vp)
+    y_ref = O.layer_prefill(d, Wn, f64(x), pos.numpy(), 1, n, ko, vo, table.numpy())
+    assert_close(f64(y), y_ref, "64 tokens after a 60000-position prefix")
+
+
 def test_chunked_prefill_attends_to_cached_prefix():
     wl, d, B, S, W, Wn, table, kp, vp, cfg, packed = _tiny_setup(seed=7, S=64, B=2, steps=40)
     kpd, vpd, td = kp.to(DEV), vp.to(DEV), table.to(DEV)
