@@ -91,6 +91,7 @@ def test_reshape_and_cache_flags_out_of_range_slot():
     (5, 8, 8, 128, 128, 1, 300),        # MHA, ragged
     (3, 16, 2, 128, 128, 900, 3100),    # GQA 8, several 1024-key splits
     (4, 4, 4, 64, 32, 1023, 1026),      # split boundaries
+    (2, 16, 1, 128, 128, 1, 700),       # GQA 16, one KV head
 ])
 def test_paged_attention_decode(B, Hq, Hkv, d, bs, ctx_lo, ctx_hi):
     dims = synth.LayerDims(Hq * d, Hq, Hkv, d, 64, bs)
@@ -267,6 +268,34 @@ def test_prefill_attention_item_without_valid_positions(ctas):
     ko, vo = bits(kp), bits(vp)
     y_ref = O.layer_prefill(d, Wn, f64(x)[keep], pos.numpy()[keep], 2, S, ko, vo, table.numpy()[[0, 2]])
     assert_close(f64(y)[keep], y_ref, "sequences 0 and 2")
+
+
+@pytest.mark.parametrize("Hq,Hkv", [(16, 2), (16, 1)])
+def test_prefill_attention_wide_query_groups(Hq, Hkv):
+    """Prefill layers whose KV heads serve 8 and 16 query heads (head_dim 128), with the
+    CTAs capped so that the query heads of one KV head share a CTA's item list."""
+    d = synth.LayerDims(Hq * 64, Hq, Hkv, 128, 512, 16)
+    B, S = 2, 200
+    W = synth.make_weights(d, 0.02, seed=171)
+    Wn = {k: f64(v) for k, v in W.items()}
+    table, nb = synth.make_block_table([S] * B, d.block_size, seed=172, extra_blocks=2)
+    kp, vp = synth.make_pool(nb, d, seed=173, fill="sentinel")
+    cfg = api.make_config(d, max_position=S + 1)
+    packed = api.pack_weights(cfg, {k: v.to(DEV) for k, v in W.items()})
+    x = synth.make_x(B * S, d.hidden, seed=174)
+    pos = synth.prefill_positions(B, S)
+    status = api.new_status()
+    api.set_prefill_attention_ctas(4)
+    try:
+        y = api.layer_prefill(cfg, packed, x.to(DEV), pos.to(DEV), B, S, kp.to(DEV), vp.to(DEV),
+                              table.to(DEV), status=status)
+        torch.cuda.synchronize()
+    finally:
+        api.set_prefill_attention_ctas(0)
+    assert int(status.item()) == 0
+    ko, vo = bits(kp), bits(vp)
+    y_ref = O.layer_prefill(d, Wn, f64(x), pos.numpy(), B, S, ko, vo, table.numpy())
+    assert_close(f64(y), y_ref, f"prefill, {Hq} query heads over {Hkv} KV heads")
 
 
 @pytest.mark.parametrize("bs", [32, 64, 256])
